@@ -1,0 +1,136 @@
+"""Float64 CPU oracle for speculative-decoding verification (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / reference leg may import this package.  It
+shares no code with the CUDA library; the C source states what each function
+computes and which passage of the pages it follows:
+
+* ``verify_attn`` / ``attn_rows`` -- multi-query causal attention of the k
+  draft queries over the paged cache ("Decoding Speculative Decoding from
+  First Principles", "Parallelizing method 2: sequence parallel"), with the
+  INT8 dequantiser that inverts CXL-SpecKV's "Algorithm 2 KV-Cache
+  Compression".
+* ``accept_greedy`` -- first-disagreement acceptance plus bonus token (same
+  blog, "Speculating to get sequence parallelism during decode").
+
+Arrays are numpy; 16-bit float types travel as their raw ``uint16`` bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+# The oracle's own element-type codes (mirrors the enum in spec_oracle.c only).
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2, "i8": 3}
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i32 = ctypes.c_int
+        attn_common = [P, i32, P, P, i32, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                       ctypes.c_double]
+        lib.oracle_verify_attn.argtypes = attn_common + [P, P]
+        lib.oracle_verify_attn.restype = i32
+        lib.oracle_attn_rows.argtypes = attn_common + [P, i32, P, P]
+        lib.oracle_attn_rows.restype = i32
+        lib.oracle_accept_greedy.argtypes = [P, i32, P, i32, i32, ctypes.c_int64, P, P, P]
+        lib.oracle_accept_greedy.restype = i32
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f64.restype = ctypes.c_double
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _attn_common(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_table,
+                 ctx_lens, scale):
+    B, k, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    assert block_table.dtype == np.int32 and ctx_lens.dtype == np.int32
+    if kv_dtype == "i8":
+        assert k_scale is not None and v_scale is not None
+        assert k_scale.dtype == np.uint16 and k_scale.shape == (NP, Hkv, P)
+    keep = (q, k_cache, v_cache, k_scale, v_scale, block_table, ctx_lens)
+    args = [_ptr(q), DTYPES[q_dtype], _ptr(k_cache), _ptr(v_cache), DTYPES[kv_dtype],
+            _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(ctx_lens),
+            B, k, Hq, Hkv, D, P, NP, block_table.shape[1], float(scale)]
+    return keep, args, (B, k, Hq, D)
+
+
+def verify_attn(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_table,
+                ctx_lens, scale):
+    """Return (out[B,k,Hq,D], lse[B,k,Hq]) in float64."""
+    keep, args, (B, k, Hq, D) = _attn_common(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale,
+                                             v_scale, block_table, ctx_lens, scale)
+    out = np.zeros((B, k, Hq, D), np.float64)
+    lse = np.zeros((B, k, Hq), np.float64)
+    rc = _load().oracle_verify_attn(*args, _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_verify_attn failed (%d): bad shape or page reference" % rc)
+    del keep
+    return out, lse
+
+
+def attn_rows(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_table, ctx_lens,
+              scale, rows):
+    """rows: int array [n, 3] of (b, i, h).  Return (out[n,D], lse[n]) in float64."""
+    keep, args, (B, k, Hq, D) = _attn_common(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale,
+                                             v_scale, block_table, ctx_lens, scale)
+    rows = np.ascontiguousarray(np.asarray(rows, np.int32).reshape(-1, 3))
+    out = np.zeros((rows.shape[0], D), np.float64)
+    lse = np.zeros((rows.shape[0],), np.float64)
+    rc = _load().oracle_attn_rows(*args, _ptr(rows), rows.shape[0], _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_attn_rows failed (%d)" % rc)
+    del keep
+    return out, lse
+
+
+def accept_greedy(logits, dtype, draft_tokens):
+    """logits [B, k+1, V]; draft_tokens int32 [B, k].
+
+    Return (accepted_len[B], next_token[B], argmax_rows[B, k+1]) as int32.
+    """
+    B, k1, V = logits.shape
+    k = k1 - 1
+    draft_tokens = np.ascontiguousarray(draft_tokens, np.int32)
+    assert draft_tokens.shape == (B, k)
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    am = np.zeros((B, k1), np.int32)
+    rc = _load().oracle_accept_greedy(_ptr(logits), DTYPES[dtype], _ptr(draft_tokens), B, k, V,
+                                      _ptr(acc), _ptr(nxt), _ptr(am))
+    if rc:
+        raise ValueError("oracle_accept_greedy failed (%d)" % rc)
+    return acc, nxt, am
+
+
+def bf16_bits_to_f64(bits: int) -> float:
+    return _load().oracle_bf16_to_f64(int(bits))
+
+
+def f16_bits_to_f64(bits: int) -> float:
+    return _load().oracle_f16_to_f64(int(bits))
+
+
+__all__ = ["verify_attn", "attn_rows", "accept_greedy", "bf16_bits_to_f64", "f16_bits_to_f64",
+           "DTYPES"]
