@@ -1,0 +1,178 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) verification hot path of
+ * speculative decoding.
+ *
+ * The target model verifies k drafted tokens in one prefill-style pass
+ * ("Decoding Speculative Decoding from First Principles", sections
+ * "Parallelizing method 2: sequence parallel" and "Speculating to get
+ * sequence parallelism during decode"; HeteroReason, "Phase 2: Speculating
+ * and Verification", single-step parallel verification).  Two operations
+ * make up that pass's data-parallel core:
+ *
+ *   spec_verify_attn    multi-query causal attention of each sequence's k
+ *                       draft queries over its paged KV cache (GQA, optional
+ *                       INT8 cache with per-(token, kv-head) fp16 scales as
+ *                       produced by CXL-SpecKV's "Algorithm 2 KV-Cache
+ *                       Compression");
+ *   spec_accept_greedy  greedy longest-prefix acceptance: the accepted length
+ *                       and the next (correction or bonus) token.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc'd, managed or
+ *     otherwise device-accessible), dense row-major with the shapes given.
+ *     The caller owns every tensor; the library never frees them.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: they enqueue kernels and return without synchronising.
+ *   - Return value: SPEC_OK (0) or a negative SPEC_ERR_* code.  On an error
+ *     nothing is enqueued and spec_last_error() (thread-local) describes it.
+ *   - The library owns a per-device workspace (split-KV partials, reduction
+ *     partials, completion tickets, an error word), grown on demand with
+ *     cudaMalloc on the first call that needs more (so a call that grows it
+ *     synchronises the device) and kept until spec_release() or exit.
+ *     Calls that overlap on the GPU (different streams without ordering)
+ *     share it and race: order them on one stream, or serialise them.
+ *   - Device-side input faults (a block_table entry outside [0, num_pages),
+ *     a context longer than the block table covers) never fault the GPU:
+ *     the kernels clamp the reference, set the device error word and carry
+ *     on; spec_device_error() reads (and clears) that word.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+enum {
+    SPEC_DTYPE_F32 = 0,
+    SPEC_DTYPE_BF16 = 1,
+    SPEC_DTYPE_F16 = 2, /* scales only */
+    SPEC_DTYPE_I8 = 3
+};
+
+/* Status codes. */
+enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID = -1,     /* bad pointer, shape, dtype or alignment */
+    SPEC_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. forced path) */
+    SPEC_ERR_CUDA = -3         /* a CUDA call failed; message has the CUDA error */
+};
+
+/* Options for spec_set_option (process-wide; default 0 = automatic). */
+enum {
+    /* 0 auto, 1 SIMT (CUDA cores) kernel, 2 tensor-core (tcgen05) kernel */
+    SPEC_OPT_ATTN_PATH = 0,
+    /* persistent CTAs of the tensor-core kernel; 0 = number of SMs */
+    SPEC_OPT_NUM_CTAS = 1,
+    /* 1: copy block_table and ctx_lens to the host and check them before
+     * launching (synchronises the stream); 0: no host check */
+    SPEC_OPT_VALIDATE = 2,
+    /* key chunk of the SIMT kernel's split-KV; 0 = automatic */
+    SPEC_OPT_SIMT_CHUNK = 3
+};
+
+/* Library version, major*10000 + minor*100 + patch. */
+SPEC_API int spec_version(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+SPEC_API const char *spec_last_error(void);
+
+/* Set a process-wide option (see SPEC_OPT_*).  Returns SPEC_OK or
+ * SPEC_ERR_INVALID for an unknown option or value. */
+SPEC_API int spec_set_option(int32_t option, int64_t value);
+
+/*
+ * Verification attention.
+ *
+ * For sequence b, draft position i (query at absolute position ctx_b + i)
+ * and query head h served by kv-head g = h / (num_q_heads / num_kv_heads):
+ *   s_j  = scale * <q[b,i,h,:], K_j>        for keys j = 0 .. ctx_b + i
+ *   lse  = ln sum_j exp(s_j)
+ *   out  = sum_j exp(s_j - lse) * V_j
+ * where key j lives in physical page block_table[b, j / page_size], slot
+ * j % page_size.  The k draft keys (positions ctx_b .. ctx_b + k - 1) must
+ * already be in the cache; this call only reads it.
+ *
+ *   q            [batch, num_draft, num_q_heads, head_dim]   q_dtype (F32|BF16)
+ *   k_cache,
+ *   v_cache      [num_pages, num_kv_heads, page_size, head_dim]  kv_dtype
+ *                (F32 | BF16 | I8).  With I8 the element is c * s.
+ *   k_scale,
+ *   v_scale      [num_pages, num_kv_heads, page_size] fp16; required with
+ *                I8, ignored (may be NULL) otherwise
+ *   block_table  [batch, max_pages_per_seq] int32 physical page ids
+ *   ctx_lens     [batch] int32 cached context per sequence, EXCLUDING the
+ *                drafts; ctx_b + num_draft <= max_pages_per_seq * page_size
+ *   scale        softmax scale (typically 1/sqrt(head_dim))
+ *   out          [batch, num_draft, num_q_heads, head_dim] in q_dtype
+ *   lse          [batch, num_draft, num_q_heads] fp32 natural log, or NULL
+ *
+ * Limits: 1 <= num_draft <= 64; num_q_heads % num_kv_heads == 0;
+ * head_dim % 32 == 0 and head_dim <= 256; page_size >= 1; q, caches and out
+ * 16-byte aligned.  A bf16 query over a bf16 or I8 cache with head_dim 128,
+ * num_draft * (num_q_heads / num_kv_heads) <= 128, a power-of-two
+ * page_size in [8, 256] and batch <= 2048 runs on the tensor-core kernel;
+ * every other accepted shape runs on the SIMT kernel.
+ */
+SPEC_API int spec_verify_attn(const void *q, const void *k_cache, const void *v_cache,
+                     const void *k_scale, const void *v_scale,
+                     const int32_t *block_table, const int32_t *ctx_lens,
+                     int32_t batch, int32_t num_draft, int32_t num_q_heads,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                     int32_t num_pages, int32_t max_pages_per_seq,
+                     int32_t q_dtype, int32_t kv_dtype, float scale,
+                     void *out, float *lse, void *stream);
+
+/*
+ * Greedy acceptance.
+ *
+ * For sequence b let a_i = argmax_v logits[b, i, v] (lowest index on ties;
+ * values compare as stored, so -0 == +0), i = 0 .. num_draft.  Then
+ *   accepted_len[b] = the largest n <= num_draft with
+ *                     draft_tokens[b, 0..n-1] == a_0..a_{n-1}
+ *   next_token[b]   = a_{accepted_len[b]}  (the target's own token at the
+ *                     first disagreement, or the bonus token after k
+ *                     agreements)
+ * so each sequence gains accepted_len[b] + 1 tokens ("Decoding Speculative
+ * Decoding from First Principles", "Speculating to get sequence parallelism
+ * during decode").  The caller commits by ctx_b += accepted_len[b] + 1.
+ *
+ *   logits        [batch, num_draft + 1, vocab]  logits_dtype (F32|BF16),
+ *                 finite values (a NaN row has no defined argmax)
+ *   draft_tokens  [batch, num_draft] int32
+ *   accepted_len  [batch] int32, written
+ *   next_token    [batch] int32, written
+ *
+ * Limits: 1 <= num_draft <= 64; 1 <= vocab < 2^31; logits 16-byte aligned.
+ */
+SPEC_API int spec_accept_greedy(const void *logits, int32_t logits_dtype, const int32_t *draft_tokens,
+                       int32_t batch, int32_t num_draft, int64_t vocab,
+                       int32_t *accepted_len, int32_t *next_token, void *stream);
+
+/* Read and clear the device error word of the current device (synchronises
+ * the device).  0 = no fault seen; otherwise a bitwise OR of SPEC_DEVERR_*. */
+SPEC_API int spec_device_error(int32_t *flags);
+
+enum {
+    SPEC_DEVERR_PAGE = 1,    /* block_table entry outside [0, num_pages) (clamped) */
+    SPEC_DEVERR_CTX = 2,     /* ctx_b + k beyond the block table (clamped) */
+    SPEC_DEVERR_TIMEOUT = 4  /* a bounded on-chip wait gave up; results invalid */
+};
+
+/* Free the current device's workspace (synchronises the device). */
+SPEC_API int spec_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

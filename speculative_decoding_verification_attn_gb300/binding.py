@@ -1,0 +1,189 @@
+"""Thin ctypes binding of ``libspecverify.so`` (see ``include/spec_verify.h``).
+
+Argument marshalling only: torch tensors supply device pointers, shapes,
+dtypes and the current CUDA stream; every step of the computation runs in
+the library's kernels.  There is no fallback: if the library has not been
+built (``python -c "import __graft_entry__ as g; g.build()"``) or fails to
+load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
+
+SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_F16, SPEC_DTYPE_I8 = 0, 1, 2, 3
+SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, -1, -2, -3
+SPEC_OPT_ATTN_PATH, SPEC_OPT_NUM_CTAS, SPEC_OPT_VALIDATE, SPEC_OPT_SIMT_CHUNK = 0, 1, 2, 3
+SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT = 1, 2, 4
+
+# every symbol the public header declares
+EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
+            "spec_accept_greedy", "spec_device_error", "spec_release"]
+
+_TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
+             torch.float16: SPEC_DTYPE_F16, torch.int8: SPEC_DTYPE_I8}
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("spec call failed (%d): %s" % (code, msg))
+        self.code = code
+
+
+def load():
+    """Load the in-tree library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        _lib = _open(LIB_PATH)
+    return _lib
+
+
+def _open(path: str):
+    if not os.path.exists(path):
+        raise RuntimeError("libspecverify.so not built at %s; run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.spec_version.restype = ctypes.c_int
+    lib.spec_last_error.restype = ctypes.c_char_p
+    lib.spec_set_option.argtypes = [i32, i64]
+    lib.spec_set_option.restype = ctypes.c_int
+    lib.spec_verify_attn.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                     i32, i32, ctypes.c_float, P, P, P]
+    lib.spec_verify_attn.restype = ctypes.c_int
+    lib.spec_accept_greedy.argtypes = [P, i32, P, i32, i32, i64, P, P, P]
+    lib.spec_accept_greedy.restype = ctypes.c_int
+    lib.spec_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+    lib.spec_device_error.restype = ctypes.c_int
+    lib.spec_release.restype = ctypes.c_int
+    return lib
+
+
+def _check(rc: int):
+    if rc != SPEC_OK:
+        raise SpecError(rc, load().spec_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def spec_version() -> int:
+    return load().spec_version()
+
+
+def spec_last_error() -> str:
+    return load().spec_last_error().decode()
+
+
+def spec_set_option(option: int, value: int) -> None:
+    _check(load().spec_set_option(option, int(value)))
+
+
+def spec_verify_attn(q, k_cache, v_cache, block_table, ctx_lens, num_draft: int, scale: float,
+                     out, lse=None, k_scale=None, v_scale=None, stream=None) -> None:
+    """Verification attention; writes ``out`` (and ``lse`` if given).
+
+    q [B, k, Hq, D]; k_cache / v_cache [NP, Hkv, P, D]; block_table
+    [B, max_pages] int32; ctx_lens [B] int32; out like q; lse [B, k, Hq] f32;
+    k_scale / v_scale [NP, Hkv, P] fp16 for an int8 cache.
+    """
+    B, k, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    if k != num_draft or D2 != D:
+        raise ValueError("shape mismatch between q, num_draft and the cache")
+    if block_table.dtype != torch.int32 or ctx_lens.dtype != torch.int32:
+        raise ValueError("block_table and ctx_lens must be int32")
+    _check(load().spec_verify_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        _ptr(ctx_lens), B, k, Hq, Hkv, D, P, NP, block_table.shape[1], _TORCH_DT[q.dtype],
+        _TORCH_DT[k_cache.dtype], float(scale), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def spec_accept_greedy(logits, draft_tokens, num_draft: int, accepted_len, next_token,
+                       stream=None) -> None:
+    """Greedy acceptance; writes ``accepted_len`` and ``next_token`` (int32 [B])."""
+    B, k1, V = logits.shape
+    if k1 != num_draft + 1 or tuple(draft_tokens.shape) != (B, num_draft):
+        raise ValueError("logits must be [B, num_draft+1, V] and drafts [B, num_draft]")
+    _check(load().spec_accept_greedy(_ptr(logits), _TORCH_DT[logits.dtype], _ptr(draft_tokens), B,
+                                     num_draft, V, _ptr(accepted_len), _ptr(next_token),
+                                     _stream(stream)))
+
+
+def spec_device_error() -> int:
+    v = ctypes.c_int32(0)
+    _check(load().spec_device_error(ctypes.byref(v)))
+    return v.value
+
+
+def spec_release() -> None:
+    _check(load().spec_release())
+
+
+# ---------------------------------------------------------------- plumbing
+
+def _np_to_torch(a: np.ndarray, kind: str) -> torch.Tensor:
+    if kind == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    if kind == "f16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16)
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def inputs_to_torch(inp, device="cuda", pin: bool = False) -> dict:
+    """Generator output (numpy) -> torch tensors on `device` (or pinned host)."""
+    s = inp.spec
+    t = {
+        "q": _np_to_torch(inp.q, s.q_dtype),
+        "k_cache": _np_to_torch(inp.k_cache, s.kv_dtype),
+        "v_cache": _np_to_torch(inp.v_cache, s.kv_dtype),
+        "block_table": torch.from_numpy(inp.block_table),
+        "ctx_lens": torch.from_numpy(inp.ctx_lens),
+        "logits": _np_to_torch(inp.logits, s.logits_dtype),
+        "draft_tokens": torch.from_numpy(inp.draft_tokens),
+    }
+    if inp.k_scale is not None:
+        t["k_scale"] = _np_to_torch(inp.k_scale, "f16")
+        t["v_scale"] = _np_to_torch(inp.v_scale, "f16")
+    if pin:
+        return {n: v.pin_memory() for n, v in t.items()}
+    return {n: v.to(device) for n, v in t.items()}
+
+
+def alloc_outputs(inp, device="cuda") -> dict:
+    s = inp.spec
+    qdt = torch.float32 if s.q_dtype == "f32" else torch.bfloat16
+    B, k = s.batch, s.num_draft
+    return {
+        "out": torch.empty((B, k, s.num_q_heads, s.head_dim), dtype=qdt, device=device),
+        "lse": torch.empty((B, k, s.num_q_heads), dtype=torch.float32, device=device),
+        "accepted_len": torch.empty((B,), dtype=torch.int32, device=device),
+        "next_token": torch.empty((B,), dtype=torch.int32, device=device),
+    }
+
+
+def run_verify(t: dict, o: dict, num_draft: int, scale: float, stream=None) -> None:
+    """One verification step: attention, then acceptance, on one stream."""
+    spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["ctx_lens"],
+                     num_draft, scale, o["out"], o["lse"], t.get("k_scale"), t.get("v_scale"),
+                     stream=stream)
+    spec_accept_greedy(t["logits"], t["draft_tokens"], num_draft, o["accepted_len"],
+                       o["next_token"], stream=stream)

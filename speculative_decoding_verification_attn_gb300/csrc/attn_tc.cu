@@ -1,0 +1,723 @@
+// Verification attention on the 5th-generation tensor cores (tcgen05 + TMEM),
+// bf16 queries over a bf16 paged KV cache, head_dim 128.
+//
+// What it computes: multi-query causal attention of each sequence's k draft
+// queries over its paged cache ("Decoding Speculative Decoding from First
+// Principles", "Parallelizing method 2: sequence parallel" and "Speculating
+// to get sequence parallelism during decode"): query i of sequence b sees
+// keys 0 .. ctx_b + i; kv-head g serves q-heads g*G .. g*G+G-1.
+//
+// Design (GB300 / sm_103a):
+//  * All k*G query rows of one (sequence, kv-head) form the M side of one
+//    128-row MMA tile, so every K/V byte is read from HBM exactly once and
+//    reused k*G times (the sequence-parallel amortisation the blog describes).
+//  * Work is the list of 64-key tiles of every (sequence, kv-head) segment,
+//    split evenly over a persistent grid of one CTA per SM (stream-K).  A CTA
+//    walks a contiguous tile range that may cross segment boundaries; a
+//    segment cut by a range boundary leaves (O/l, lse) partials that the
+//    combine kernel merges with log-sum-exp weights (split-KV).
+//  * Warp roles: warp 4 = TMA producer (page-table driven: one 2-D box per
+//    (page, head-dim half)), warp 5 = MMA issuer and TMEM owner, warps 0-3 =
+//    softmax / rescale / epilogue, one query row per thread (TMEM lane).
+//  * S = Q K^T lands in TMEM (double buffered), the softmax warps turn it into
+//    bf16 P in place, and O += P V takes P straight from TMEM.  The running
+//    max is only moved when it grows by more than 2^8, so O is rarely
+//    rescaled (exact in real arithmetic: O and l share the reference max).
+//  * Every mbarrier wait is bounded (1 s); a timeout sets the device error
+//    word and an abort flag that makes every role drain and return.
+#include <cuda.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace specv {
+namespace {
+
+constexpr int D = 128;
+constexpr int TN = 64;           // keys per tile
+constexpr int NS = 4;            // K/V pipeline stages
+constexpr int ROWS = 128;        // MMA M: query rows (padded)
+constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
+constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
+constexpr int KV_HALF = TN * 128;         // 8 KB
+constexpr int KV_BYTES = 2 * KV_HALF;     // 16 KB per tensor per stage
+constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
+constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
+constexpr int MAX_BOX = TN / 8;           // boxes per tile (page_size >= 8)
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 256;       // S0 [0,64) S1 [64,128) O [128,256)
+constexpr uint32_t TM_S = 0, TM_O = 128;
+constexpr int MAX_BATCH = 2048;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr uint32_t IDESC_QK = umma_idesc_bf16(ROWS, TN, 0, 0);  // A,B K-major
+constexpr uint32_t IDESC_PV = umma_idesc_bf16(ROWS, D, 0, 1);   // B (V) MN-major
+
+struct Smem {
+    // offsets from the 1024-aligned base
+    static constexpr int Q = 0;
+    static constexpr int STAGES = Q + 2 * Q_BYTES;
+    static constexpr int BARS = STAGES + NS * STAGE_BYTES;
+    // barriers (uint64 each)
+    static constexpr int B_KFULL = 0, B_VFULL = NS, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
+                         B_QEMPTY = 3 * NS + 2, B_SFULL = 3 * NS + 4, B_PFULL = 3 * NS + 6,
+                         B_ODONE = 3 * NS + 8, B_DRAIN = 3 * NS + 9, NUM_BARS = 3 * NS + 10;
+    static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
+    static constexpr int PIDS = MISC + 16;                     // [LOOKAHEAD+1][MAX_BOX] int
+    static constexpr int CTX = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;  // [MAX_BATCH] int
+    static constexpr int PRE = CTX + MAX_BATCH * 4;           // [MAX_BATCH+1] int
+    static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
+};
+constexpr size_t SMEM_BYTES = Smem::END + 1024;  // + alignment slack
+
+struct TcParams {
+    AttnArgs a;
+    float* part_o;    // [2*C][ROWS][D]
+    float* part_lse;  // [2*C][ROWS]
+};
+
+// Walks a CTA's tile range: tile -> (sequence b, kv-head, tile-in-segment).
+struct Cursor {
+    int b, kvh, lt, nb;
+    int64_t seg_start;  // global index of the segment's first tile
+    __device__ void init(int64_t t, const int* pre, const int* ctx, int B, int Hkv, int k) {
+        int lo = 0, hi = B - 1;  // largest b with pre[b]*Hkv <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)pre[mid] * Hkv <= t) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        nb = (ctx[b] + k + TN - 1) / TN;
+        const int64_t off = t - (int64_t)pre[b] * Hkv;
+        kvh = (int)(off / nb);
+        lt = (int)(off % nb);
+        seg_start = (int64_t)pre[b] * Hkv + (int64_t)kvh * nb;
+    }
+    __device__ void next(const int* ctx, int Hkv, int k) {
+        if (++lt == nb) {
+            lt = 0;
+            seg_start += nb;
+            if (++kvh == Hkv) {
+                kvh = 0;
+                ++b;
+                nb = (ctx[b] + k + TN - 1) / TN;
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the whole warp gets its verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* dev_err) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, dev_err);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Bounded wait used only while draining after an abort (ignores the flag).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, const TcParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const AttnArgs& a = prm.a;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BARS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Smem::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC + 4);
+    int* pid_ring = reinterpret_cast<int*>(sm + Smem::PIDS);
+    int* s_ctx = reinterpret_cast<int*>(sm + Smem::CTX);
+    int* s_pre = reinterpret_cast<int*>(sm + Smem::PRE);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.B, k = a.k, Hkv = a.Hkv, G = a.Hq / a.Hkv, R = k * G, P = a.P;
+    const int BH = P < TN ? P : TN;  // box height (keys per TMA box)
+
+    // ---- setup: barriers, TMEM, zero Q pad rows, per-sequence tile prefix
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars[Smem::B_KFULL + s], 1);
+            mbar_init(&bars[Smem::B_VFULL + s], 1);
+            mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&bars[Smem::B_QFULL + q], 1);
+            mbar_init(&bars[Smem::B_QEMPTY + q], 1);
+            mbar_init(&bars[Smem::B_SFULL + q], 1);
+            mbar_init(&bars[Smem::B_PFULL + q], 4);
+        }
+        mbar_init(&bars[Smem::B_ODONE], 1);
+        mbar_init(&bars[Smem::B_DRAIN], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    {
+        // rows R..127 of both Q buffers stay zero for the whole kernel
+        uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int e = tid; e < 2 * Q_BYTES / 16; e += THREADS) {
+            const int row = (e % (Q_HALF / 16)) / 8;
+            if (row >= R) q4[e] = z;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 4) {
+        const int per = (B + 31) / 32, lo = lane * per, hi = min(B, lo + per);
+        int sum = 0;
+        for (int b = lo; b < hi; ++b) {
+            int c = a.ctx_lens[b];
+            const int64_t cap = (int64_t)a.max_pages * P - k;
+            if (c < 0 || (int64_t)c > cap) {
+                raise_device_error(a.dev_err, SPEC_DEVERR_CTX);
+                c = c < 0 ? 0 : (int)(cap < 0 ? 0 : cap);
+            }
+            s_ctx[b] = c;
+            sum += (c + k + TN - 1) / TN;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int b = lo; b < hi; ++b) {
+            s_pre[b] = run;
+            run += (s_ctx[b] + k + TN - 1) / TN;
+        }
+        if (lane == 31) s_pre[B] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t T = (int64_t)s_pre[B] * Hkv;
+    const int64_t C = gridDim.x;
+    const int64_t t_begin = (int64_t)blockIdx.x * T / C;
+    const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
+    const int n_tiles = (int)(t_end - t_begin);
+
+    if (warp == 4) {
+        // ================= TMA producer =================
+        Cursor cur, ahead;
+        if (n_tiles > 0) {
+            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            ahead = cur;
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        if (lane == 0) {
+            prefetch_tmap(&qmap);
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
+        // block-table entries of tile `ah` -> ring slot (cp.async, lookahead)
+        auto fetch_pids = [&](int slot, const Cursor& c) {
+            const int key0 = c.lt * TN;
+            const int L = s_ctx[c.b] + k;
+            const int nvalid = min(TN, L - key0);
+            const int nbox = (nvalid + BH - 1) / BH;
+            if (lane < nbox) {
+                const int lp = (key0 + lane * BH) / P;
+                cp_async_4(&pid_ring[slot * MAX_BOX + lane],
+                           &a.block_table[(int64_t)c.b * a.max_pages + lp]);
+            }
+        };
+        for (int la = 0; la < LOOKAHEAD; ++la) {
+            if (la < n_tiles) {
+                fetch_pids(la % (LOOKAHEAD + 1), ahead);
+                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+        }
+        int pc = -1;  // piece counter
+        int issued_q[2] = {0, 0};
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            if (it + LOOKAHEAD < n_tiles) {
+                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
+                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+            cp_async_wait<LOOKAHEAD>();
+            __syncwarp();
+            const bool first = (it == 0) || (cur.lt == 0);
+            if (first) {
+                ++pc;
+                const int qb = pc & 1, use = pc >> 1;
+                if (lane == 0) {
+                    if (use >= 1)
+                        ok = mbar_wait(&bars[Smem::B_QEMPTY + qb], (use - 1) & 1, abort_flag,
+                                       a.dev_err);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL + qb], 2 * R * 128);
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(sm + Smem::Q + qb * Q_BYTES + h * Q_HALF, &qmap,
+                                        &bars[Smem::B_QFULL + qb], h * 64, cur.kvh * G, cur.b * k);
+                        issued_q[qb] = use + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            const int s = it % NS, use = it / NS;
+            if (lane == 0) {
+                if (use >= 1)
+                    ok = mbar_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag,
+                                   a.dev_err);
+                if (ok) {
+                    const int key0 = cur.lt * TN;
+                    const int L = s_ctx[cur.b] + k;
+                    const int nvalid = min(TN, L - key0);
+                    const int nbox = (nvalid + BH - 1) / BH;
+                    const uint32_t bytes = (uint32_t)nbox * BH * 128 * 2;
+                    mbar_arrive_expect_tx(&bars[Smem::B_KFULL + s], bytes);
+                    mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], bytes);
+                    uint8_t* kst = sm + Smem::STAGES + s * STAGE_BYTES;
+                    uint8_t* vst = kst + KV_BYTES;
+                    const int slot = it % (LOOKAHEAD + 1);
+                    for (int bx = 0; bx < nbox; ++bx) {
+                        int page = pid_ring[slot * MAX_BOX + bx];
+                        if (page < 0 || page >= a.num_pages) {
+                            raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                            page = 0;
+                        }
+                        const int key = key0 + bx * BH;
+                        const int row = (page * Hkv + cur.kvh) * P + (key % P);
+                        for (int h = 0; h < 2; ++h) {
+                            tma_load_2d(kst + h * KV_HALF + bx * BH * 128, &kmap,
+                                        &bars[Smem::B_KFULL + s], h * 64, row, pol);
+                            tma_load_2d(vst + h * KV_HALF + bx * BH * 128, &vmap,
+                                        &bars[Smem::B_VFULL + s], h * 64, row, pol);
+                        }
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+        cp_async_wait<0>();
+        if (!ok && lane == 0) {
+            // drain: wait (bounded) for every copy this CTA issued
+            const int issued = n_tiles;  // upper bound on stage uses issued
+            for (int s = 0; s < NS; ++s) {
+                const int uses = issued > s ? (issued - 1 - s) / NS + 1 : 0;
+                if (uses > 0) {
+                    mbar_drain(&bars[Smem::B_KFULL + s], (uses - 1) & 1);
+                    mbar_drain(&bars[Smem::B_VFULL + s], (uses - 1) & 1);
+                }
+            }
+            for (int q = 0; q < 2; ++q)
+                if (issued_q[q] > 0) mbar_drain(&bars[Smem::B_QFULL + q], (issued_q[q] - 1) & 1);
+        }
+    } else if (warp == 5) {
+        // ================= MMA issuer =================
+        if (lane == 0 && n_tiles > 0) {
+            Cursor cur;
+            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            int pc = -1;
+            bool ok = true;
+            int pend_it = -1;
+            bool pend_first = false;
+            auto issue_pv = [&](int j, bool first_of_piece) -> bool {
+                const int sbj = j & 1, sj = j % NS;
+                if (!mbar_wait(&bars[Smem::B_PFULL + sbj], (j >> 1) & 1, abort_flag, a.dev_err))
+                    return false;
+                if (!mbar_wait(&bars[Smem::B_VFULL + sj], (j / NS) & 1, abort_flag, a.dev_err))
+                    return false;
+                tc_fence_after();
+                const uint32_t vbase = smem_u32(sm + Smem::STAGES + sj * STAGE_BYTES + KV_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < TN / 16; ++kk) {
+                    const uint64_t bdesc = umma_sdesc_sw128(vbase + kk * 16 * 128, KV_HALF, 1024);
+                    umma_ts(tmem + TM_O, tmem + TM_S + sbj * TN + kk * 8, bdesc, IDESC_PV,
+                            (kk > 0 || !first_of_piece) ? 1u : 0u);
+                }
+                umma_commit(&bars[Smem::B_KVEMPTY + sj]);
+                umma_commit(&bars[Smem::B_ODONE]);
+                return true;
+            };
+            for (int it = 0; it < n_tiles && ok; ++it) {
+                const bool first = (it == 0) || (cur.lt == 0);
+                const bool last = (it == n_tiles - 1) || (cur.lt == cur.nb - 1);
+                if (first) ++pc;
+                const int qb = pc & 1;
+                if (first)
+                    ok = mbar_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag, a.dev_err);
+                const int s = it % NS;
+                if (ok)
+                    ok = mbar_wait(&bars[Smem::B_KFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
+                if (!ok) break;
+                tc_fence_after();
+                const int sb = it & 1;
+                const uint32_t qbase = smem_u32(sm + Smem::Q + qb * Q_BYTES);
+                const uint32_t kbase = smem_u32(sm + Smem::STAGES + s * STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t col = (kk & 3) * 32;  // 16 bf16 = 32 B inside the swizzle row
+                    const uint64_t adesc =
+                        umma_sdesc_sw128(qbase + (kk >> 2) * Q_HALF + col, 16, 1024);
+                    const uint64_t bdesc =
+                        umma_sdesc_sw128(kbase + (kk >> 2) * KV_HALF + col, 16, 1024);
+                    umma_ss(tmem + TM_S + sb * TN, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&bars[Smem::B_SFULL + sb]);
+                if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
+                if (pend_it >= 0) ok = issue_pv(pend_it, pend_first);
+                pend_it = it;
+                pend_first = first;
+                if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+            }
+            if (ok && pend_it >= 0) ok = issue_pv(pend_it, pend_first);
+            // make sure every tensor-core op finished before TMEM is released
+            umma_commit(&bars[Smem::B_DRAIN]);
+            mbar_drain(&bars[Smem::B_DRAIN], 0);
+        }
+    } else {
+        // ================= softmax / rescale / epilogue (warps 0-3) =================
+        const int r = tid;  // query row == TMEM lane
+        const bool warp_active = warp * 32 < R;
+        const bool row_valid = r < R;
+        const int i_row = row_valid ? r / G : k - 1;
+        const float sl2 = a.scale * kLog2e;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        Cursor cur;
+        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            const bool first = (it == 0) || (cur.lt == 0);
+            const bool last = (it == n_tiles - 1) || (cur.lt == cur.nb - 1);
+            const int sb = it & 1, s = it % NS;
+            const int ctx = s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
+            const int nvalid = min(TN, L - key0);
+            if (first) {
+                m_ref = -INFINITY;
+                l = 0.f;
+            }
+            ok = warp_wait(&bars[Smem::B_SFULL + sb], (it >> 1) & 1, abort_flag, a.dev_err);
+            if (!ok) break;
+            if (warp_active) {
+                tc_fence_after();
+                uint32_t sr[2][32];
+                tmem_ld32(lane_base + TM_S + sb * TN, sr[0]);
+                tmem_ld32(lane_base + TM_S + sb * TN + 32, sr[1]);
+                tmem_wait_ld();
+                // visible keys of this row in this tile: c < cmax
+                const int cmax = max(0, min(nvalid, ctx + i_row - key0 + 1));
+                float mt = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < TN; ++c) {
+                    const float v = __uint_as_float(sr[c >> 5][c & 31]) * sl2;
+                    if (c < cmax) mt = fmaxf(mt, v);
+                }
+                const float m_new = fmaxf(m_ref, mt);
+                float alpha = 1.f;
+                const bool move = m_new > m_ref + kRescaleThreshold;  // also -inf -> finite
+                if (move) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
+                    m_ref = m_new;
+                    l *= alpha;
+                }
+                uint32_t pk[32];
+                float psum = 0.f;
+#pragma unroll
+                for (int c2 = 0; c2 < TN / 2; ++c2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    const int c = 2 * c2;
+                    if (c < cmax) p0 = exp2f(__uint_as_float(sr[c >> 5][c & 31]) * sl2 - m_ref);
+                    if (c + 1 < cmax)
+                        p1 = exp2f(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]) * sl2 - m_ref);
+                    psum += p0 + p1;
+                    pk[c2] = pack_bf16x2(p0, p1);
+                }
+                l += psum;
+                tmem_st32(lane_base + TM_S + sb * TN, pk);
+                tmem_wait_st();
+                if (!first) {
+                    // PV of the previous tile must be done before O is touched
+                    ok = warp_wait(&bars[Smem::B_ODONE], (it - 1) & 1, abort_flag, a.dev_err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, move && alpha != 1.f)) {
+#pragma unroll
+                        for (int c4 = 0; c4 < D / 32; ++c4) {
+                            uint32_t ov[32];
+                            tmem_ld32(lane_base + TM_O + c4 * 32, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 32; ++c)
+                                ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                            tmem_st32(lane_base + TM_O + c4 * 32, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+            }
+            if (nvalid < TN && warp == 0) {
+                // rows past the last key of the sequence: zero V so that
+                // 0 * (stale or canary) never reaches the accumulator
+                ok = warp_wait(&bars[Smem::B_VFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
+                if (!ok) break;
+                uint8_t* vst = sm + Smem::STAGES + s * STAGE_BYTES + KV_BYTES;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                for (int e = nvalid * 8 + lane; e < TN * 8; e += 32) {
+                    const int row = e / 8, chunk = e % 8;
+                    *reinterpret_cast<uint4*>(vst + row * 128 + chunk * 16) = z;
+                    *reinterpret_cast<uint4*>(vst + KV_HALF + row * 128 + chunk * 16) = z;
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Smem::B_PFULL + sb]);
+            if (last && warp_active) {
+                ok = warp_wait(&bars[Smem::B_ODONE], it & 1, abort_flag, a.dev_err);
+                if (!ok) break;
+                tc_fence_after();
+                const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
+                const float inv_l = l > 0.f ? 1.f / l : 0.f;
+                const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+                const int g = r % G, h = cur.kvh * G + g;
+                const int64_t orow = ((int64_t)cur.b * k + i_row) * a.Hq + h;
+                const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + TM_O + c4 * 32, ov);
+                    tmem_wait_ld();
+                    if (!row_valid) continue;
+                    if (complete) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            static_cast<__nv_bfloat16*>(a.out) + orow * D + c4 * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l,
+                                              __uint_as_float(ov[8 * v + 1]) * inv_l);
+                            w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l,
+                                              __uint_as_float(ov[8 * v + 3]) * inv_l);
+                            w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l,
+                                              __uint_as_float(ov[8 * v + 5]) * inv_l);
+                            w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l,
+                                              __uint_as_float(ov[8 * v + 7]) * inv_l);
+                            dst[v] = w;
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(
+                            prm.part_o + ((int64_t)slot * ROWS + r) * D + c4 * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(ov[4 * v + 0]) * inv_l,
+                                                 __uint_as_float(ov[4 * v + 1]) * inv_l,
+                                                 __uint_as_float(ov[4 * v + 2]) * inv_l,
+                                                 __uint_as_float(ov[4 * v + 3]) * inv_l);
+                    }
+                }
+                if (row_valid) {
+                    if (complete) {
+                        if (a.lse) a.lse[orow] = lse;
+                    } else {
+                        prm.part_lse[(int64_t)slot * ROWS + r] = lse;
+                    }
+                }
+                tc_fence_before();
+            }
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// Merge the partials of every segment cut by a CTA-range boundary.
+// grid (B*Hkv, ceil(R/8)), 8 warps, one query row per warp.
+__global__ void __launch_bounds__(256)
+combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
+                  const float* __restrict__ part_lse) {
+    __shared__ int s_red[8];
+    const int seg = blockIdx.x, kvh = seg % a.Hkv, b = seg / a.Hkv;
+    const int G = a.Hq / a.Hkv, R = a.k * G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t cap = (int64_t)a.max_pages * a.P - a.k;
+    auto tiles_of = [&](int bb) {
+        int c = a.ctx_lens[bb];
+        if (c < 0 || (int64_t)c > cap) c = c < 0 ? 0 : (int)(cap < 0 ? 0 : cap);
+        return (c + a.k + TN - 1) / TN;
+    };
+    // tiles before sequence b, and in total
+    int before = 0, total = 0;
+    for (int bb = threadIdx.x; bb < a.B; bb += blockDim.x) {
+        const int n = tiles_of(bb);
+        total += n;
+        if (bb < b) before += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    if (lane == 0) s_red[warp] = before;
+    __syncthreads();
+    int pre_b = 0;
+    for (int w = 0; w < 8; ++w) pre_b += s_red[w];
+    __syncthreads();
+    if (lane == 0) s_red[warp] = total;
+    __syncthreads();
+    int tot = 0;
+    for (int w = 0; w < 8; ++w) tot += s_red[w];
+
+    const int64_t T = (int64_t)tot * a.Hkv, C = num_ctas;
+    const int nb = tiles_of(b);
+    const int64_t s0 = (int64_t)pre_b * a.Hkv + (int64_t)kvh * nb, s1 = s0 + nb;
+    auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
+    const int c_first = cta_of(s0), c_last = cta_of(s1 - 1);
+    if (c_first == c_last) return;  // written directly by its CTA
+    const int row = blockIdx.y * 8 + warp;
+    if (row >= R) return;
+
+    float m = -INFINITY;
+    for (int c = c_first; c <= c_last; ++c) {
+        const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
+        m = fmaxf(m, part_lse[(int64_t)slot * ROWS + row]);
+    }
+    float tsum = 0.f;
+    for (int c = c_first; c <= c_last; ++c) {
+        const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
+        tsum += expf(part_lse[(int64_t)slot * ROWS + row] - m);
+    }
+    const float lse_tot = m + logf(tsum);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c_first; c <= c_last; ++c) {
+        const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
+        const float w = expf(part_lse[(int64_t)slot * ROWS + row] - lse_tot);
+        const float4 v = reinterpret_cast<const float4*>(part_o + ((int64_t)slot * ROWS + row) * D)[lane];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    const int i = row / G, h = kvh * G + row % G;
+    const int64_t orow = ((int64_t)b * a.k + i) * a.Hq + h;
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * D)[lane] = o;
+    if (lane == 0 && a.lse) a.lse[orow] = lse_tot;
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+bool tc_supported(const AttnArgs& a) {
+    const int G = a.Hq / a.Hkv;
+    const bool pow2 = (a.P & (a.P - 1)) == 0;
+    return a.q_dtype == SPEC_DTYPE_BF16 && a.kv_dtype == SPEC_DTYPE_BF16 && a.D == D &&
+           a.k * G <= ROWS && G <= 256 && pow2 && a.P >= 8 && a.P <= 256 && a.B <= MAX_BATCH &&
+           (int64_t)a.num_pages * a.Hkv * a.P < (1LL << 31) && (int64_t)a.B * a.k < (1LL << 31);
+}
+
+size_t tc_workspace_bytes(const AttnArgs&, int num_ctas) {
+    return (size_t)2 * num_ctas * ROWS * (D + 1) * sizeof(float) + 256;
+}
+
+cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream) {
+    if (a.B == 0) return cudaSuccess;
+    EncodeTiledFn encode = get_encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const int G = a.Hq / a.Hkv;
+    CUtensorMap qmap, kmap, vmap;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.k};
+        cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)a.k};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const int BH = a.P < TN ? a.P : TN;
+    const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
+    for (int t = 0; t < 2; ++t) {
+        cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+        cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)BH};
+        cuuint32_t es[2] = {1, 1};
+        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    TcParams prm;
+    prm.a = a;
+    prm.part_o = static_cast<float*>(workspace);
+    prm.part_lse = prm.part_o + (size_t)2 * num_ctas * ROWS * D;
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attn_tc_kernel<<<num_ctas, THREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int R = a.k * G;
+    dim3 cgrid(a.B * a.Hkv, (R + 7) / 8);
+    combine_tc_kernel<<<cgrid, 256, 0, stream>>>(a, num_ctas, prm.part_o, prm.part_lse);
+    return cudaGetLastError();
+}
+
+}  // namespace specv

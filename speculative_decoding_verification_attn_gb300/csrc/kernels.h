@@ -1,0 +1,61 @@
+// Internal launch interface between the C-ABI shim (spec_abi.cu) and the
+// kernel translation units.  Host-visible only; no torch types anywhere.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace specv {
+
+// Geometry and pointers of one verification-attention call.
+struct AttnArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const uint16_t* k_scale;  // fp16 bits, INT8 caches only
+    const uint16_t* v_scale;
+    const int32_t* block_table;
+    const int32_t* ctx_lens;
+    int32_t B, k, Hq, Hkv, D, P, num_pages, max_pages;
+    int32_t q_dtype, kv_dtype;
+    float scale;
+    void* out;
+    float* lse;
+    int* dev_err;  // device error word
+};
+
+// ---- SIMT kernel (CUDA cores; any supported dtype / shape) ----
+struct SimtPlan {
+    int32_t chunk;       // keys per split chunk (multiple of 16)
+    int32_t max_chunks;  // chunks per sequence at the longest possible context
+    int32_t row_groups;  // query-row groups per (sequence, kv-head)
+    int32_t rows_per_group;
+};
+SimtPlan simt_plan(const AttnArgs& a, int num_sms, int forced_chunk);
+size_t simt_workspace_bytes(const AttnArgs& a, const SimtPlan& p);
+cudaError_t launch_attn_simt(const AttnArgs& a, const SimtPlan& p, void* workspace,
+                             cudaStream_t stream);
+
+// ---- tensor-core kernel (tcgen05 + TMA, persistent, split-KV stream-K) ----
+bool tc_supported(const AttnArgs& a);
+size_t tc_workspace_bytes(const AttnArgs& a, int num_ctas);
+cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream);
+
+// ---- greedy acceptance ----
+struct AcceptArgs {
+    const void* logits;
+    int32_t dtype;
+    const int32_t* draft;
+    int32_t B, k;
+    int64_t V;
+    int32_t* accepted_len;
+    int32_t* next_token;
+};
+size_t accept_workspace_bytes(const AcceptArgs& a);
+// `tickets` must hold B zeroed int32 (self-resetting across calls).
+cudaError_t launch_accept(const AcceptArgs& a, void* workspace, int32_t* tickets,
+                          cudaStream_t stream);
+
+}  // namespace specv

@@ -1,0 +1,297 @@
+// C ABI of the verification hot path: argument validation, the per-device
+// workspace, path selection and launches on the caller's stream.  Every
+// entry point returns a status code; on an error nothing is enqueued and the
+// thread-local message says why.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(SPEC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+std::atomic<int64_t> g_opt_path{0}, g_opt_ctas{0}, g_opt_validate{0}, g_opt_simt_chunk{0};
+
+// Per-device workspace: [error word + tickets | scratch].
+constexpr size_t kHeader = 64 * 1024;   // error word at 0, acceptance tickets at 256
+constexpr int kMaxTickets = (int)((kHeader - 256) / 4);
+struct Workspace {
+    void* base = nullptr;
+    size_t bytes = 0;
+    int sms = 0;
+};
+std::mutex g_ws_mu;
+std::vector<Workspace> g_ws;
+
+// Returns the current device's workspace with at least `scratch` bytes of
+// scratch space (allocating or growing it), or sets an error.
+int get_workspace(size_t scratch, Workspace** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
+    Workspace& w = g_ws[dev];
+    if (w.sms == 0) {
+        e = cudaDeviceGetAttribute(&w.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+    const size_t need = kHeader + ((scratch + 255) & ~size_t(255));
+    if (w.bytes < need) {
+        if (w.base) {
+            e = cudaDeviceSynchronize();  // earlier calls may still use the old buffer
+            if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        size_t grow = need < (size_t)64 << 20 ? (size_t)64 << 20 : need;
+        e = cudaMalloc(&w.base, grow);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+        e = cudaMemset(w.base, 0, kHeader);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        w.bytes = grow;
+    }
+    *out = &w;
+    return SPEC_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int dtype_size(int32_t dt) {
+    switch (dt) {
+    case SPEC_DTYPE_F32: return 4;
+    case SPEC_DTYPE_BF16: return 2;
+    case SPEC_DTYPE_F16: return 2;
+    case SPEC_DTYPE_I8: return 1;
+    default: return 0;
+    }
+}
+
+// Host-side check of block_table / ctx_lens (SPEC_OPT_VALIDATE).
+int validate_tables(const specv::AttnArgs& a, cudaStream_t stream) {
+    std::vector<int32_t> ctx(a.B), bt((size_t)a.B * a.max_pages);
+    cudaError_t e = cudaMemcpyAsync(ctx.data(), a.ctx_lens, sizeof(int32_t) * a.B,
+                                    cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(bt.data(), a.block_table, sizeof(int32_t) * bt.size(),
+                            cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "validate: copy tables");
+    for (int b = 0; b < a.B; ++b) {
+        const int64_t L = (int64_t)ctx[b] + a.k;
+        if (ctx[b] < 0 || L > (int64_t)a.max_pages * a.P)
+            return fail(SPEC_ERR_INVALID, "ctx_lens[%d]=%d: ctx + num_draft exceeds the %d pages "
+                        "of the block table", b, ctx[b], a.max_pages);
+        const int64_t n = (L + a.P - 1) / a.P;
+        for (int64_t p = 0; p < n; ++p) {
+            const int32_t id = bt[(size_t)b * a.max_pages + p];
+            if (id < 0 || id >= a.num_pages)
+                return fail(SPEC_ERR_INVALID, "block_table[%d][%lld]=%d outside [0, %d)", b,
+                            (long long)p, id, a.num_pages);
+        }
+    }
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_version(void) { return 100; }
+
+const char* spec_last_error(void) { return g_err.c_str(); }
+
+int spec_set_option(int32_t option, int64_t value) {
+    switch (option) {
+    case SPEC_OPT_ATTN_PATH:
+        if (value < 0 || value > 2) return fail(SPEC_ERR_INVALID, "attn path must be 0, 1 or 2");
+        g_opt_path = value;
+        return SPEC_OK;
+    case SPEC_OPT_NUM_CTAS:
+        if (value < 0 || value > 65535) return fail(SPEC_ERR_INVALID, "num_ctas out of range");
+        g_opt_ctas = value;
+        return SPEC_OK;
+    case SPEC_OPT_VALIDATE:
+        g_opt_validate = value ? 1 : 0;
+        return SPEC_OK;
+    case SPEC_OPT_SIMT_CHUNK:
+        if (value < 0 || value > (1 << 30)) return fail(SPEC_ERR_INVALID, "chunk out of range");
+        g_opt_simt_chunk = value;
+        return SPEC_OK;
+    default:
+        return fail(SPEC_ERR_INVALID, "unknown option %d", option);
+    }
+}
+
+int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, const void* k_scale,
+                     const void* v_scale, const int32_t* block_table, const int32_t* ctx_lens,
+                     int32_t batch, int32_t num_draft, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t page_size, int32_t num_pages,
+                     int32_t max_pages_per_seq, int32_t q_dtype, int32_t kv_dtype, float scale,
+                     void* out, float* lse, void* stream) {
+    g_err.clear();
+    if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
+    if (num_draft < 1 || num_draft > 64) return fail(SPEC_ERR_INVALID, "num_draft must be in [1, 64]");
+    if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads)
+        return fail(SPEC_ERR_INVALID, "num_q_heads must be a positive multiple of num_kv_heads");
+    if (head_dim < 32 || head_dim > 256 || head_dim % 32)
+        return fail(SPEC_ERR_INVALID, "head_dim must be a multiple of 32 in [32, 256]");
+    if (page_size < 1) return fail(SPEC_ERR_INVALID, "page_size < 1");
+    if (num_pages < 1 || max_pages_per_seq < 1)
+        return fail(SPEC_ERR_INVALID, "num_pages and max_pages_per_seq must be >= 1");
+    if (q_dtype != SPEC_DTYPE_F32 && q_dtype != SPEC_DTYPE_BF16)
+        return fail(SPEC_ERR_INVALID, "q_dtype must be F32 or BF16");
+    if (kv_dtype != SPEC_DTYPE_F32 && kv_dtype != SPEC_DTYPE_BF16 && kv_dtype != SPEC_DTYPE_I8)
+        return fail(SPEC_ERR_INVALID, "kv_dtype must be F32, BF16 or I8");
+    if (!(scale == scale)) return fail(SPEC_ERR_INVALID, "scale is NaN");
+    if (batch == 0) return SPEC_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out)
+        return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    if (kv_dtype == SPEC_DTYPE_I8 && (!k_scale || !v_scale))
+        return fail(SPEC_ERR_INVALID, "an I8 cache needs k_scale and v_scale");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return fail(SPEC_ERR_INVALID, "q, caches and out must be 16-byte aligned");
+    if ((int64_t)num_pages * num_kv_heads * page_size * head_dim >= (1LL << 40))
+        return fail(SPEC_ERR_INVALID, "cache too large");
+    const int64_t R = (int64_t)num_draft * (num_q_heads / num_kv_heads);
+    (void)dtype_size;
+
+    specv::AttnArgs a;
+    a.q = q; a.k_cache = k_cache; a.v_cache = v_cache;
+    a.k_scale = static_cast<const uint16_t*>(k_scale);
+    a.v_scale = static_cast<const uint16_t*>(v_scale);
+    a.block_table = block_table; a.ctx_lens = ctx_lens;
+    a.B = batch; a.k = num_draft; a.Hq = num_q_heads; a.Hkv = num_kv_heads; a.D = head_dim;
+    a.P = page_size; a.num_pages = num_pages; a.max_pages = max_pages_per_seq;
+    a.q_dtype = q_dtype; a.kv_dtype = kv_dtype; a.scale = scale;
+    a.out = out; a.lse = lse;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const int64_t path = g_opt_path.load();
+    const bool tc_ok = specv::tc_supported(a);
+    bool use_tc;
+    if (path == 1) use_tc = false;
+    else if (path == 2) {
+        if (!tc_ok)
+            return fail(SPEC_ERR_UNSUPPORTED, "tensor-core path forced but this shape/dtype is "
+                        "not supported by it");
+        use_tc = true;
+    } else use_tc = tc_ok;
+
+    Workspace* ws = nullptr;
+    int rc = get_workspace(0, &ws);
+    if (rc) return rc;
+    if (g_opt_validate.load()) {
+        rc = validate_tables(a, st);
+        if (rc) return rc;
+    }
+    cudaError_t e;
+    if (use_tc) {
+        int ctas = (int)g_opt_ctas.load();
+        if (ctas <= 0) ctas = ws->sms;
+        rc = get_workspace(specv::tc_workspace_bytes(a, ctas), &ws);
+        if (rc) return rc;
+        a.dev_err = static_cast<int*>(ws->base);
+        e = specv::launch_attn_tc(a, ctas, static_cast<char*>(ws->base) + kHeader, st);
+        if (e != cudaSuccess) return cuda_fail(e, "verify_attn (tensor-core) launch");
+    } else {
+        const specv::SimtPlan p = specv::simt_plan(a, ws->sms, (int)g_opt_simt_chunk.load());
+        const int64_t gy = (int64_t)batch * num_kv_heads * p.row_groups;
+        if (gy > 65535 || R > (1 << 20))
+            return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads too large for the SIMT path");
+        rc = get_workspace(specv::simt_workspace_bytes(a, p), &ws);
+        if (rc) return rc;
+        a.dev_err = static_cast<int*>(ws->base);
+        e = specv::launch_attn_simt(a, p, static_cast<char*>(ws->base) + kHeader, st);
+        if (e != cudaSuccess) return cuda_fail(e, "verify_attn (SIMT) launch");
+    }
+    return SPEC_OK;
+}
+
+int spec_accept_greedy(const void* logits, int32_t logits_dtype, const int32_t* draft_tokens,
+                       int32_t batch, int32_t num_draft, int64_t vocab, int32_t* accepted_len,
+                       int32_t* next_token, void* stream) {
+    g_err.clear();
+    if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
+    if (num_draft < 1 || num_draft > 64) return fail(SPEC_ERR_INVALID, "num_draft must be in [1, 64]");
+    if (vocab < 1 || vocab >= (1LL << 31)) return fail(SPEC_ERR_INVALID, "vocab must be in [1, 2^31)");
+    if (logits_dtype != SPEC_DTYPE_F32 && logits_dtype != SPEC_DTYPE_BF16)
+        return fail(SPEC_ERR_INVALID, "logits_dtype must be F32 or BF16");
+    if (batch == 0) return SPEC_OK;
+    if (batch > kMaxTickets) return fail(SPEC_ERR_UNSUPPORTED, "batch > %d", kMaxTickets);
+    if (!logits || !draft_tokens || !accepted_len || !next_token)
+        return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    if (!aligned16(logits)) return fail(SPEC_ERR_INVALID, "logits must be 16-byte aligned");
+    specv::AcceptArgs a;
+    a.logits = logits; a.dtype = logits_dtype; a.draft = draft_tokens; a.B = batch;
+    a.k = num_draft; a.V = vocab; a.accepted_len = accepted_len; a.next_token = next_token;
+    const int64_t blocks = (int64_t)batch * (num_draft + 1) * ((vocab + 8191) / 8192);
+    if (blocks >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "logits too large");
+    Workspace* ws = nullptr;
+    int rc = get_workspace(specv::accept_workspace_bytes(a), &ws);
+    if (rc) return rc;
+    int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws->base) + 256);
+    cudaError_t e = specv::launch_accept(a, static_cast<char*>(ws->base) + kHeader, tickets,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "accept_greedy launch");
+    return SPEC_OK;
+}
+
+int spec_device_error(int32_t* flags) {
+    g_err.clear();
+    if (!flags) return fail(SPEC_ERR_INVALID, "flags is NULL");
+    Workspace* ws = nullptr;
+    int rc = get_workspace(0, &ws);
+    if (rc) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, ws->base, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(ws->base, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    *flags = v;
+    return SPEC_OK;
+}
+
+int spec_release(void) {
+    g_err.clear();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if ((int)g_ws.size() > dev && g_ws[dev].base) {
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        cudaFree(g_ws[dev].base);
+        g_ws[dev].base = nullptr;
+        g_ws[dev].bytes = 0;
+    }
+    return SPEC_OK;
+}
+
+}  // extern "C"

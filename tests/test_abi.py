@@ -1,0 +1,109 @@
+"""The C-ABI library: it builds for sm_103a, loads, exports every symbol the
+public header declares, and rejects bad arguments before touching the GPU.
+Runs without a GPU (argument validation precedes every CUDA call)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_attn_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*SPEC_API\s+(?:int|const char \*)\s*(spec_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_calls():
+    syms = declared_symbols()
+    assert "spec_verify_attn" in syms and "spec_accept_greedy" in syms
+    from speculative_decoding_verification_attn_gb300 import binding
+    assert sorted(binding.EXPORTED) == syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.spec_version() >= 100
+
+
+def test_internal_symbols_are_hidden(lib):
+    with pytest.raises(AttributeError):
+        getattr(lib, "_ZN5specv9simt_planERKNS_8AttnArgsEii")
+
+
+def _attn(lib, **kw):
+    args = dict(q=16, kc=16, vc=16, ks=None, vs=None, bt=16, ctx=16, B=1, k=4, Hq=8, Hkv=2, D=128,
+                P=16, NP=8, MP=4, qdt=1, kvdt=1, scale=0.088, out=16, lse=None, stream=None)
+    args.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.spec_verify_attn(vp(args["q"]), vp(args["kc"]), vp(args["vc"]), vp(args["ks"]),
+                                vp(args["vs"]), vp(args["bt"]), vp(args["ctx"]), args["B"],
+                                args["k"], args["Hq"], args["Hkv"], args["D"], args["P"],
+                                args["NP"], args["MP"], args["qdt"], args["kvdt"], args["scale"],
+                                vp(args["out"]), vp(args["lse"]), vp(args["stream"]))
+
+
+@pytest.mark.parametrize("bad,needle", [
+    (dict(k=0), "num_draft"),
+    (dict(k=65), "num_draft"),
+    (dict(Hq=6, Hkv=4), "multiple"),
+    (dict(D=100), "head_dim"),
+    (dict(P=0), "page_size"),
+    (dict(qdt=3), "q_dtype"),
+    (dict(kvdt=2), "kv_dtype"),
+    (dict(q=0), "null"),
+    (dict(kvdt=3), "I8"),
+    (dict(q=24), "aligned"),
+    (dict(scale=float("nan")), "NaN"),
+])
+def test_attn_rejects_bad_arguments(lib, bad, needle):
+    rc = _attn(lib, **bad)
+    assert rc == -1
+    assert needle in lib.spec_last_error().decode()
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _attn(lib, B=0, q=None, kc=None, vc=None, out=None) == 0
+    assert lib.spec_last_error().decode() == ""
+
+
+@pytest.mark.parametrize("bad,needle", [
+    (dict(k=0), "num_draft"),
+    (dict(V=0), "vocab"),
+    (dict(dt=3), "logits_dtype"),
+    (dict(logits=0), "null"),
+    (dict(logits=18), "aligned"),
+])
+def test_accept_rejects_bad_arguments(lib, bad, needle):
+    a = dict(logits=16, dt=1, draft=16, B=2, k=4, V=1000, acc=16, nxt=16)
+    a.update(bad)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    rc = lib.spec_accept_greedy(vp(a["logits"]), a["dt"], vp(a["draft"]), a["B"], a["k"], a["V"],
+                                vp(a["acc"]), vp(a["nxt"]), None)
+    assert rc == -1
+    assert needle in lib.spec_last_error().decode()
+
+
+def test_options(lib):
+    assert lib.spec_set_option(0, 3) == -1
+    assert lib.spec_set_option(99, 0) == -1
+    assert lib.spec_set_option(0, 0) == 0
+    assert lib.spec_set_option(1, 0) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from speculative_decoding_verification_attn_gb300 import binding
+    with pytest.raises(RuntimeError):
+        binding._open(str(tmp_path / "missing.so"))

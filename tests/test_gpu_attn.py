@@ -1,0 +1,155 @@
+"""GPU parity of spec_verify_attn against the float64 oracle.
+
+Small cases (the oracle computes every output) span several 64-key tiles,
+ragged tails, contexts of zero, every supported page size, GQA groups of 1 to
+8 and 1 to 128 query rows per kv-head, forced stream-K splits of every size,
+both kernels; the named full-size workloads are checked on sampled rows at
+the launch configuration the benchmark times.  NaN canaries fill every
+unused cache slot: a kernel that reads past a sequence shows non-finite
+output.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_verification_attn_gb300 import binding
+from speculative_decoding_verification_attn_gb300.workload import (
+    WORKLOADS, make_inputs, small_spec)
+
+from gpu_util import (assert_attn_close, check_attn_full, check_attn_sampled, full_inputs,
+                      gpu_attn, tol_for)
+from _util import oracle_attn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    from speculative_decoding_verification_attn_gb300 import build
+    build.build()
+    binding.load()
+    for opt in range(4):
+        binding.spec_set_option(opt, 0)
+    yield
+    for opt in range(4):
+        binding.spec_set_option(opt, 0)
+
+
+SMALL_BF16 = [
+    dict(),
+    dict(num_q_heads=4, num_kv_heads=4, num_draft=1),                    # 1 row per kv-head
+    dict(num_q_heads=28, num_kv_heads=4, num_draft=16, page_size=32),     # 112 rows
+    dict(num_q_heads=16, num_kv_heads=2, num_draft=8),                    # 64 rows
+    dict(num_q_heads=4, num_kv_heads=2, num_draft=64),                    # 128 rows
+    dict(ctx=[0, 1, 63, 64, 65], batch=5, num_draft=3),                   # tile edges
+    dict(page_size=8, ctx=(1, 200)),
+    dict(page_size=64, ctx=(1, 400)),
+    dict(page_size=128, ctx=(100, 600)),
+    dict(page_size=256, ctx=(250, 700), batch=2),
+    dict(batch=1, num_q_heads=8, num_kv_heads=1, ctx=[3000]),              # one long segment
+    dict(num_q_heads=7, num_kv_heads=7, num_draft=5, ctx=(0, 130)),
+]
+
+
+@pytest.mark.parametrize("kw", SMALL_BF16, ids=[str(i) for i in range(len(SMALL_BF16))])
+def test_tensor_core_small(oracle_mod, kw):
+    inp = make_inputs(small_spec(**kw), seed=21)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    check_attn_full(oracle_mod, inp, str(kw))
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 5, 37, 152, 400])
+def test_tensor_core_stream_k_splits(oracle_mod, ctas):
+    inp = make_inputs(small_spec(batch=4, num_q_heads=16, num_kv_heads=4, num_draft=6,
+                                 ctx=(0, 900)), seed=22)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
+    check_attn_full(oracle_mod, inp, "ctas=%d" % ctas)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(kv_dtype="i8"),
+    dict(kv_dtype="i8", num_q_heads=16, num_kv_heads=2, num_draft=8),
+    dict(q_dtype="f32", kv_dtype="f32", head_dim=64),
+    dict(q_dtype="f32", kv_dtype="i8", head_dim=256, num_draft=2),
+    dict(q_dtype="bf16", kv_dtype="f32", head_dim=32, page_size=5, ctx=(0, 77)),
+    dict(head_dim=96, page_size=3, ctx=[0, 10, 31]),
+])
+@pytest.mark.parametrize("chunk", [0, 16, 48])
+def test_simt_small(oracle_mod, kw, chunk):
+    inp = make_inputs(small_spec(**kw), seed=23)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 1)
+    binding.spec_set_option(binding.SPEC_OPT_SIMT_CHUNK, chunk)
+    check_attn_full(oracle_mod, inp, "%s chunk=%d" % (kw, chunk))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_fp32_workload(oracle_mod, seed):
+    check_attn_full(oracle_mod, make_inputs("tiny_fp32", seed=seed), "tiny_fp32")
+
+
+def test_tensor_core_matches_simt():
+    inp = make_inputs(small_spec(batch=6, num_q_heads=12, num_kv_heads=3, num_draft=5,
+                                 ctx=(0, 700)), seed=24)
+    t = binding.inputs_to_torch(inp)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    a_out, a_lse = gpu_attn(inp, t)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 1)
+    b_out, b_lse = gpu_attn(inp, t)
+    assert np.abs(a_out - b_out).max() < 2e-2
+    assert np.abs(a_lse - b_lse).max() < 2e-3
+
+
+@pytest.mark.parametrize("name", ["mha7b_bf16", "gqa8b_ragged_bf16", "long_step_k16_bf16",
+                                  "int8kv_70b_layer"])
+def test_named_workload_sampled(oracle_mod, name):
+    inp = full_inputs(name, 0)
+    check_attn_sampled(oracle_mod, inp, n=40, what=name)
+
+
+def test_lse_optional(oracle_mod):
+    inp = make_inputs(small_spec(), seed=25)
+    t = binding.inputs_to_torch(inp)
+    o = binding.alloc_outputs(inp)
+    binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["ctx_lens"],
+                             inp.spec.num_draft, inp.scale, o["out"], None)
+    torch.cuda.synchronize()
+    ref, _ = oracle_attn(oracle_mod, inp)
+    assert np.abs(o["out"].double().cpu().numpy() - ref).max() < 2e-2
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_bad_page_id_is_clamped_and_flagged(path):
+    inp = make_inputs(small_spec(), seed=26)
+    inp.block_table[0, 0] = inp.num_pages + 5
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, path)
+    assert binding.spec_device_error() == 0
+    out, _ = gpu_attn(inp)
+    assert binding.spec_device_error() == binding.SPEC_DEVERR_PAGE
+    assert np.isfinite(out[1:]).all()
+
+
+def test_validate_option_rejects_bad_tables():
+    inp = make_inputs(small_spec(), seed=27)
+    inp.block_table[1, 0] = -1
+    binding.spec_set_option(binding.SPEC_OPT_VALIDATE, 1)
+    with pytest.raises(binding.SpecError, match="block_table"):
+        gpu_attn(inp)
+    inp2 = make_inputs(small_spec(), seed=27)
+    inp2.ctx_lens[0] = inp2.max_pages * inp2.spec.page_size
+    with pytest.raises(binding.SpecError, match="ctx_lens"):
+        gpu_attn(inp2)
+
+
+def test_misaligned_pointer_rejected():
+    inp = make_inputs(small_spec(), seed=28)
+    t = binding.inputs_to_torch(inp)
+    o = binding.alloc_outputs(inp)
+    flat = torch.empty(t["q"].numel() + 8, dtype=torch.bfloat16, device="cuda")
+    q_bad = flat[1:1 + t["q"].numel()].view(t["q"].shape)
+    with pytest.raises(binding.SpecError, match="aligned"):
+        binding.spec_verify_attn(q_bad, t["k_cache"], t["v_cache"], t["block_table"],
+                                 t["ctx_lens"], inp.spec.num_draft, inp.scale, o["out"], o["lse"])
