@@ -1,0 +1,388 @@
+"""Benchmark of the verification hot path (attention + greedy acceptance).
+
+One step = spec_verify_attn + spec_accept_greedy over one batch of a named
+synthetic workload (default: the 7B-target bf16 shape -- batch 8, 32 q/kv
+heads, head_dim 128, context 2048, k = 8, page size 16, vocab 32000).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the float64 CPU oracle, same metric
+
+Prints one JSON line.  `value` is verified draft tokens per second (B*k per
+step / device step time, inputs resident in HBM); `e2e` is the same metric
+through the public API with the per-step inputs copied from pinned host
+memory and the results read back inside the timed region; `roofline` relates
+the attention call's algorithmic bytes to its measured time and to the
+measured HBM copy bandwidth.  With N > 1 (torchrun) every rank runs its own
+replica on its own GPU (the path has no cross-GPU exchange); the slowest
+rank's time counts and `value` sums all ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_attn_gb300.workload import (  # noqa: E402
+    WORKLOADS, algorithmic_bytes, make_inputs)
+
+DEFAULT_WORKLOAD = "mha7b_bf16"
+METRIC = "verified draft tokens/sec"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: int, rank_seconds: float, world: int, device=None):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    slowest = reduce_max(rank_seconds, world, device)
+    return units_per_rank * world / slowest, slowest
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_attn_gb300",
+                                           "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "verify_attn_%s.md" % workload)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        smax = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if s[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_step_estimate(inp, target_s: float, seed: int = 0):
+    """Time the float64 oracle on a bounded sample of one step and scale it to
+    the whole step.  Returns (seconds per full step, description)."""
+    import oracle
+    s = inp.spec
+    B, k, Hq = s.batch, s.num_draft, s.num_q_heads
+    rows_total = B * k * Hq
+    rng = np.random.default_rng(seed)
+    all_rows = np.stack(np.meshgrid(np.arange(B), np.arange(k), np.arange(Hq), indexing="ij"),
+                        -1).reshape(-1, 3).astype(np.int32)
+    # calibrate on a few rows, then fill the time budget
+    probe = all_rows[rng.choice(rows_total, size=min(8, rows_total), replace=False)]
+    t0 = time.perf_counter()
+    oracle.attn_rows(inp.q, s.q_dtype, inp.k_cache, inp.v_cache, s.kv_dtype, inp.k_scale,
+                     inp.v_scale, inp.block_table, inp.ctx_lens, inp.scale, probe)
+    per_row = max((time.perf_counter() - t0) / len(probe), 1e-7)
+    n = int(min(rows_total, max(len(probe), target_s * 0.8 / per_row)))
+    rows = all_rows[rng.choice(rows_total, size=n, replace=False)]
+    t0 = time.perf_counter()
+    oracle.attn_rows(inp.q, s.q_dtype, inp.k_cache, inp.v_cache, s.kv_dtype, inp.k_scale,
+                     inp.v_scale, inp.block_table, inp.ctx_lens, inp.scale, rows)
+    t_attn = (time.perf_counter() - t0) * rows_total / n
+    t0 = time.perf_counter()
+    oracle.accept_greedy(inp.logits, s.logits_dtype, inp.draft_tokens)
+    t_acc = time.perf_counter() - t0
+    desc = ("%d of %d attention rows (b, i, h) timed and scaled by %.1fx, plus acceptance "
+            "over all %d sequences; single-threaded C float64 oracle" %
+            (n, rows_total, rows_total / n, B))
+    return t_attn + t_acc, desc
+
+
+def run_reference(args, inp, world, rank):
+    """--impl reference: the oracle as it stands on the host cores."""
+    if rank != 0:
+        return
+    s = inp.spec
+    units = s.batch * s.num_draft
+    per_step_budget = 1.0
+    for _ in range(args.warmup):
+        oracle_step_estimate(inp, per_step_budget, seed=1000)
+    times, desc = [], ""
+    for st in range(args.steps):
+        t, desc = oracle_step_estimate(inp, per_step_budget, seed=st)
+        times.append(t)
+    t_step = float(np.mean(times))
+    value = units / t_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(inp, "host memory (CPU oracle)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(inp, l2_note):
+    s = inp.spec
+    ctx = s.ctx if isinstance(s.ctx, int) else [int(inp.ctx_lens.min()), int(inp.ctx_lens.max())]
+    return {"workload": s.name, "batch": s.batch, "q_heads": s.num_q_heads,
+            "kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "ctx": ctx,
+            "num_draft": s.num_draft, "page_size": s.page_size, "vocab": s.vocab,
+            "kv_dtype": s.kv_dtype, "seed": inp.seed, "l2": l2_note, "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- GPU run
+
+def run_gpu(args, inp, world, rank, local):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_verification_attn_gb300 import binding
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    binding.load()
+    s = inp.spec
+    k, scale = s.num_draft, inp.scale
+    nbytes = algorithmic_bytes(inp)
+    units = s.batch * k
+
+    base = binding.inputs_to_torch(inp, device)
+    # rotate over enough input copies that one step's inputs are out of L2
+    # by the time they are used again
+    n_sets = max(2, math.ceil(2.5 * L2_BYTES / nbytes["total"]))
+    sets = [base] + [{n: v.clone() for n, v in base.items()} for _ in range(n_sets - 1)]
+    outs = [binding.alloc_outputs(inp, device) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream()
+
+    def step(j):
+        t, o = sets[j % n_sets], outs[j % n_sets]
+        binding.run_verify(t, o, k, scale)
+
+    for j in range(max(args.warmup, 3)):
+        step(j)
+    torch.cuda.synchronize()
+
+    # attention / acceptance / step times from events on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        # keep the GPU under the same load for ~1 s so the sampler sees it
+        t_pad = time.perf_counter()
+        j = 0
+        while time.perf_counter() - t_pad < 1.0:
+            step(j)
+            j += 1
+            if j % 64 == 0:
+                torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for j in range(args.steps):
+            t, o = sets[j % n_sets], outs[j % n_sets]
+            ev[j][0].record(stream)
+            binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                     t["ctx_lens"], k, scale, o["out"], o["lse"],
+                                     t.get("k_scale"), t.get("v_scale"))
+            ev[j][1].record(stream)
+            binding.spec_accept_greedy(t["logits"], t["draft_tokens"], k, o["accepted_len"],
+                                       o["next_token"])
+            ev[j][2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    clocks = clk.summary()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    acc_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    value, slowest_step_s = aggregate(units, total_ms / 1e3 / args.steps, world, device)
+    ms_per_step = slowest_step_s * 1e3
+
+    # end to end through the public API: per-step inputs from pinned host
+    # memory, results read back, every step
+    host_names = ["q", "logits", "draft_tokens", "block_table", "ctx_lens"]
+    host = binding.inputs_to_torch(inp, pin=True)
+    h_in = {n: host[n] for n in host_names}
+    h_out = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+             for n, v in outs[0].items()}
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+
+    def e2e_step(j):
+        t, o = sets[j % n_sets], outs[j % n_sets]
+        for n in host_names:
+            t[n].copy_(h_in[n], non_blocking=True)
+        binding.run_verify(t, o, k, scale)
+        for n, v in o.items():
+            h_out[n].copy_(v, non_blocking=True)
+
+    for j in range(max(args.warmup, 3)):
+        e2e_step(j)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for j in range(args.steps):
+        e2e_step(j)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _ = aggregate(units, e0.elapsed_time(e1) / 1e3 / args.steps, world, device)
+
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes["attn"] / (attn_ms / 1e3) / 1e9
+    traffic = profiled_traffic(s.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if s.q_dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) q/K/V, N(0,2) logits; no datasets or weights)",
+        "config": workload_config(inp, "inputs > L2: %d rotating copies of %.0f MB" %
+                                  (n_sets, nbytes["total"] / 1e6)),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * launches_per_step(inp),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "spec_verify_attn (attention + split-KV combine)",
+                     "peak_source": peak_kind, "attn_ms": attn_ms, "accept_ms": acc_ms,
+                     "attn_bytes": nbytes["attn"], "step_bytes": nbytes["total"],
+                     "step_frac": nbytes["total"] / (ms_per_step / 1e3) / 1e9 / peak},
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        t_cpu, desc = oracle_step_estimate(inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": units / t_cpu, "unit": UNIT, "cores": 1,
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def launches_per_step(inp) -> int:
+    # attention kernel + split-KV combine kernel + acceptance kernel
+    return 3
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, make_inputs(args.workload, args.seed, canary=False), world, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    inp = make_inputs(args.workload, args.seed, canary=False)
+    run_gpu(args, inp, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -608,19 +608,25 @@ combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
     const int row = blockIdx.y * 8 + warp;
     if (row >= R) return;
 
+    // CTA c covers tiles [c*T/C, (c+1)*T/C); a CTA with an empty range wrote
+    // nothing and is skipped
+    auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
     float m = -INFINITY;
     for (int c = c_first; c <= c_last; ++c) {
+        if (empty(c)) continue;
         const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
         m = fmaxf(m, part_lse[(int64_t)slot * ROWS + row]);
     }
     float tsum = 0.f;
     for (int c = c_first; c <= c_last; ++c) {
+        if (empty(c)) continue;
         const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
         tsum += expf(part_lse[(int64_t)slot * ROWS + row] - m);
     }
     const float lse_tot = m + logf(tsum);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = c_first; c <= c_last; ++c) {
+        if (empty(c)) continue;
         const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
         const float w = expf(part_lse[(int64_t)slot * ROWS + row] - lse_tot);
         const float4 v = reinterpret_cast<const float4*>(part_o + ((int64_t)slot * ROWS + row) * D)[lane];

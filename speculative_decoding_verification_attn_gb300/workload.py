@@ -247,7 +247,7 @@ def make_inputs(spec: Union[WorkloadSpec, str], seed: int = 0, canary: bool = Tr
     if spec.draft_mode == "geometric_break":
         # positions agree until the first miss; every later one is a miss
         match = np.cumprod(match, axis=1).astype(bool)
-    if spec.draft_mode == "uniform":
+    if spec.draft_mode == "uniform" or V == 1:
         other = r_tok.integers(0, V, size=(B, k))
     else:
         # uniform over the V-1 tokens that differ from the target's argmax
