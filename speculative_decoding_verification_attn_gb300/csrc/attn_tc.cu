@@ -8,9 +8,15 @@
 // keys 0 .. ctx_b + i; kv-head g serves q-heads g*G .. g*G+G-1.
 //
 // Design (GB300 / sm_103a):
-//  * All k*G query rows of one (sequence, kv-head) form the M side of one
-//    128-row MMA tile, so every K/V byte is read from HBM exactly once and
-//    reused k*G times (the sequence-parallel amortisation the blog describes).
+//  * All R = k*G query rows of one (sequence, kv-head) sit on the M side of
+//    one 128-row MMA, so every K/V byte is read from HBM exactly once and
+//    reused R times (the sequence-parallel amortisation the blog describes).
+//    When R <= 64 the rows are replicated REP = 128 / roundup32(R) times
+//    (4 copies for R <= 32, 2 for R <= 64), one copy per group of TMEM lane
+//    quadrants, and copy c only keeps the keys of column slice c of every
+//    64-key tile: the softmax work of a tile is spread over all four warps
+//    instead of the one warp that owns lanes 0..R-1, and the copies' partial
+//    (max, sum, O) are merged once per segment.
 //  * Work is the list of 64-key tiles of every (sequence, kv-head) segment,
 //    split evenly over a persistent grid of one CTA per SM (stream-K).  A CTA
 //    walks a contiguous tile range that may cross segment boundaries; a
@@ -18,13 +24,15 @@
 //    combine kernel merges with log-sum-exp weights (split-KV).
 //  * Warp roles: warp 4 = TMA producer (page-table driven: one 2-D box per
 //    (page, head-dim half)), warp 5 = MMA issuer and TMEM owner, warps 0-3 =
-//    softmax / rescale / epilogue, one query row per thread (TMEM lane).
+//    softmax / rescale / epilogue, one (copy, query row) per thread.
 //  * S = Q K^T lands in TMEM (double buffered), the softmax warps turn it into
 //    bf16 P in place, and O += P V takes P straight from TMEM.  The running
-//    max is only moved when it grows by more than 2^8, so O is rarely
-//    rescaled (exact in real arithmetic: O and l share the reference max).
+//    max only moves when it grows by more than 2^8, so O is rarely rescaled
+//    (exact in real arithmetic: O and l share the reference max), and a tile's
+//    P is released without waiting for the previous tile's P V.
 //  * Every mbarrier wait is bounded (1 s); a timeout sets the device error
-//    word and an abort flag that makes every role drain and return.
+//    word and an abort flag after which every role skips its remaining work
+//    (still passing every CTA barrier) and returns.
 #include <cuda.h>
 #include <math.h>
 
@@ -36,7 +44,7 @@ namespace {
 constexpr int D = 128;
 constexpr int TN = 64;           // keys per tile
 constexpr int NS = 4;            // K/V pipeline stages
-constexpr int ROWS = 128;        // MMA M: query rows (padded)
+constexpr int ROWS = 128;        // MMA M: query rows (padded / replicated)
 constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
 constexpr int KV_HALF = TN * 128;         // 8 KB
@@ -65,18 +73,30 @@ struct Smem {
                          B_QEMPTY = 3 * NS + 2, B_SFULL = 3 * NS + 4, B_PFULL = 3 * NS + 6,
                          B_ODONE = 3 * NS + 8, B_DRAIN = 3 * NS + 9, NUM_BARS = 3 * NS + 10;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
-    static constexpr int PIDS = MISC + 16;                     // [LOOKAHEAD+1][MAX_BOX] int
+    static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
+    static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
     static constexpr int CTX = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;  // [MAX_BATCH] int
     static constexpr int PRE = CTX + MAX_BATCH * 4;           // [MAX_BATCH+1] int
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
 };
 constexpr size_t SMEM_BYTES = Smem::END + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct TcParams {
     AttnArgs a;
     float* part_o;    // [2*C][ROWS][D]
     float* part_lse;  // [2*C][ROWS]
 };
+
+// Row replication: RQ rows per copy (R rounded up to 32), REP copies.
+__host__ __device__ constexpr int rows_per_copy(int R) { return ((R + 31) / 32) * 32; }
+__host__ __device__ constexpr int num_copies(int R) {
+    return (ROWS % rows_per_copy(R) == 0) ? ROWS / rows_per_copy(R) : 1;
+}
+// Row `row` of the 128-row Q tile holds real query data.
+__device__ __forceinline__ bool q_row_used(int row, int R, int RQ, int REP) {
+    return row / RQ < REP && row % RQ < R;
+}
 
 // Walks a CTA's tile range: tile -> (sequence b, kv-head, tile-in-segment).
 struct Cursor {
@@ -139,6 +159,320 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) return;
 }
 
+// What every role of a CTA shares.
+struct Cta {
+    const AttnArgs* a;
+    const TcParams* prm;
+    uint8_t* sm;
+    uint64_t* bars;
+    volatile int* abort_flag;
+    const int* s_ctx;
+    const int* s_pre;
+    uint32_t tmem;
+    int64_t t_begin, t_end;
+    int n_tiles, R, G;
+};
+
+// Load CW consecutive fp32 TMEM columns of this thread's lane.
+template <int CW>
+__device__ __forceinline__ void load_cols(uint32_t taddr, uint32_t (&v)[CW]) {
+    if constexpr (CW == 16) {
+        tmem_ld16(taddr, v);
+    } else if constexpr (CW == 32) {
+        tmem_ld32(taddr, v);
+    } else {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        tmem_ld32(taddr, lo);
+        tmem_ld32(taddr + 32, hi);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void store_cols(uint32_t taddr, const uint32_t* v) {
+    if constexpr (N == 8) {
+        tmem_st8(taddr, v);
+    } else if constexpr (N == 16) {
+        tmem_st16(taddr, v);
+    } else {
+        tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(v));
+    }
+}
+
+// ================= softmax / rescale / epilogue (warps 0-3) =================
+template <int REP>
+__device__ void softmax_role(const Cta& x) {
+    constexpr int RQ = REP == 4 ? 32 : REP == 2 ? 64 : ROWS;
+    constexpr int CW = TN / REP;  // key columns of a tile owned by one copy
+    const AttnArgs& a = *x.a;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R = x.R, G = x.G, k = a.k;
+    const int c = (warp * 32) / RQ;                 // copy of this thread
+    const int r = warp * 32 + lane - c * RQ;        // query row inside the copy
+    const bool warp_active = c < REP && warp * 32 - c * RQ < R;
+    const bool row_valid = warp_active && r < R;
+    const int i_row = row_valid ? r / G : k - 1;
+    const int cbase = c * CW;
+    const float sl2 = a.scale * kLog2e;
+    const uint32_t lane_base = x.tmem + ((uint32_t)(warp * 32) << 16);
+    float* s_stat_m = reinterpret_cast<float*>(x.sm + Smem::STAT);
+    float* s_stat_l = s_stat_m + 4 * ROWS;
+    uint64_t* bars = x.bars;
+
+    float m_ref = -INFINITY, l = 0.f;
+    Cursor cur;
+    if (x.n_tiles > 0) cur.init(x.t_begin, x.s_pre, x.s_ctx, a.B, a.Hkv, k);
+    bool ok = true;
+    int pc = -1;
+    for (int it = 0; it < x.n_tiles; ++it) {
+        const bool first = (it == 0) || (cur.lt == 0);
+        const bool last = (it == x.n_tiles - 1) || (cur.lt == cur.nb - 1);
+        if (first) ++pc;
+        const int sb = it & 1, s = it % NS;
+        const int ctx = x.s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
+        const int nvalid = min(TN, L - key0);
+        if (first) {
+            m_ref = -INFINITY;
+            l = 0.f;
+        }
+        // s_full(it) also implies every P V up to tile it-2 has finished
+        if (ok) ok = warp_wait(&bars[Smem::B_SFULL + sb], (it >> 1) & 1, x.abort_flag, a.dev_err);
+        if (ok && warp_active) {
+            tc_fence_after();
+            uint32_t sr[CW];
+            load_cols<CW>(lane_base + TM_S + sb * TN + cbase, sr);
+            tmem_wait_ld();
+            // keys of this row visible in this copy's slice: cc < cmax
+            const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
+            float mt = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < CW; ++cc)
+                if (cc < cmax) mt = fmaxf(mt, __uint_as_float(sr[cc]) * sl2);
+            const float m_new = fmaxf(m_ref, mt);
+            float alpha = 1.f;
+            const bool move = m_new > m_ref + kRescaleThreshold;  // also -inf -> finite
+            if (move) {
+                alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+                m_ref = m_new;
+                l *= alpha;
+            }
+            uint32_t pk[CW / 2];
+            float psum = 0.f;
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 2; ++c2) {
+                const int cc = 2 * c2;
+                const float p0 = cc < cmax ? fast_exp2(__uint_as_float(sr[cc]) * sl2 - m_ref) : 0.f;
+                const float p1 =
+                    cc + 1 < cmax ? fast_exp2(__uint_as_float(sr[cc + 1]) * sl2 - m_ref) : 0.f;
+                psum += p0 + p1;
+                pk[c2] = pack_bf16x2(p0, p1);
+            }
+            l += psum;
+            // P of this copy's slice; the other copies' slices of this lane are 0
+            const uint32_t zero[CW / 2] = {};
+#pragma unroll
+            for (int cc = 0; cc < REP; ++cc) {
+                if (cc == c)
+                    store_cols<CW / 2>(lane_base + TM_S + sb * TN + cc * (CW / 2), pk);
+                else
+                    store_cols<CW / 2>(lane_base + TM_S + sb * TN + cc * (CW / 2), zero);
+            }
+            tmem_wait_st();
+            if (!first && __any_sync(0xffffffffu, move)) {
+                // O must hold every earlier P V before it is rescaled
+                ok = warp_wait(&bars[Smem::B_ODONE], (it - 1) & 1, x.abort_flag, a.dev_err);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c4 = 0; c4 < D / 32; ++c4) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + TM_O + c4 * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(lane_base + TM_O + c4 * 32, ov);
+                    }
+                    tmem_wait_st();
+                }
+            }
+        }
+        if (ok && nvalid < TN && warp == 0) {
+            // rows past the last key of the sequence: zero V so that
+            // 0 * (stale or canary) never reaches the accumulator
+            ok = warp_wait(&bars[Smem::B_VFULL + s], (it / NS) & 1, x.abort_flag, a.dev_err);
+            if (ok) {
+                uint8_t* vst = x.sm + Smem::STAGES + s * STAGE_BYTES + KV_BYTES;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                for (int e = nvalid * 8 + lane; e < TN * 8; e += 32) {
+                    const int row = e / 8, chunk = e % 8;
+                    *reinterpret_cast<uint4*>(vst + row * 128 + chunk * 16) = z;
+                    *reinterpret_cast<uint4*>(vst + KV_HALF + row * 128 + chunk * 16) = z;
+                }
+                fence_proxy_async_smem();
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[Smem::B_PFULL + sb]);
+
+        if (last) {
+            // ---- epilogue of the piece that ends at this tile
+            const int qb = pc & 1;
+            if (ok && warp_active) {
+                // observe P V(it-1) before P V(it) so the parity wait is unambiguous
+                if (!first)
+                    ok = warp_wait(&bars[Smem::B_ODONE], (it - 1) & 1, x.abort_flag, a.dev_err);
+                if (ok) ok = warp_wait(&bars[Smem::B_ODONE], it & 1, x.abort_flag, a.dev_err);
+                tc_fence_after();
+            }
+            const bool complete = cur.seg_start >= x.t_begin && cur.seg_start + cur.nb <= x.t_end;
+            const int slot = 2 * blockIdx.x + (cur.seg_start < x.t_begin ? 0 : 1);
+            auto out_row = [&](int rr) {
+                return ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+            };
+            if constexpr (REP == 1) {
+                if (ok && warp_active) {
+                    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+                    const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll
+                    for (int c4 = 0; c4 < D / 32; ++c4) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + TM_O + c4 * 32, ov);
+                        tmem_wait_ld();
+                        if (!row_valid) continue;
+                        if (complete) {
+                            uint4* dst = reinterpret_cast<uint4*>(
+                                static_cast<__nv_bfloat16*>(a.out) + out_row(r) * D + c4 * 32);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l,
+                                                  __uint_as_float(ov[8 * v + 1]) * inv_l);
+                                w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l,
+                                                  __uint_as_float(ov[8 * v + 3]) * inv_l);
+                                w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l,
+                                                  __uint_as_float(ov[8 * v + 5]) * inv_l);
+                                w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l,
+                                                  __uint_as_float(ov[8 * v + 7]) * inv_l);
+                                dst[v] = w;
+                            }
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(
+                                x.prm->part_o + ((int64_t)slot * ROWS + r) * D + c4 * 32);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                dst[v] = make_float4(__uint_as_float(ov[4 * v + 0]) * inv_l,
+                                                     __uint_as_float(ov[4 * v + 1]) * inv_l,
+                                                     __uint_as_float(ov[4 * v + 2]) * inv_l,
+                                                     __uint_as_float(ov[4 * v + 3]) * inv_l);
+                        }
+                    }
+                    if (row_valid) {
+                        if (complete) {
+                            if (a.lse) a.lse[out_row(r)] = lse;
+                        } else {
+                            x.prm->part_lse[(int64_t)slot * ROWS + r] = lse;
+                        }
+                    }
+                }
+            } else {
+                // merge the REP copies of every row: weights from (m, l), the
+                // weighted O rows summed in fp32 in the Q buffer of this piece
+                // (its QK MMAs are done), rows swizzled by 16-byte chunk
+                if (row_valid) {
+                    s_stat_m[c * ROWS + r] = m_ref;
+                    s_stat_l[c * ROWS + r] = l;
+                }
+                named_bar_sync(1, 128);
+                float w = 0.f, lse = -INFINITY;
+                if (row_valid) {
+                    float mt = -INFINITY;
+#pragma unroll
+                    for (int cc = 0; cc < REP; ++cc) mt = fmaxf(mt, s_stat_m[cc * ROWS + r]);
+                    float Lsum = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < REP; ++cc) {
+                        const float mc = s_stat_m[cc * ROWS + r];
+                        if (mc != -INFINITY) Lsum += s_stat_l[cc * ROWS + r] * fast_exp2(mc - mt);
+                    }
+                    w = (Lsum > 0.f && m_ref != -INFINITY) ? fast_exp2(m_ref - mt) / Lsum : 0.f;
+                    lse = Lsum > 0.f ? (mt + log2f(Lsum)) * kLn2 : -INFINITY;
+                }
+                float* scratch = reinterpret_cast<float*>(x.sm + Smem::Q + qb * Q_BYTES);
+#pragma unroll 1
+                for (int cc = 0; cc < REP; ++cc) {
+                    if (ok && warp_active && c == cc) {
+#pragma unroll
+                        for (int c4 = 0; c4 < D / 32; ++c4) {
+                            uint32_t ov[32];
+                            tmem_ld32(lane_base + TM_O + c4 * 32, ov);
+                            tmem_wait_ld();
+                            if (!row_valid) continue;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const int chunk = c4 * 8 + v;
+                                float4* dst = reinterpret_cast<float4*>(
+                                    scratch + r * D + ((chunk ^ (r & 31)) * 4));
+                                float4 o = make_float4(__uint_as_float(ov[4 * v + 0]) * w,
+                                                       __uint_as_float(ov[4 * v + 1]) * w,
+                                                       __uint_as_float(ov[4 * v + 2]) * w,
+                                                       __uint_as_float(ov[4 * v + 3]) * w);
+                                if (cc > 0) {
+                                    const float4 prev = *dst;
+                                    o.x += prev.x;
+                                    o.y += prev.y;
+                                    o.z += prev.z;
+                                    o.w += prev.w;
+                                }
+                                *dst = o;
+                            }
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                }
+                if (ok) {
+                    for (int idx = tid; idx < R * (D / 4); idx += 128) {
+                        const int rr = idx / (D / 4), chunk = idx % (D / 4);
+                        const float4 o = *reinterpret_cast<const float4*>(
+                            scratch + rr * D + ((chunk ^ (rr & 31)) * 4));
+                        if (complete) {
+                            uint2 w2;
+                            w2.x = pack_bf16x2(o.x, o.y);
+                            w2.y = pack_bf16x2(o.z, o.w);
+                            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                     out_row(rr) * D)[chunk] = w2;
+                        } else {
+                            reinterpret_cast<float4*>(
+                                x.prm->part_o + ((int64_t)slot * ROWS + rr) * D)[chunk] = o;
+                        }
+                    }
+                    if (row_valid && c == 0) {
+                        if (complete) {
+                            if (a.lse) a.lse[out_row(r)] = lse;
+                        } else {
+                            x.prm->part_lse[(int64_t)slot * ROWS + r] = lse;
+                        }
+                    }
+                }
+                named_bar_sync(1, 128);
+                // restore the zero padding rows the scratch overwrote
+                uint4* q4 = reinterpret_cast<uint4*>(scratch);
+                for (int e = tid; e < R * D * 4 / 16; e += 128) {
+                    const int row = (e % (Q_HALF / 16)) / 8;
+                    if (!q_row_used(row, R, RQ, REP)) q4[e] = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            // the Q buffer of this piece may now be reloaded
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Smem::B_QEMPTY + qb]);
+        }
+        if (it + 1 < x.n_tiles) cur.next(x.s_ctx, a.Hkv, k);
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const TcParams prm) {
@@ -155,6 +489,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, k = a.k, Hkv = a.Hkv, G = a.Hq / a.Hkv, R = k * G, P = a.P;
+    const int RQ = rows_per_copy(R), REP = num_copies(R);
     const int BH = P < TN ? P : TN;  // box height (keys per TMA box)
 
     // ---- setup: barriers, TMEM, zero Q pad rows, per-sequence tile prefix
@@ -166,7 +501,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         for (int q = 0; q < 2; ++q) {
             mbar_init(&bars[Smem::B_QFULL + q], 1);
-            mbar_init(&bars[Smem::B_QEMPTY + q], 1);
+            mbar_init(&bars[Smem::B_QEMPTY + q], 1 + 4);  // MMA commit + 4 softmax warps
             mbar_init(&bars[Smem::B_SFULL + q], 1);
             mbar_init(&bars[Smem::B_PFULL + q], 4);
         }
@@ -180,12 +515,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tmem_relinquish();
     }
     {
-        // rows R..127 of both Q buffers stay zero for the whole kernel
+        // rows that hold no query stay zero in both Q buffers
         uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
-        const uint4 z = make_uint4(0, 0, 0, 0);
         for (int e = tid; e < 2 * Q_BYTES / 16; e += THREADS) {
             const int row = (e % (Q_HALF / 16)) / 8;
-            if (row >= R) q4[e] = z;
+            if (!q_row_used(row, R, RQ, REP)) q4[e] = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
     }
@@ -239,7 +573,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
         }
-        // block-table entries of tile `ah` -> ring slot (cp.async, lookahead)
+        // block-table entries of a tile -> ring slot (cp.async, LOOKAHEAD tiles ahead)
         auto fetch_pids = [&](int slot, const Cursor& c) {
             const int key0 = c.lt * TN;
             const int L = s_ctx[c.b] + k;
@@ -258,7 +592,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             cp_async_commit();
         }
-        int pc = -1;  // piece counter
+        int pc = -1;      // piece counter
+        int n_issued = 0; // tiles whose K/V loads were issued
         int issued_q[2] = {0, 0};
         bool ok = true;
         for (int it = 0; it < n_tiles && ok; ++it) {
@@ -278,10 +613,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         ok = mbar_wait(&bars[Smem::B_QEMPTY + qb], (use - 1) & 1, abort_flag,
                                        a.dev_err);
                     if (ok) {
-                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL + qb], 2 * R * 128);
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_3d(sm + Smem::Q + qb * Q_BYTES + h * Q_HALF, &qmap,
-                                        &bars[Smem::B_QFULL + qb], h * 64, cur.kvh * G, cur.b * k);
+                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL + qb], REP * 2 * R * 128);
+                        for (int c = 0; c < REP; ++c)
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_3d(sm + Smem::Q + qb * Q_BYTES + h * Q_HALF + c * RQ * 128,
+                                            &qmap, &bars[Smem::B_QFULL + qb], h * 64, cur.kvh * G,
+                                            cur.b * k);
                         issued_q[qb] = use + 1;
                     }
                 }
@@ -319,6 +656,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                         &bars[Smem::B_VFULL + s], h * 64, row, pol);
                         }
                     }
+                    n_issued = it + 1;
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -327,10 +665,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         cp_async_wait<0>();
         if (!ok && lane == 0) {
-            // drain: wait (bounded) for every copy this CTA issued
-            const int issued = n_tiles;  // upper bound on stage uses issued
+            // drain: wait (bounded) for the copies this CTA issued
             for (int s = 0; s < NS; ++s) {
-                const int uses = issued > s ? (issued - 1 - s) / NS + 1 : 0;
+                const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
                 if (uses > 0) {
                     mbar_drain(&bars[Smem::B_KFULL + s], (uses - 1) & 1);
                     mbar_drain(&bars[Smem::B_VFULL + s], (uses - 1) & 1);
@@ -358,6 +695,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const uint32_t vbase = smem_u32(sm + Smem::STAGES + sj * STAGE_BYTES + KV_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < TN / 16; ++kk) {
+                    // V tile: MN-major, 64-column halves KV_HALF apart, 8-key groups 1 KB apart
                     const uint64_t bdesc = umma_sdesc_sw128(vbase + kk * 16 * 128, KV_HALF, 1024);
                     umma_ts(tmem + TM_O, tmem + TM_S + sbj * TN + kk * 8, bdesc, IDESC_PV,
                             (kk > 0 || !first_of_piece) ? 1u : 0u);
@@ -403,157 +741,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_drain(&bars[Smem::B_DRAIN], 0);
         }
     } else {
-        // ================= softmax / rescale / epilogue (warps 0-3) =================
-        const int r = tid;  // query row == TMEM lane
-        const bool warp_active = warp * 32 < R;
-        const bool row_valid = r < R;
-        const int i_row = row_valid ? r / G : k - 1;
-        const float sl2 = a.scale * kLog2e;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        float m_ref = -INFINITY, l = 0.f;
-        Cursor cur;
-        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
-        bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            const bool first = (it == 0) || (cur.lt == 0);
-            const bool last = (it == n_tiles - 1) || (cur.lt == cur.nb - 1);
-            const int sb = it & 1, s = it % NS;
-            const int ctx = s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
-            const int nvalid = min(TN, L - key0);
-            if (first) {
-                m_ref = -INFINITY;
-                l = 0.f;
-            }
-            ok = warp_wait(&bars[Smem::B_SFULL + sb], (it >> 1) & 1, abort_flag, a.dev_err);
-            if (!ok) break;
-            if (warp_active) {
-                tc_fence_after();
-                uint32_t sr[2][32];
-                tmem_ld32(lane_base + TM_S + sb * TN, sr[0]);
-                tmem_ld32(lane_base + TM_S + sb * TN + 32, sr[1]);
-                tmem_wait_ld();
-                // visible keys of this row in this tile: c < cmax
-                const int cmax = max(0, min(nvalid, ctx + i_row - key0 + 1));
-                float mt = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < TN; ++c) {
-                    const float v = __uint_as_float(sr[c >> 5][c & 31]) * sl2;
-                    if (c < cmax) mt = fmaxf(mt, v);
-                }
-                const float m_new = fmaxf(m_ref, mt);
-                float alpha = 1.f;
-                const bool move = m_new > m_ref + kRescaleThreshold;  // also -inf -> finite
-                if (move) {
-                    alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
-                    m_ref = m_new;
-                    l *= alpha;
-                }
-                uint32_t pk[32];
-                float psum = 0.f;
-#pragma unroll
-                for (int c2 = 0; c2 < TN / 2; ++c2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    const int c = 2 * c2;
-                    if (c < cmax) p0 = exp2f(__uint_as_float(sr[c >> 5][c & 31]) * sl2 - m_ref);
-                    if (c + 1 < cmax)
-                        p1 = exp2f(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]) * sl2 - m_ref);
-                    psum += p0 + p1;
-                    pk[c2] = pack_bf16x2(p0, p1);
-                }
-                l += psum;
-                tmem_st32(lane_base + TM_S + sb * TN, pk);
-                tmem_wait_st();
-                if (!first) {
-                    // PV of the previous tile must be done before O is touched
-                    ok = warp_wait(&bars[Smem::B_ODONE], (it - 1) & 1, abort_flag, a.dev_err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, move && alpha != 1.f)) {
-#pragma unroll
-                        for (int c4 = 0; c4 < D / 32; ++c4) {
-                            uint32_t ov[32];
-                            tmem_ld32(lane_base + TM_O + c4 * 32, ov);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                            tmem_st32(lane_base + TM_O + c4 * 32, ov);
-                        }
-                        tmem_wait_st();
-                    }
-                }
-            }
-            if (nvalid < TN && warp == 0) {
-                // rows past the last key of the sequence: zero V so that
-                // 0 * (stale or canary) never reaches the accumulator
-                ok = warp_wait(&bars[Smem::B_VFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
-                if (!ok) break;
-                uint8_t* vst = sm + Smem::STAGES + s * STAGE_BYTES + KV_BYTES;
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int e = nvalid * 8 + lane; e < TN * 8; e += 32) {
-                    const int row = e / 8, chunk = e % 8;
-                    *reinterpret_cast<uint4*>(vst + row * 128 + chunk * 16) = z;
-                    *reinterpret_cast<uint4*>(vst + KV_HALF + row * 128 + chunk * 16) = z;
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[Smem::B_PFULL + sb]);
-            if (last && warp_active) {
-                ok = warp_wait(&bars[Smem::B_ODONE], it & 1, abort_flag, a.dev_err);
-                if (!ok) break;
-                tc_fence_after();
-                const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
-                const float inv_l = l > 0.f ? 1.f / l : 0.f;
-                const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-                const int g = r % G, h = cur.kvh * G + g;
-                const int64_t orow = ((int64_t)cur.b * k + i_row) * a.Hq + h;
-                const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
-#pragma unroll
-                for (int c4 = 0; c4 < D / 32; ++c4) {
-                    uint32_t ov[32];
-                    tmem_ld32(lane_base + TM_O + c4 * 32, ov);
-                    tmem_wait_ld();
-                    if (!row_valid) continue;
-                    if (complete) {
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            static_cast<__nv_bfloat16*>(a.out) + orow * D + c4 * 32);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l,
-                                              __uint_as_float(ov[8 * v + 1]) * inv_l);
-                            w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l,
-                                              __uint_as_float(ov[8 * v + 3]) * inv_l);
-                            w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l,
-                                              __uint_as_float(ov[8 * v + 5]) * inv_l);
-                            w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l,
-                                              __uint_as_float(ov[8 * v + 7]) * inv_l);
-                            dst[v] = w;
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(
-                            prm.part_o + ((int64_t)slot * ROWS + r) * D + c4 * 32);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(__uint_as_float(ov[4 * v + 0]) * inv_l,
-                                                 __uint_as_float(ov[4 * v + 1]) * inv_l,
-                                                 __uint_as_float(ov[4 * v + 2]) * inv_l,
-                                                 __uint_as_float(ov[4 * v + 3]) * inv_l);
-                    }
-                }
-                if (row_valid) {
-                    if (complete) {
-                        if (a.lse) a.lse[orow] = lse;
-                    } else {
-                        prm.part_lse[(int64_t)slot * ROWS + r] = lse;
-                    }
-                }
-                tc_fence_before();
-            }
-            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
-        }
+        Cta x;
+        x.a = &a;
+        x.prm = &prm;
+        x.sm = sm;
+        x.bars = bars;
+        x.abort_flag = abort_flag;
+        x.s_ctx = s_ctx;
+        x.s_pre = s_pre;
+        x.tmem = tmem;
+        x.t_begin = t_begin;
+        x.t_end = t_end;
+        x.n_tiles = n_tiles;
+        x.R = R;
+        x.G = G;
+        if (REP == 4) softmax_role<4>(x);
+        else if (REP == 2) softmax_role<2>(x);
+        else softmax_role<1>(x);
     }
 
     tc_fence_before();
