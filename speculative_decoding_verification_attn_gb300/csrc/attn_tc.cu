@@ -51,10 +51,12 @@ constexpr int KV_HALF = TN * 128;         // 8 KB
 constexpr int KV_BYTES = 2 * KV_HALF;     // 16 KB per tensor per stage
 constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
-constexpr int MAX_BOX = TN / 8;           // boxes per tile (page_size >= 8)
-constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;       // S0 [0,64) S1 [64,128) O [128,256)
-constexpr uint32_t TM_S = 0, TM_O = 128;
+constexpr int MAX_BOX = TN / 8;           // pages per tile (page_size >= 8)
+constexpr int NUM_PRODUCERS = 64;         // threads of warps 5-6
+constexpr int THREADS = 7 * 32;           // softmax 0-3, MMA 4, producers 5-6
+// TMEM columns: S0 [0,64) S1 [64,128) O [128,256) P0 [256,288) P1 [288,320)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 256;
 constexpr int MAX_BATCH = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -69,7 +71,7 @@ struct Smem {
     static constexpr int STAGES = Q + 2 * Q_BYTES;
     static constexpr int BARS = STAGES + NS * STAGE_BYTES;
     // barriers (uint64 each)
-    static constexpr int B_KFULL = 0, B_VFULL = NS, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
+    static constexpr int B_KVFULL = 0, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
                          B_QEMPTY = 3 * NS + 2, B_SFULL = 3 * NS + 4, B_PFULL = 3 * NS + 6,
                          B_ODONE = 3 * NS + 8, B_DRAIN = 3 * NS + 9, NUM_BARS = 3 * NS + 10;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
@@ -142,6 +144,21 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes.
+__device__ __forceinline__ void cp_async_16_zfill(void* smem_dst, const void* gsrc,
+                                                  uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the whole warp gets its verdict.
@@ -219,6 +236,13 @@ __device__ void softmax_role(const Cta& x) {
     float* s_stat_l = s_stat_m + 4 * ROWS;
     uint64_t* bars = x.bars;
 
+    {
+        // both P buffers start at zero: a lane only ever rewrites its copy's slice
+        const uint32_t zero[32] = {};
+        tmem_st32(lane_base + TM_P, zero);
+        tmem_st32(lane_base + TM_P + TN / 2, zero);
+        tmem_wait_st();
+    }
     float m_ref = -INFINITY, l = 0.f;
     Cursor cur;
     if (x.n_tiles > 0) cur.init(x.t_begin, x.s_pre, x.s_ctx, a.B, a.Hkv, k);
@@ -228,7 +252,7 @@ __device__ void softmax_role(const Cta& x) {
         const bool first = (it == 0) || (cur.lt == 0);
         const bool last = (it == x.n_tiles - 1) || (cur.lt == cur.nb - 1);
         if (first) ++pc;
-        const int sb = it & 1, s = it % NS;
+        const int sb = it & 1;
         const int ctx = x.s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
         const int nvalid = min(TN, L - key0);
         if (first) {
@@ -244,10 +268,14 @@ __device__ void softmax_role(const Cta& x) {
             tmem_wait_ld();
             // keys of this row visible in this copy's slice: cc < cmax
             const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
+            // branch-free: masked scores become -inf (exp2 -> 0)
+            float v[CW];
             float mt = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < CW; ++cc)
-                if (cc < cmax) mt = fmaxf(mt, __uint_as_float(sr[cc]) * sl2);
+            for (int cc = 0; cc < CW; ++cc) {
+                v[cc] = cc < cmax ? __uint_as_float(sr[cc]) * sl2 : -INFINITY;
+                mt = fmaxf(mt, v[cc]);
+            }
             const float m_new = fmaxf(m_ref, mt);
             float alpha = 1.f;
             const bool move = m_new > m_ref + kRescaleThreshold;  // also -inf -> finite
@@ -256,27 +284,20 @@ __device__ void softmax_role(const Cta& x) {
                 m_ref = m_new;
                 l *= alpha;
             }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // keeps -inf - m finite
             uint32_t pk[CW / 2];
-            float psum = 0.f;
+            float psum0 = 0.f, psum1 = 0.f;
 #pragma unroll
             for (int c2 = 0; c2 < CW / 2; ++c2) {
-                const int cc = 2 * c2;
-                const float p0 = cc < cmax ? fast_exp2(__uint_as_float(sr[cc]) * sl2 - m_ref) : 0.f;
-                const float p1 =
-                    cc + 1 < cmax ? fast_exp2(__uint_as_float(sr[cc + 1]) * sl2 - m_ref) : 0.f;
-                psum += p0 + p1;
+                const float p0 = fast_exp2(v[2 * c2] - m_use);
+                const float p1 = fast_exp2(v[2 * c2 + 1] - m_use);
+                psum0 += p0;
+                psum1 += p1;
                 pk[c2] = pack_bf16x2(p0, p1);
             }
-            l += psum;
-            // P of this copy's slice; the other copies' slices of this lane are 0
-            const uint32_t zero[CW / 2] = {};
-#pragma unroll
-            for (int cc = 0; cc < REP; ++cc) {
-                if (cc == c)
-                    store_cols<CW / 2>(lane_base + TM_S + sb * TN + cc * (CW / 2), pk);
-                else
-                    store_cols<CW / 2>(lane_base + TM_S + sb * TN + cc * (CW / 2), zero);
-            }
+            l += psum0 + psum1;
+            // this copy's slice of P; the other slices of this lane stay zero
+            store_cols<CW / 2>(lane_base + TM_P + sb * (TN / 2) + c * (CW / 2), pk);
             tmem_wait_st();
             if (!first && __any_sync(0xffffffffu, move)) {
                 // O must hold every earlier P V before it is rescaled
@@ -295,21 +316,6 @@ __device__ void softmax_role(const Cta& x) {
                     }
                     tmem_wait_st();
                 }
-            }
-        }
-        if (ok && nvalid < TN && warp == 0) {
-            // rows past the last key of the sequence: zero V so that
-            // 0 * (stale or canary) never reaches the accumulator
-            ok = warp_wait(&bars[Smem::B_VFULL + s], (it / NS) & 1, x.abort_flag, a.dev_err);
-            if (ok) {
-                uint8_t* vst = x.sm + Smem::STAGES + s * STAGE_BYTES + KV_BYTES;
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int e = nvalid * 8 + lane; e < TN * 8; e += 32) {
-                    const int row = e / 8, chunk = e % 8;
-                    *reinterpret_cast<uint4*>(vst + row * 128 + chunk * 16) = z;
-                    *reinterpret_cast<uint4*>(vst + KV_HALF + row * 128 + chunk * 16) = z;
-                }
-                fence_proxy_async_smem();
             }
         }
         tc_fence_before();
@@ -495,8 +501,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // ---- setup: barriers, TMEM, zero Q pad rows, per-sequence tile prefix
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars[Smem::B_KFULL + s], 1);
-            mbar_init(&bars[Smem::B_VFULL + s], 1);
+            mbar_init(&bars[Smem::B_KVFULL + s], NUM_PRODUCERS);  // cp.async noinc arrivals
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
         for (int q = 0; q < 2; ++q) {
@@ -510,7 +515,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 4) {
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
@@ -560,28 +565,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp == 4) {
-        // ================= TMA producer =================
+    if (warp >= 5) {
+        // ================= producers (warps 5-6) =================
+        // K/V: cp.async 16-byte copies, one key row = 16 chunks of 256 B, written
+        // into the 128-byte-swizzled K-major (K) / MN-major (V) layouts the MMAs
+        // read; keys past the sequence end are zero-filled.  Completion reaches
+        // kv_full through cp.async.mbarrier.arrive.noinc, so no producer thread
+        // ever waits for data.  Q (twice per piece at most) comes by TMA.
+        const int pt = tid - 5 * 32;          // 0..63
+        const int chunk = pt & 15;            // 16-byte column of a key row
+        const int half = chunk >> 3, cw = chunk & 7;
+        const int row0 = pt >> 4;             // key rows row0, row0+4, ...
         Cursor cur, ahead;
         if (n_tiles > 0) {
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             ahead = cur;
         }
         const uint64_t pol = l2_policy_evict_first();
-        if (lane == 0) {
-            prefetch_tmap(&qmap);
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
-        }
+        if (pt == 0) prefetch_tmap(&qmap);
         // block-table entries of a tile -> ring slot (cp.async, LOOKAHEAD tiles ahead)
         auto fetch_pids = [&](int slot, const Cursor& c) {
             const int key0 = c.lt * TN;
             const int L = s_ctx[c.b] + k;
             const int nvalid = min(TN, L - key0);
             const int nbox = (nvalid + BH - 1) / BH;
-            if (lane < nbox) {
-                const int lp = (key0 + lane * BH) / P;
-                cp_async_4(&pid_ring[slot * MAX_BOX + lane],
+            if (pt < nbox) {
+                const int lp = (key0 + pt * BH) / P;
+                cp_async_4(&pid_ring[slot * MAX_BOX + pt],
                            &a.block_table[(int64_t)c.b * a.max_pages + lp]);
             }
         };
@@ -592,23 +602,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             cp_async_commit();
         }
-        int pc = -1;      // piece counter
-        int n_issued = 0; // tiles whose K/V loads were issued
+        const char* kbase = static_cast<const char*>(a.k_cache);
+        const char* vbase = static_cast<const char*>(a.v_cache);
+        int pc = -1;
         int issued_q[2] = {0, 0};
         bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            if (it + LOOKAHEAD < n_tiles) {
-                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
-                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
-            }
-            cp_async_commit();
-            cp_async_wait<LOOKAHEAD>();
-            __syncwarp();
+        for (int it = 0; it < n_tiles; ++it) {
+            // the block-table entries of tile `it` (committed LOOKAHEAD groups ago)
+            cp_async_wait<LOOKAHEAD - 1>();
+            named_bar_sync(2, NUM_PRODUCERS);
             const bool first = (it == 0) || (cur.lt == 0);
             if (first) {
                 ++pc;
                 const int qb = pc & 1, use = pc >> 1;
-                if (lane == 0) {
+                if (pt == 0 && ok) {
                     if (use >= 1)
                         ok = mbar_wait(&bars[Smem::B_QEMPTY + qb], (use - 1) & 1, abort_flag,
                                        a.dev_err);
@@ -622,61 +629,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         issued_q[qb] = use + 1;
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
             }
             const int s = it % NS, use = it / NS;
-            if (lane == 0) {
-                if (use >= 1)
-                    ok = mbar_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag,
-                                   a.dev_err);
-                if (ok) {
-                    const int key0 = cur.lt * TN;
-                    const int L = s_ctx[cur.b] + k;
-                    const int nvalid = min(TN, L - key0);
-                    const int nbox = (nvalid + BH - 1) / BH;
-                    const uint32_t bytes = (uint32_t)nbox * BH * 128 * 2;
-                    mbar_arrive_expect_tx(&bars[Smem::B_KFULL + s], bytes);
-                    mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], bytes);
-                    uint8_t* kst = sm + Smem::STAGES + s * STAGE_BYTES;
-                    uint8_t* vst = kst + KV_BYTES;
-                    const int slot = it % (LOOKAHEAD + 1);
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        int page = pid_ring[slot * MAX_BOX + bx];
-                        if (page < 0 || page >= a.num_pages) {
-                            raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
-                            page = 0;
-                        }
-                        const int key = key0 + bx * BH;
-                        const int row = (page * Hkv + cur.kvh) * P + (key % P);
-                        for (int h = 0; h < 2; ++h) {
-                            tma_load_2d(kst + h * KV_HALF + bx * BH * 128, &kmap,
-                                        &bars[Smem::B_KFULL + s], h * 64, row, pol);
-                            tma_load_2d(vst + h * KV_HALF + bx * BH * 128, &vmap,
-                                        &bars[Smem::B_VFULL + s], h * 64, row, pol);
-                        }
+            if (ok && use >= 1)
+                ok = warp_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag, a.dev_err);
+            if (ok) {
+                const int key0 = cur.lt * TN;
+                const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
+                const int slot = it % (LOOKAHEAD + 1);
+                uint8_t* kst = sm + Smem::STAGES + s * STAGE_BYTES;
+                const uint32_t doff = half * KV_HALF;
+#pragma unroll 4
+                for (int u = 0; u < TN / 4; ++u) {
+                    const int kr = row0 + 4 * u;  // key row inside the tile
+                    const bool valid = kr < nvalid;
+                    int page = pid_ring[slot * MAX_BOX + (valid ? kr / BH : 0)];
+                    if (page < 0 || page >= a.num_pages) {
+                        if (valid) raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                        page = 0;
                     }
-                    n_issued = it + 1;
+                    const int64_t grow = ((int64_t)page * Hkv + cur.kvh) * P + (key0 + kr) % P;
+                    const int64_t goff = grow * (D * 2) + chunk * 16;
+                    const uint32_t soff = doff + kr * 128 + ((cw ^ (kr & 7)) * 16);
+                    const uint32_t nbytes = valid ? 16u : 0u;
+                    cp_async_16_zfill(kst + soff, kbase + (valid ? goff : 0), nbytes, pol);
+                    cp_async_16_zfill(kst + KV_BYTES + soff, vbase + (valid ? goff : 0), nbytes, pol);
                 }
+                cp_async_mbar_arrive_noinc(&bars[Smem::B_KVFULL + s]);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();
+            // prefetch the block-table entries LOOKAHEAD tiles ahead
+            if (it + LOOKAHEAD < n_tiles) {
+                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
+                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
+        // every copy this thread issued has landed before the CTA can exit
         cp_async_wait<0>();
-        if (!ok && lane == 0) {
-            // drain: wait (bounded) for the copies this CTA issued
-            for (int s = 0; s < NS; ++s) {
-                const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
-                if (uses > 0) {
-                    mbar_drain(&bars[Smem::B_KFULL + s], (uses - 1) & 1);
-                    mbar_drain(&bars[Smem::B_VFULL + s], (uses - 1) & 1);
-                }
-            }
+        if (pt == 0 && *abort_flag)
             for (int q = 0; q < 2; ++q)
                 if (issued_q[q] > 0) mbar_drain(&bars[Smem::B_QFULL + q], (issued_q[q] - 1) & 1);
-        }
-    } else if (warp == 5) {
+    } else if (warp == 4) {
         // ================= MMA issuer =================
         if (lane == 0 && n_tiles > 0) {
             Cursor cur;
@@ -688,8 +682,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             auto issue_pv = [&](int j, bool first_of_piece) -> bool {
                 const int sbj = j & 1, sj = j % NS;
                 if (!mbar_wait(&bars[Smem::B_PFULL + sbj], (j >> 1) & 1, abort_flag, a.dev_err))
-                    return false;
-                if (!mbar_wait(&bars[Smem::B_VFULL + sj], (j / NS) & 1, abort_flag, a.dev_err))
                     return false;
                 tc_fence_after();
                 const uint32_t vbase = smem_u32(sm + Smem::STAGES + sj * STAGE_BYTES + KV_BYTES);
@@ -713,8 +705,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     ok = mbar_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag, a.dev_err);
                 const int s = it % NS;
                 if (ok)
-                    ok = mbar_wait(&bars[Smem::B_KFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
+                    ok = mbar_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
                 if (!ok) break;
+                // K/V arrived through the generic proxy (cp.async); the tensor
+                // core reads through the async proxy
+                fence_proxy_async_smem();
                 tc_fence_after();
                 const int sb = it & 1;
                 const uint32_t qbase = smem_u32(sm + Smem::Q + qb * Q_BYTES);
@@ -763,7 +758,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 4) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // Merge the partials of every segment cut by a CTA-range boundary.
