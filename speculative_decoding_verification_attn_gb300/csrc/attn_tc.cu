@@ -689,7 +689,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 for (int kk = 0; kk < TN / 16; ++kk) {
                     // V tile: MN-major, 64-column halves KV_HALF apart, 8-key groups 1 KB apart
                     const uint64_t bdesc = umma_sdesc_sw128(vbase + kk * 16 * 128, KV_HALF, 1024);
-                    umma_ts(tmem + TM_O, tmem + TM_S + sbj * TN + kk * 8, bdesc, IDESC_PV,
+                    umma_ts(tmem + TM_O, tmem + TM_P + sbj * (TN / 2) + kk * 8, bdesc, IDESC_PV,
                             (kk > 0 || !first_of_piece) ? 1u : 0u);
                 }
                 umma_commit(&bars[Smem::B_KVEMPTY + sj]);
