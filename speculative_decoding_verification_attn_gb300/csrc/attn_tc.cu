@@ -47,13 +47,11 @@ constexpr int NS = 4;            // K/V pipeline stages
 constexpr int ROWS = 128;        // MMA M: query rows (padded / replicated)
 constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
-constexpr int KV_HALF = TN * 128;         // 8 KB
-constexpr int KV_BYTES = 2 * KV_HALF;     // 16 KB per tensor per stage
+constexpr int KV_BYTES = TN * D * 2;      // 16 KB per tensor per stage
 constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int MAX_BOX = TN / 8;           // pages per tile (page_size >= 8)
-constexpr int NUM_PRODUCERS = 64;         // threads of warps 5-6
-constexpr int THREADS = 7 * 32;           // softmax 0-3, MMA 4, producers 5-6
+constexpr int THREADS = 6 * 32;           // softmax 0-3, MMA 4, producer 5
 // TMEM columns: S0 [0,64) S1 [64,128) O [128,256) P0 [256,288) P1 [288,320)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 256;
@@ -62,7 +60,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr uint32_t IDESC_QK = umma_idesc_bf16(ROWS, TN, 0, 0);  // A,B K-major
 constexpr uint32_t IDESC_PV = umma_idesc_bf16(ROWS, D, 0, 1);   // B (V) MN-major
 
 struct Smem {
@@ -146,21 +143,6 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes.
-__device__ __forceinline__ void cp_async_16_zfill(void* smem_dst, const void* gsrc,
-                                                  uint32_t src_bytes, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
-                     smem_u32(smem_dst)),
-                 "l"(gsrc), "r"(src_bytes), "l"(policy)
-                 : "memory");
-}
-// Arrive on `bar` once this thread's earlier cp.async copies have landed
-// (counts as one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
 // Warp-uniform bounded wait: lane 0 polls, the whole warp gets its verdict.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* dev_err) {
@@ -187,7 +169,7 @@ struct Cta {
     const int* s_pre;
     uint32_t tmem;
     int64_t t_begin, t_end;
-    int n_tiles, R, G;
+    int n_tiles, R, G, BH;
 };
 
 // Load CW consecutive fp32 TMEM columns of this thread's lane.
@@ -223,7 +205,7 @@ __device__ void softmax_role(const Cta& x) {
     constexpr int CW = TN / REP;  // key columns of a tile owned by one copy
     const AttnArgs& a = *x.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int R = x.R, G = x.G, k = a.k;
+    const int R = x.R, G = x.G, k = a.k, BH = x.BH;
     const int c = (warp * 32) / RQ;                 // copy of this thread
     const int r = warp * 32 + lane - c * RQ;        // query row inside the copy
     const bool warp_active = c < REP && warp * 32 - c * RQ < R;
@@ -316,6 +298,22 @@ __device__ void softmax_role(const Cta& x) {
                     }
                     tmem_wait_st();
                 }
+            }
+        }
+        if (ok && nvalid % BH != 0 && warp == 0) {
+            // keys past the sequence end inside its last page: zero their V
+            // rows so that 0 * (stale or canary) never reaches O
+            ok = warp_wait(&bars[Smem::B_KVFULL + it % NS], (it / NS) & 1, x.abort_flag,
+                           a.dev_err);
+            if (ok) {
+                uint8_t* vst = x.sm + Smem::STAGES + (it % NS) * STAGE_BYTES + KV_BYTES;
+                const int bx = nvalid / BH, r_end = BH;
+                for (int e = (nvalid % BH) * 16 + lane; e < r_end * 16; e += 32) {
+                    const int rr = e / 16, h = (e / 8) & 1, ch = e % 8;
+                    *reinterpret_cast<uint4*>(vst + bx * BH * 256 + h * BH * 128 + rr * 128 +
+                                              ch * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
             }
         }
         tc_fence_before();
@@ -501,7 +499,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // ---- setup: barriers, TMEM, zero Q pad rows, per-sequence tile prefix
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars[Smem::B_KVFULL + s], NUM_PRODUCERS);  // cp.async noinc arrivals
+            mbar_init(&bars[Smem::B_KVFULL + s], 1);
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
         for (int q = 0; q < 2; ++q) {
@@ -565,33 +563,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp >= 5) {
-        // ================= producers (warps 5-6) =================
-        // K/V: cp.async 16-byte copies, one key row = 16 chunks of 256 B, written
-        // into the 128-byte-swizzled K-major (K) / MN-major (V) layouts the MMAs
-        // read; keys past the sequence end are zero-filled.  Completion reaches
-        // kv_full through cp.async.mbarrier.arrive.noinc, so no producer thread
-        // ever waits for data.  Q (twice per piece at most) comes by TMA.
-        const int pt = tid - 5 * 32;          // 0..63
-        const int chunk = pt & 15;            // 16-byte column of a key row
-        const int half = chunk >> 3, cw = chunk & 7;
-        const int row0 = pt >> 4;             // key rows row0, row0+4, ...
+    if (warp == 5) {
+        // ================= TMA producer (warp 5) =================
+        // One 3-D box per (page, tensor): both 64-column halves of BH keys of
+        // one kv-head, 256*BH bytes, landing as [half][key][128 B] with the
+        // 128-byte swizzle the MMAs read.  Boxes of a tile are issued by
+        // parallel lanes; block-table entries are prefetched LOOKAHEAD tiles
+        // ahead with cp.async.
         Cursor cur, ahead;
         if (n_tiles > 0) {
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             ahead = cur;
         }
         const uint64_t pol = l2_policy_evict_first();
-        if (pt == 0) prefetch_tmap(&qmap);
-        // block-table entries of a tile -> ring slot (cp.async, LOOKAHEAD tiles ahead)
+        if (lane == 0) {
+            prefetch_tmap(&qmap);
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
         auto fetch_pids = [&](int slot, const Cursor& c) {
             const int key0 = c.lt * TN;
-            const int L = s_ctx[c.b] + k;
-            const int nvalid = min(TN, L - key0);
+            const int nvalid = min(TN, s_ctx[c.b] + k - key0);
             const int nbox = (nvalid + BH - 1) / BH;
-            if (pt < nbox) {
-                const int lp = (key0 + pt * BH) / P;
-                cp_async_4(&pid_ring[slot * MAX_BOX + pt],
+            if (lane < nbox) {
+                const int lp = (key0 + lane * BH) / P;
+                cp_async_4(&pid_ring[slot * MAX_BOX + lane],
                            &a.block_table[(int64_t)c.b * a.max_pages + lp]);
             }
         };
@@ -602,20 +598,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             cp_async_commit();
         }
-        const char* kbase = static_cast<const char*>(a.k_cache);
-        const char* vbase = static_cast<const char*>(a.v_cache);
         int pc = -1;
+        int n_issued = 0;
         int issued_q[2] = {0, 0};
         bool ok = true;
-        for (int it = 0; it < n_tiles; ++it) {
-            // the block-table entries of tile `it` (committed LOOKAHEAD groups ago)
-            cp_async_wait<LOOKAHEAD - 1>();
-            named_bar_sync(2, NUM_PRODUCERS);
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            if (it + LOOKAHEAD < n_tiles) {
+                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
+                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+            cp_async_wait<LOOKAHEAD>();  // entries of tile `it`
+            __syncwarp();
             const bool first = (it == 0) || (cur.lt == 0);
             if (first) {
                 ++pc;
                 const int qb = pc & 1, use = pc >> 1;
-                if (pt == 0 && ok) {
+                if (lane == 0) {
                     if (use >= 1)
                         ok = mbar_wait(&bars[Smem::B_QEMPTY + qb], (use - 1) & 1, abort_flag,
                                        a.dev_err);
@@ -629,47 +628,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         issued_q[qb] = use + 1;
                     }
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
             }
             const int s = it % NS, use = it / NS;
-            if (ok && use >= 1)
-                ok = warp_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag, a.dev_err);
-            if (ok) {
-                const int key0 = cur.lt * TN;
-                const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
-                const int slot = it % (LOOKAHEAD + 1);
-                uint8_t* kst = sm + Smem::STAGES + s * STAGE_BYTES;
-                const uint32_t doff = half * KV_HALF;
-#pragma unroll 4
-                for (int u = 0; u < TN / 4; ++u) {
-                    const int kr = row0 + 4 * u;  // key row inside the tile
-                    const bool valid = kr < nvalid;
-                    int page = pid_ring[slot * MAX_BOX + (valid ? kr / BH : 0)];
-                    if (page < 0 || page >= a.num_pages) {
-                        if (valid) raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
-                        page = 0;
-                    }
-                    const int64_t grow = ((int64_t)page * Hkv + cur.kvh) * P + (key0 + kr) % P;
-                    const int64_t goff = grow * (D * 2) + chunk * 16;
-                    const uint32_t soff = doff + kr * 128 + ((cw ^ (kr & 7)) * 16);
-                    const uint32_t nbytes = valid ? 16u : 0u;
-                    cp_async_16_zfill(kst + soff, kbase + (valid ? goff : 0), nbytes, pol);
-                    cp_async_16_zfill(kst + KV_BYTES + soff, vbase + (valid ? goff : 0), nbytes, pol);
+            const int key0 = cur.lt * TN;
+            const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
+            const int nbox = (nvalid + BH - 1) / BH;
+            if (lane == 0) {
+                if (use >= 1)
+                    ok = mbar_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag,
+                                   a.dev_err);
+                if (ok) mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s], 2u * nbox * BH * 256);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane < 2 * nbox) {
+                const int tensor = lane & 1, bx = lane >> 1;
+                int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
+                if (page < 0 || page >= a.num_pages) {
+                    raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                    page = 0;
                 }
-                cp_async_mbar_arrive_noinc(&bars[Smem::B_KVFULL + s]);
+                const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BH) % P;
+                tma_load_3d_hint(sm + Smem::STAGES + s * STAGE_BYTES + tensor * KV_BYTES +
+                                     bx * BH * 256,
+                                 tensor ? (const void*)&vmap : (const void*)&kmap,
+                                 &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
             }
-            // prefetch the block-table entries LOOKAHEAD tiles ahead
-            if (it + LOOKAHEAD < n_tiles) {
-                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
-                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
-            }
-            cp_async_commit();
+            n_issued = it + 1;
+            __syncwarp();
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
-        // every copy this thread issued has landed before the CTA can exit
         cp_async_wait<0>();
-        if (pt == 0 && *abort_flag)
+        if (!ok && lane == 0) {
+            // drain: wait (bounded) for the copies this CTA issued
+            for (int s = 0; s < NS; ++s) {
+                const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
+                if (uses > 0) mbar_drain(&bars[Smem::B_KVFULL + s], (uses - 1) & 1);
+            }
             for (int q = 0; q < 2; ++q)
                 if (issued_q[q] > 0) mbar_drain(&bars[Smem::B_QFULL + q], (issued_q[q] - 1) & 1);
+        }
     } else if (warp == 4) {
         // ================= MMA issuer =================
         if (lane == 0 && n_tiles > 0) {
@@ -677,18 +677,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             int pc = -1;
             bool ok = true;
-            int pend_it = -1;
+            int pend_it = -1, pend_nbox = 0;
             bool pend_first = false;
-            auto issue_pv = [&](int j, bool first_of_piece) -> bool {
+            const uint32_t idesc_qk = umma_idesc_bf16(ROWS, BH, 0, 0);  // per-box N = BH keys
+            // O += P V over the first nbox*BH keys of tile j (the rest are past
+            // the sequence end and hold no probability mass)
+            auto issue_pv = [&](int j, bool first_of_piece, int nbox) -> bool {
                 const int sbj = j & 1, sj = j % NS;
                 if (!mbar_wait(&bars[Smem::B_PFULL + sbj], (j >> 1) & 1, abort_flag, a.dev_err))
                     return false;
                 tc_fence_after();
                 const uint32_t vbase = smem_u32(sm + Smem::STAGES + sj * STAGE_BYTES + KV_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < TN / 16; ++kk) {
-                    // V tile: MN-major, 64-column halves KV_HALF apart, 8-key groups 1 KB apart
-                    const uint64_t bdesc = umma_sdesc_sw128(vbase + kk * 16 * 128, KV_HALF, 1024);
+                const int nk = nbox * BH / 16;
+                for (int kk = 0; kk < nk; ++kk) {
+                    // V: MN-major; inside box bx the two 64-column halves are
+                    // BH*128 B apart (LBO) and 8-key groups 1 KB apart (SBO)
+                    const int key = kk * 16, bx = key / BH, r0 = key % BH;
+                    const uint64_t bdesc =
+                        umma_sdesc_sw128(vbase + bx * BH * 256 + r0 * 128, BH * 128, 1024);
                     umma_ts(tmem + TM_O, tmem + TM_P + sbj * (TN / 2) + kk * 8, bdesc, IDESC_PV,
                             (kk > 0 || !first_of_piece) ? 1u : 0u);
                 }
@@ -707,30 +713,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (ok)
                     ok = mbar_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
                 if (!ok) break;
-                // K/V arrived through the generic proxy (cp.async); the tensor
-                // core reads through the async proxy
-                fence_proxy_async_smem();
                 tc_fence_after();
+                const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
+                const int nbox = (nvalid + BH - 1) / BH;
                 const int sb = it & 1;
                 const uint32_t qbase = smem_u32(sm + Smem::Q + qb * Q_BYTES);
                 const uint32_t kbase = smem_u32(sm + Smem::STAGES + s * STAGE_BYTES);
+                // S[:, box] = Q K_box^T, one N = BH MMA chain per page box
+                for (int bx = 0; bx < nbox; ++bx) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t col = (kk & 3) * 32;  // 16 bf16 = 32 B inside the swizzle row
-                    const uint64_t adesc =
-                        umma_sdesc_sw128(qbase + (kk >> 2) * Q_HALF + col, 16, 1024);
-                    const uint64_t bdesc =
-                        umma_sdesc_sw128(kbase + (kk >> 2) * KV_HALF + col, 16, 1024);
-                    umma_ss(tmem + TM_S + sb * TN, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t col = (kk & 3) * 32;  // 16 bf16 = 32 B inside a swizzle row
+                        const uint64_t adesc =
+                            umma_sdesc_sw128(qbase + (kk >> 2) * Q_HALF + col, 16, 1024);
+                        const uint64_t bdesc = umma_sdesc_sw128(
+                            kbase + bx * BH * 256 + (kk >> 2) * BH * 128 + col, 16, 1024);
+                        umma_ss(tmem + TM_S + sb * TN + bx * BH, adesc, bdesc, idesc_qk,
+                                kk > 0 ? 1u : 0u);
+                    }
                 }
                 umma_commit(&bars[Smem::B_SFULL + sb]);
                 if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
-                if (pend_it >= 0) ok = issue_pv(pend_it, pend_first);
+                if (pend_it >= 0) ok = issue_pv(pend_it, pend_first, pend_nbox);
                 pend_it = it;
                 pend_first = first;
+                pend_nbox = nbox;
                 if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
             }
-            if (ok && pend_it >= 0) ok = issue_pv(pend_it, pend_first);
+            if (ok && pend_it >= 0) ok = issue_pv(pend_it, pend_first, pend_nbox);
             // make sure every tensor-core op finished before TMEM is released
             umma_commit(&bars[Smem::B_DRAIN]);
             mbar_drain(&bars[Smem::B_DRAIN], 0);
@@ -750,6 +760,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         x.n_tiles = n_tiles;
         x.R = R;
         x.G = G;
+        x.BH = BH;
         if (REP == 4) softmax_role<4>(x);
         else if (REP == 2) softmax_role<2>(x);
         else softmax_role<1>(x);
@@ -869,7 +880,7 @@ bool tc_supported(const AttnArgs& a) {
     const int G = a.Hq / a.Hkv;
     const bool pow2 = (a.P & (a.P - 1)) == 0;
     return a.q_dtype == SPEC_DTYPE_BF16 && a.kv_dtype == SPEC_DTYPE_BF16 && a.D == D &&
-           a.k * G <= ROWS && G <= 256 && pow2 && a.P >= 8 && a.P <= 256 && a.B <= MAX_BATCH &&
+           a.k * G <= ROWS && G <= 256 && pow2 && a.P >= 16 && a.P <= 256 && a.B <= MAX_BATCH &&
            (int64_t)a.num_pages * a.Hkv * a.P < (1LL << 31) && (int64_t)a.B * a.k < (1LL << 31);
 }
 
@@ -894,14 +905,16 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // K/V: [rows = num_pages*Hkv*P] x [2 halves] x [64 columns]; one box =
+    // BH consecutive rows of one page, both halves
     const int BH = a.P < TN ? a.P : TN;
     const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
     for (int t = 0; t < 2; ++t) {
-        cuuint64_t dims[2] = {(cuuint64_t)D, rows};
-        cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)BH};
-        cuuint32_t es[2] = {1, 1};
-        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+        cuuint64_t dims[3] = {64, rows, 2};
+        cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)BH, 2};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
