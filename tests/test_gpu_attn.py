@@ -44,7 +44,7 @@ SMALL_BF16 = [
     dict(num_q_heads=16, num_kv_heads=2, num_draft=8),                    # 64 rows
     dict(num_q_heads=4, num_kv_heads=2, num_draft=64),                    # 128 rows
     dict(ctx=[0, 1, 63, 64, 65], batch=5, num_draft=3),                   # tile edges
-    dict(page_size=8, ctx=(1, 200)),
+    dict(page_size=32, ctx=(1, 200), num_draft=2),
     dict(page_size=64, ctx=(1, 400)),
     dict(page_size=128, ctx=(100, 600)),
     dict(page_size=256, ctx=(250, 700), batch=2),
@@ -89,6 +89,16 @@ def test_simt_small(oracle_mod, kw, chunk):
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_tiny_fp32_workload(oracle_mod, seed):
     check_attn_full(oracle_mod, make_inputs("tiny_fp32", seed=seed), "tiny_fp32")
+
+
+def test_page_size_8_runs_on_simt(oracle_mod):
+    # the tensor-core kernel loads one TMA box per page and needs >= 16 keys
+    # per box; smaller pages go to the SIMT kernel under the automatic path
+    inp = make_inputs(small_spec(page_size=8, ctx=(1, 200)), seed=29)
+    check_attn_full(oracle_mod, inp, "page_size=8")
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    with pytest.raises(binding.SpecError, match="not supported"):
+        gpu_attn(inp)
 
 
 def test_tensor_core_matches_simt():
