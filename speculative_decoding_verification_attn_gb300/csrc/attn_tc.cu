@@ -50,11 +50,13 @@ constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
 constexpr int KV_BYTES = TN * D * 2;      // 16 KB per tensor per stage
 constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
-constexpr int MAX_BOX = TN / 8;           // pages per tile (page_size >= 8)
+constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
+constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
 constexpr int THREADS = 6 * 32;           // softmax 0-3, MMA 4, producer 5
 // TMEM columns: S0 [0,64) S1 [64,128) O [128,256) P0 [256,288) P1 [288,320)
+// Q0 [320,384) Q1 [384,448) (bf16 pairs)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 256;
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 256, TM_Q = 320;
 constexpr int MAX_BATCH = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -494,7 +496,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, k = a.k, Hkv = a.Hkv, G = a.Hq / a.Hkv, R = k * G, P = a.P;
     const int RQ = rows_per_copy(R), REP = num_copies(R);
-    const int BH = P < TN ? P : TN;  // box height (keys per TMA box)
+    const int BH = BOX_ROWS;  // keys per TMA box (a 16-row slice of one page)
 
     // ---- setup: barriers, TMEM, zero Q pad rows, per-sequence tile prefix
     if (tid == 0) {
@@ -671,35 +673,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (issued_q[q] > 0) mbar_drain(&bars[Smem::B_QFULL + q], (issued_q[q] - 1) & 1);
         }
     } else if (warp == 4) {
-        // ================= MMA issuer =================
-        if (lane == 0 && n_tiles > 0) {
+        // ================= MMA issuer (lane 0) + K relayout (whole warp) =================
+        // A K box lands as [h0 rows 0-7 | h0 rows 8-15 | h1 rows 0-7 | h1 rows 8-15]
+        // (1 KB blocks, 128-byte swizzle).  Swapping the middle blocks gives
+        // [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15]: every 8-key group of the tile
+        // is then 2 KB after the previous one, one uniform stride for an
+        // N = 64 QK MMA.  The swizzle phase of a row is its index mod 8, which
+        // the move keeps.  V keeps the box layout; P V runs one K = 16 MMA per box.
+        if (n_tiles > 0) {
             Cursor cur;
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             int pc = -1;
             bool ok = true;
             int pend_it = -1, pend_nbox = 0;
             bool pend_first = false;
-            const uint32_t idesc_qk = umma_idesc_bf16(ROWS, BH, 0, 0);  // per-box N = BH keys
-            // O += P V over the first nbox*BH keys of tile j (the rest are past
+            const uint32_t idesc_qk = umma_idesc_bf16(ROWS, TN, 0, 0);
+            // smem descriptors are built once; an operand's start address
+            // lives in the low 14 bits (in 16-byte units), so stepping to
+            // another k-slice, box or stage is one 64-bit add
+            const uint64_t qdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::Q), 16, 1024);
+            const uint64_t kdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::STAGES), 16, 2048);
+            const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::STAGES + KV_BYTES),
+                                                     BOX_ROWS * 128, 1024);
+            // O += P V over the first nbox boxes of tile j (the rest are past
             // the sequence end and hold no probability mass)
             auto issue_pv = [&](int j, bool first_of_piece, int nbox) -> bool {
                 const int sbj = j & 1, sj = j % NS;
-                if (!mbar_wait(&bars[Smem::B_PFULL + sbj], (j >> 1) & 1, abort_flag, a.dev_err))
+                if (!warp_wait(&bars[Smem::B_PFULL + sbj], (j >> 1) & 1, abort_flag, a.dev_err))
                     return false;
                 tc_fence_after();
-                const uint32_t vbase = smem_u32(sm + Smem::STAGES + sj * STAGE_BYTES + KV_BYTES);
-                const int nk = nbox * BH / 16;
-                for (int kk = 0; kk < nk; ++kk) {
-                    // V: MN-major; inside box bx the two 64-column halves are
-                    // BH*128 B apart (LBO) and 8-key groups 1 KB apart (SBO)
-                    const int key = kk * 16, bx = key / BH, r0 = key % BH;
-                    const uint64_t bdesc =
-                        umma_sdesc_sw128(vbase + bx * BH * 256 + r0 * 128, BH * 128, 1024);
-                    umma_ts(tmem + TM_O, tmem + TM_P + sbj * (TN / 2) + kk * 8, bdesc, IDESC_PV,
-                            (kk > 0 || !first_of_piece) ? 1u : 0u);
+                if (lane == 0) {
+                    // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
+                    const uint64_t vd = vdesc0 + ((uint32_t)(sj * STAGE_BYTES) >> 4);
+                    const uint32_t pcol = tmem + TM_P + sbj * (TN / 2);
+#pragma unroll
+                    for (int bx = 0; bx < MAX_BOX; ++bx)
+                        if (bx < nbox)
+                            umma_ts(tmem + TM_O, pcol + bx * (BOX_ROWS / 2),
+                                    vd + ((bx * BOX_ROWS * 256) >> 4), IDESC_PV,
+                                    (bx > 0 || !first_of_piece) ? 1u : 0u);
+                    umma_commit(&bars[Smem::B_KVEMPTY + sj]);
+                    umma_commit(&bars[Smem::B_ODONE]);
                 }
-                umma_commit(&bars[Smem::B_KVEMPTY + sj]);
-                umma_commit(&bars[Smem::B_ODONE]);
+                __syncwarp();
                 return true;
             };
             for (int it = 0; it < n_tiles && ok; ++it) {
@@ -708,32 +724,53 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (first) ++pc;
                 const int qb = pc & 1;
                 if (first)
-                    ok = mbar_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag, a.dev_err);
+                    ok = warp_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag, a.dev_err);
                 const int s = it % NS;
                 if (ok)
-                    ok = mbar_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
+                    ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
                 if (!ok) break;
-                tc_fence_after();
                 const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
-                const int nbox = (nvalid + BH - 1) / BH;
-                const int sb = it & 1;
-                const uint32_t qbase = smem_u32(sm + Smem::Q + qb * Q_BYTES);
-                const uint32_t kbase = smem_u32(sm + Smem::STAGES + s * STAGE_BYTES);
-                // S[:, box] = Q K_box^T, one N = BH MMA chain per page box
-                for (int bx = 0; bx < nbox; ++bx) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t col = (kk & 3) * 32;  // 16 bf16 = 32 B inside a swizzle row
-                        const uint64_t adesc =
-                            umma_sdesc_sw128(qbase + (kk >> 2) * Q_HALF + col, 16, 1024);
-                        const uint64_t bdesc = umma_sdesc_sw128(
-                            kbase + bx * BH * 256 + (kk >> 2) * BH * 128 + col, 16, 1024);
-                        umma_ss(tmem + TM_S + sb * TN + bx * BH, adesc, bdesc, idesc_qk,
-                                kk > 0 ? 1u : 0u);
+                const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
+                {
+                    // K relayout: swap 1 KB blocks 1 and 2 of every loaded box
+                    uint4* kst = reinterpret_cast<uint4*>(sm + Smem::STAGES + s * STAGE_BYTES);
+                    for (int bx = 0; bx < nbox; ++bx) {
+                        uint4* b1 = kst + bx * (BOX_ROWS * 256 / 16) + 1024 / 16;
+                        uint4* b2 = b1 + 1024 / 16;
+                        const uint4 x0 = b1[lane], x1 = b1[lane + 32];
+                        const uint4 y0 = b2[lane], y1 = b2[lane + 32];
+                        b1[lane] = y0;
+                        b1[lane + 32] = y1;
+                        b2[lane] = x0;
+                        b2[lane + 32] = x1;
                     }
+                    fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
                 }
-                umma_commit(&bars[Smem::B_SFULL + sb]);
-                if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
+                __syncwarp();
+                tc_fence_after();
+                const int sb = it & 1;
+                if (lane == 0) {
+                    const uint32_t qt = tmem + TM_Q + qb * (D / 2);
+                    if (first) {
+                        // Q of this piece: smem (TMA, 128-byte swizzle) -> TMEM once;
+                        // k-slice kk = 64-column half kk/4, 32-byte step kk%4
+                        const uint64_t qd = qdesc0 + ((uint32_t)(qb * Q_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            tmem_cp_128x256b(qt + kk * 8,
+                                             qd + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                    }
+                    // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
+                    const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_ts(tmem + TM_S + sb * TN, qt + kk * 8,
+                                kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk,
+                                kk > 0 ? 1u : 0u);
+                    umma_commit(&bars[Smem::B_SFULL + sb]);
+                    if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
+                }
+                __syncwarp();
                 if (pend_it >= 0) ok = issue_pv(pend_it, pend_first, pend_nbox);
                 pend_it = it;
                 pend_first = first;
@@ -741,9 +778,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
             }
             if (ok && pend_it >= 0) ok = issue_pv(pend_it, pend_first, pend_nbox);
-            // make sure every tensor-core op finished before TMEM is released
-            umma_commit(&bars[Smem::B_DRAIN]);
-            mbar_drain(&bars[Smem::B_DRAIN], 0);
+            // every tensor-core op must be finished before TMEM is released
+            if (lane == 0) {
+                umma_commit(&bars[Smem::B_DRAIN]);
+                mbar_drain(&bars[Smem::B_DRAIN], 0);
+            }
+            __syncwarp();
         }
     } else {
         Cta x;
@@ -907,7 +947,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
     }
     // K/V: [rows = num_pages*Hkv*P] x [2 halves] x [64 columns]; one box =
     // BH consecutive rows of one page, both halves
-    const int BH = a.P < TN ? a.P : TN;
+    const int BH = BOX_ROWS;
     const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
     for (int t = 0; t < 2; ++t) {
         cuuint64_t dims[3] = {64, rows, 2};

@@ -201,6 +201,13 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         : "memory");
 }
 
+// Copy a 128-row x 256-bit matrix (described by a smem descriptor) into TMEM
+// lanes 0..127, 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile(
