@@ -52,7 +52,7 @@ constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
-constexpr int THREADS = 6 * 32;           // softmax 0-3, MMA 4, producer 5
+constexpr int THREADS = 7 * 32;           // softmax 0-3, QK MMA 4, PV MMA 5, producer 6
 // TMEM columns: S0 [0,64) S1 [64,128) O [128,256) P0 [256,288) P1 [288,320)
 // Q0 [320,384) Q1 [384,448) (bf16 pairs)
 constexpr uint32_t TMEM_COLS = 512;
@@ -72,7 +72,7 @@ struct Smem {
     // barriers (uint64 each)
     static constexpr int B_KVFULL = 0, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
                          B_QEMPTY = 3 * NS + 2, B_SFULL = 3 * NS + 4, B_PFULL = 3 * NS + 6,
-                         B_ODONE = 3 * NS + 8, B_DRAIN = 3 * NS + 9, NUM_BARS = 3 * NS + 10;
+                         B_ODONE = 3 * NS + 8, B_DRAIN = 3 * NS + 10, NUM_BARS = 3 * NS + 12;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
     static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
     static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
@@ -280,12 +280,21 @@ __device__ void softmax_role(const Cta& x) {
                 pk[c2] = pack_bf16x2(p0, p1);
             }
             l += psum0 + psum1;
+            // P buffer sb is free once P V(it-2) has finished.  P V of tile j
+            // completes a phase of o_done[j & 1]; the next phase of that
+            // barrier needs this tile's P, so the parity wait is unambiguous
+            if (it >= 2) {
+                ok = warp_wait(&bars[Smem::B_ODONE + (it & 1)], ((it - 2) >> 1) & 1, x.abort_flag,
+                               a.dev_err);
+                tc_fence_after();
+            }
             // this copy's slice of P; the other slices of this lane stay zero
             store_cols<CW / 2>(lane_base + TM_P + sb * (TN / 2) + c * (CW / 2), pk);
             tmem_wait_st();
             if (!first && __any_sync(0xffffffffu, move)) {
                 // O must hold every earlier P V before it is rescaled
-                ok = warp_wait(&bars[Smem::B_ODONE], (it - 1) & 1, x.abort_flag, a.dev_err);
+                ok = warp_wait(&bars[Smem::B_ODONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1,
+                                   x.abort_flag, a.dev_err);
                 if (ok) {
                     tc_fence_after();
 #pragma unroll
@@ -328,8 +337,11 @@ __device__ void softmax_role(const Cta& x) {
             if (ok && warp_active) {
                 // observe P V(it-1) before P V(it) so the parity wait is unambiguous
                 if (!first)
-                    ok = warp_wait(&bars[Smem::B_ODONE], (it - 1) & 1, x.abort_flag, a.dev_err);
-                if (ok) ok = warp_wait(&bars[Smem::B_ODONE], it & 1, x.abort_flag, a.dev_err);
+                    ok = warp_wait(&bars[Smem::B_ODONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1,
+                                   x.abort_flag, a.dev_err);
+                if (ok)
+                    ok = warp_wait(&bars[Smem::B_ODONE + (it & 1)], (it >> 1) & 1, x.abort_flag,
+                                   a.dev_err);
                 tc_fence_after();
             }
             const bool complete = cur.seg_start >= x.t_begin && cur.seg_start + cur.nb <= x.t_end;
@@ -510,8 +522,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&bars[Smem::B_SFULL + q], 1);
             mbar_init(&bars[Smem::B_PFULL + q], 4);
         }
-        mbar_init(&bars[Smem::B_ODONE], 1);
+        mbar_init(&bars[Smem::B_ODONE], 1);  // P V of even tiles
+        mbar_init(&bars[Smem::B_ODONE + 1], 1);  // P V of odd tiles
         mbar_init(&bars[Smem::B_DRAIN], 1);
+        mbar_init(&bars[Smem::B_DRAIN + 1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -565,8 +579,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp == 5) {
-        // ================= TMA producer (warp 5) =================
+    if (warp == 6) {
+        // ================= TMA producer (warp 6) =================
         // One 3-D box per (page, tensor): both 64-column halves of BH keys of
         // one kv-head, 256*BH bytes, landing as [half][key][128 B] with the
         // 128-byte swizzle the MMAs read.  Boxes of a tile are issued by
@@ -672,21 +686,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             for (int q = 0; q < 2; ++q)
                 if (issued_q[q] > 0) mbar_drain(&bars[Smem::B_QFULL + q], (issued_q[q] - 1) & 1);
         }
-    } else if (warp == 4) {
-        // ================= MMA issuer (lane 0) + K relayout (whole warp) =================
-        // A K box lands as [h0 rows 0-7 | h0 rows 8-15 | h1 rows 0-7 | h1 rows 8-15]
-        // (1 KB blocks, 128-byte swizzle).  Swapping the middle blocks gives
-        // [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15]: every 8-key group of the tile
-        // is then 2 KB after the previous one, one uniform stride for an
-        // N = 64 QK MMA.  The swizzle phase of a row is its index mod 8, which
-        // the move keeps.  V keeps the box layout; P V runs one K = 16 MMA per box.
+    } else if (warp == 4 || warp == 5) {
+        // ================= tensor-core issue: warp 4 = Q K^T, warp 5 = P V =================
+        // A tcgen05.mma takes ~100 cycles to issue from one warp whatever its
+        // N, so the two GEMMs of a tile are issued by two warps in parallel.
+        //
+        // Warp 4 also relayouts K: a K box lands as [h0 rows 0-7 | h0 rows
+        // 8-15 | h1 rows 0-7 | h1 rows 8-15] (1 KB blocks, 128-byte swizzle);
+        // swapping the middle blocks gives [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15],
+        // so every 8-key group of the tile sits 2 KB after the previous one (one
+        // uniform stride for an N = 64 MMA).  A row's swizzle phase is its index
+        // mod 8, which the move keeps.  V keeps the box layout; P V runs one
+        // K = 16 MMA per box.
+        const bool qk_warp = warp == 4;
         if (n_tiles > 0) {
             Cursor cur;
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             int pc = -1;
             bool ok = true;
-            int pend_it = -1, pend_nbox = 0;
-            bool pend_first = false;
             const uint32_t idesc_qk = umma_idesc_bf16(ROWS, TN, 0, 0);
             // smem descriptors are built once; an operand's start address
             // lives in the low 14 bits (in 16-byte units), so stepping to
@@ -695,93 +712,94 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const uint64_t kdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::STAGES), 16, 2048);
             const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::STAGES + KV_BYTES),
                                                      BOX_ROWS * 128, 1024);
-            // O += P V over the first nbox boxes of tile j (the rest are past
-            // the sequence end and hold no probability mass)
-            auto issue_pv = [&](int j, bool first_of_piece, int nbox) -> bool {
-                const int sbj = j & 1, sj = j % NS;
-                if (!warp_wait(&bars[Smem::B_PFULL + sbj], (j >> 1) & 1, abort_flag, a.dev_err))
-                    return false;
-                tc_fence_after();
-                if (lane == 0) {
-                    // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
-                    const uint64_t vd = vdesc0 + ((uint32_t)(sj * STAGE_BYTES) >> 4);
-                    const uint32_t pcol = tmem + TM_P + sbj * (TN / 2);
-#pragma unroll
-                    for (int bx = 0; bx < MAX_BOX; ++bx)
-                        if (bx < nbox)
-                            umma_ts(tmem + TM_O, pcol + bx * (BOX_ROWS / 2),
-                                    vd + ((bx * BOX_ROWS * 256) >> 4), IDESC_PV,
-                                    (bx > 0 || !first_of_piece) ? 1u : 0u);
-                    umma_commit(&bars[Smem::B_KVEMPTY + sj]);
-                    umma_commit(&bars[Smem::B_ODONE]);
-                }
-                __syncwarp();
-                return true;
-            };
             for (int it = 0; it < n_tiles && ok; ++it) {
                 const bool first = (it == 0) || (cur.lt == 0);
                 const bool last = (it == n_tiles - 1) || (cur.lt == cur.nb - 1);
                 if (first) ++pc;
-                const int qb = pc & 1;
-                if (first)
-                    ok = warp_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag, a.dev_err);
-                const int s = it % NS;
-                if (ok)
-                    ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
-                if (!ok) break;
+                const int qb = pc & 1, s = it % NS, sb = it & 1;
                 const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
                 const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-                {
-                    // K relayout: swap 1 KB blocks 1 and 2 of every loaded box
-                    uint4* kst = reinterpret_cast<uint4*>(sm + Smem::STAGES + s * STAGE_BYTES);
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        uint4* b1 = kst + bx * (BOX_ROWS * 256 / 16) + 1024 / 16;
-                        uint4* b2 = b1 + 1024 / 16;
-                        const uint4 x0 = b1[lane], x1 = b1[lane + 32];
-                        const uint4 y0 = b2[lane], y1 = b2[lane + 32];
-                        b1[lane] = y0;
-                        b1[lane + 32] = y1;
-                        b2[lane] = x0;
-                        b2[lane + 32] = x1;
+                if (qk_warp) {
+                    if (first)
+                        ok = warp_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag,
+                                       a.dev_err);
+                    if (ok)
+                        ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag,
+                                       a.dev_err);
+                    // S buffer sb is free once the softmax has read tile it-2
+                    if (ok && it >= 2)
+                        ok = warp_wait(&bars[Smem::B_PFULL + sb], ((it - 2) >> 1) & 1, abort_flag,
+                                       a.dev_err);
+                    if (!ok) break;
+                    {
+                        // K relayout: swap 1 KB blocks 1 and 2 of every loaded box
+                        uint4* kst = reinterpret_cast<uint4*>(sm + Smem::STAGES + s * STAGE_BYTES);
+                        for (int bx = 0; bx < nbox; ++bx) {
+                            uint4* b1 = kst + bx * (BOX_ROWS * 256 / 16) + 1024 / 16;
+                            uint4* b2 = b1 + 1024 / 16;
+                            const uint4 x0 = b1[lane], x1 = b1[lane + 32];
+                            const uint4 y0 = b2[lane], y1 = b2[lane + 32];
+                            b1[lane] = y0;
+                            b1[lane + 32] = y1;
+                            b2[lane] = x0;
+                            b2[lane + 32] = x1;
+                        }
+                        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
                     }
-                    fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-                }
-                __syncwarp();
-                tc_fence_after();
-                const int sb = it & 1;
-                if (lane == 0) {
-                    const uint32_t qt = tmem + TM_Q + qb * (D / 2);
-                    if (first) {
-                        // Q of this piece: smem (TMA, 128-byte swizzle) -> TMEM once;
-                        // k-slice kk = 64-column half kk/4, 32-byte step kk%4
-                        const uint64_t qd = qdesc0 + ((uint32_t)(qb * Q_BYTES) >> 4);
+                    __syncwarp();
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t qt = tmem + TM_Q + qb * (D / 2);
+                        if (first) {
+                            // Q of this piece: smem (TMA, 128-byte swizzle) -> TMEM once;
+                            // k-slice kk = 64-column half kk/4, 32-byte step kk%4
+                            const uint64_t qd = qdesc0 + ((uint32_t)(qb * Q_BYTES) >> 4);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                tmem_cp_128x256b(qt + kk * 8,
+                                                 qd + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                        }
+                        // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
+                        const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            tmem_cp_128x256b(qt + kk * 8,
-                                             qd + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                            umma_ts(tmem + TM_S + sb * TN, qt + kk * 8,
+                                    kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                        umma_commit(&bars[Smem::B_SFULL + sb]);
+                        if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
                     }
-                    // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
-                    const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                    __syncwarp();
+                } else {
+                    // O += P V over the first nbox boxes of tile it (the rest are
+                    // past the sequence end and hold no probability mass)
+                    ok = warp_wait(&bars[Smem::B_PFULL + sb], (it >> 1) & 1, abort_flag, a.dev_err);
+                    if (ok)
+                        ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag,
+                                       a.dev_err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
+                        const uint64_t vd = vdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                        const uint32_t pcol = tmem + TM_P + sb * (TN / 2);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ts(tmem + TM_S + sb * TN, qt + kk * 8,
-                                kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk,
-                                kk > 0 ? 1u : 0u);
-                    umma_commit(&bars[Smem::B_SFULL + sb]);
-                    if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
+                        for (int bx = 0; bx < MAX_BOX; ++bx)
+                            if (bx < nbox)
+                                umma_ts(tmem + TM_O, pcol + bx * (BOX_ROWS / 2),
+                                        vd + ((bx * BOX_ROWS * 256) >> 4), IDESC_PV,
+                                        (bx > 0 || !first) ? 1u : 0u);
+                        umma_commit(&bars[Smem::B_KVEMPTY + s]);
+                        umma_commit(&bars[Smem::B_ODONE + sb]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
-                if (pend_it >= 0) ok = issue_pv(pend_it, pend_first, pend_nbox);
-                pend_it = it;
-                pend_first = first;
-                pend_nbox = nbox;
                 if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
             }
-            if (ok && pend_it >= 0) ok = issue_pv(pend_it, pend_first, pend_nbox);
-            // every tensor-core op must be finished before TMEM is released
+            // every tensor-core op of this warp must finish before TMEM is released
             if (lane == 0) {
-                umma_commit(&bars[Smem::B_DRAIN]);
-                mbar_drain(&bars[Smem::B_DRAIN], 0);
+                umma_commit(&bars[Smem::B_DRAIN + (qk_warp ? 0 : 1)]);
+                mbar_drain(&bars[Smem::B_DRAIN + (qk_warp ? 0 : 1)], 0);
             }
             __syncwarp();
         }
