@@ -43,7 +43,7 @@ namespace {
 
 constexpr int D = 128;
 constexpr int TN = 64;           // keys per tile
-constexpr int NS = 4;            // K/V pipeline stages
+constexpr int NS = 5;            // K/V pipeline stages
 constexpr int ROWS = 128;        // MMA M: query rows (padded / replicated)
 constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
@@ -52,12 +52,13 @@ constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
-constexpr int THREADS = 7 * 32;           // softmax 0-3, QK MMA 4, PV MMA 5, producer 6
+constexpr int THREADS = 8 * 32;  // softmax 0-3, QK MMA 4, PV MMA 5, producer 6, K relayout 7
 // TMEM columns: S0 [0,64) S1 [64,128) O [128,256) P0 [256,288) P1 [288,320)
 // Q0 [320,384) Q1 [384,448) (bf16 pairs)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 256, TM_Q = 320;
-constexpr int MAX_BATCH = 2048;
+constexpr int MAX_BATCH = 1024;
+constexpr int SCRATCH_BYTES = 16 * 1024;  // copy-merge buffer of the epilogue
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -66,13 +67,14 @@ constexpr uint32_t IDESC_PV = umma_idesc_bf16(ROWS, D, 0, 1);   // B (V) MN-majo
 
 struct Smem {
     // offsets from the 1024-aligned base
-    static constexpr int Q = 0;
-    static constexpr int STAGES = Q + 2 * Q_BYTES;
-    static constexpr int BARS = STAGES + NS * STAGE_BYTES;
+    static constexpr int Q = 0;                                // one Q staging buffer
+    static constexpr int STAGES = Q + Q_BYTES;
+    static constexpr int SCRATCH = STAGES + NS * STAGE_BYTES;
+    static constexpr int BARS = SCRATCH + SCRATCH_BYTES;
     // barriers (uint64 each)
-    static constexpr int B_KVFULL = 0, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
-                         B_QEMPTY = 3 * NS + 2, B_SFULL = 3 * NS + 4, B_PFULL = 3 * NS + 6,
-                         B_ODONE = 3 * NS + 8, B_DRAIN = 3 * NS + 10, NUM_BARS = 3 * NS + 12;
+    static constexpr int B_KVFULL = 0, B_KREADY = NS, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
+                         B_QFREE = 3 * NS + 1, B_SFULL = 3 * NS + 2, B_PFULL = 3 * NS + 4,
+                         B_ODONE = 3 * NS + 6, B_DRAIN = 3 * NS + 8, NUM_BARS = 3 * NS + 10;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
     static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
     static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
@@ -231,11 +233,9 @@ __device__ void softmax_role(const Cta& x) {
     Cursor cur;
     if (x.n_tiles > 0) cur.init(x.t_begin, x.s_pre, x.s_ctx, a.B, a.Hkv, k);
     bool ok = true;
-    int pc = -1;
     for (int it = 0; it < x.n_tiles; ++it) {
         const bool first = (it == 0) || (cur.lt == 0);
         const bool last = (it == x.n_tiles - 1) || (cur.lt == cur.nb - 1);
-        if (first) ++pc;
         const int sb = it & 1;
         const int ctx = x.s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
         const int nvalid = min(TN, L - key0);
@@ -333,7 +333,6 @@ __device__ void softmax_role(const Cta& x) {
 
         if (last) {
             // ---- epilogue of the piece that ends at this tile
-            const int qb = pc & 1;
             if (ok && warp_active) {
                 // observe P V(it-1) before P V(it) so the parity wait is unambiguous
                 if (!first)
@@ -396,8 +395,8 @@ __device__ void softmax_role(const Cta& x) {
                 }
             } else {
                 // merge the REP copies of every row: weights from (m, l), the
-                // weighted O rows summed in fp32 in the Q buffer of this piece
-                // (its QK MMAs are done), rows swizzled by 16-byte chunk
+                // weighted O rows summed in fp32 in the scratch buffer (rows
+                // swizzled by 16-byte chunk), one or two column passes
                 if (row_valid) {
                     s_stat_m[c * ROWS + r] = m_ref;
                     s_stat_l[c * ROWS + r] = l;
@@ -417,75 +416,71 @@ __device__ void softmax_role(const Cta& x) {
                     w = (Lsum > 0.f && m_ref != -INFINITY) ? fast_exp2(m_ref - mt) / Lsum : 0.f;
                     lse = Lsum > 0.f ? (mt + log2f(Lsum)) * kLn2 : -INFINITY;
                 }
-                float* scratch = reinterpret_cast<float*>(x.sm + Smem::Q + qb * Q_BYTES);
+                // columns per pass so that R x CPP floats fit the 16 KB scratch
+                constexpr int CPP = REP == 4 ? D : D / 2;
+                constexpr int NCH = CPP / 4;  // 16-byte chunks of a scratch row
+                float* scratch = reinterpret_cast<float*>(x.sm + Smem::SCRATCH);
+#pragma unroll
+                for (int pass = 0; pass < D / CPP; ++pass) {
 #pragma unroll 1
-                for (int cc = 0; cc < REP; ++cc) {
-                    if (ok && warp_active && c == cc) {
+                    for (int cc = 0; cc < REP; ++cc) {
+                        if (ok && warp_active && c == cc) {
 #pragma unroll
-                        for (int c4 = 0; c4 < D / 32; ++c4) {
-                            uint32_t ov[32];
-                            tmem_ld32(lane_base + TM_O + c4 * 32, ov);
-                            tmem_wait_ld();
-                            if (!row_valid) continue;
+                            for (int c4 = 0; c4 < CPP / 32; ++c4) {
+                                uint32_t ov[32];
+                                tmem_ld32(lane_base + TM_O + pass * CPP + c4 * 32, ov);
+                                tmem_wait_ld();
+                                if (!row_valid) continue;
 #pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                const int chunk = c4 * 8 + v;
-                                float4* dst = reinterpret_cast<float4*>(
-                                    scratch + r * D + ((chunk ^ (r & 31)) * 4));
-                                float4 o = make_float4(__uint_as_float(ov[4 * v + 0]) * w,
-                                                       __uint_as_float(ov[4 * v + 1]) * w,
-                                                       __uint_as_float(ov[4 * v + 2]) * w,
-                                                       __uint_as_float(ov[4 * v + 3]) * w);
-                                if (cc > 0) {
-                                    const float4 prev = *dst;
-                                    o.x += prev.x;
-                                    o.y += prev.y;
-                                    o.z += prev.z;
-                                    o.w += prev.w;
+                                for (int v = 0; v < 8; ++v) {
+                                    const int chunk = c4 * 8 + v;
+                                    float4* dst = reinterpret_cast<float4*>(
+                                        scratch + r * CPP + ((chunk ^ (r & (NCH - 1))) * 4));
+                                    float4 o = make_float4(__uint_as_float(ov[4 * v + 0]) * w,
+                                                           __uint_as_float(ov[4 * v + 1]) * w,
+                                                           __uint_as_float(ov[4 * v + 2]) * w,
+                                                           __uint_as_float(ov[4 * v + 3]) * w);
+                                    if (cc > 0) {
+                                        const float4 prev = *dst;
+                                        o.x += prev.x;
+                                        o.y += prev.y;
+                                        o.z += prev.z;
+                                        o.w += prev.w;
+                                    }
+                                    *dst = o;
                                 }
-                                *dst = o;
+                            }
+                        }
+                        named_bar_sync(1, 128);
+                    }
+                    if (ok) {
+                        for (int idx = tid; idx < R * NCH; idx += 128) {
+                            const int rr = idx / NCH, chunk = idx % NCH;
+                            const float4 o = *reinterpret_cast<const float4*>(
+                                scratch + rr * CPP + ((chunk ^ (rr & (NCH - 1))) * 4));
+                            const int col = pass * CPP + chunk * 4;
+                            if (complete) {
+                                uint2 w2;
+                                w2.x = pack_bf16x2(o.x, o.y);
+                                w2.y = pack_bf16x2(o.z, o.w);
+                                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                          out_row(rr) * D + col) = w2;
+                            } else {
+                                *reinterpret_cast<float4*>(
+                                    x.prm->part_o + ((int64_t)slot * ROWS + rr) * D + col) = o;
                             }
                         }
                     }
-                    named_bar_sync(1, 128);
+                    named_bar_sync(1, 128);  // scratch reused by the next pass / piece
                 }
-                if (ok) {
-                    for (int idx = tid; idx < R * (D / 4); idx += 128) {
-                        const int rr = idx / (D / 4), chunk = idx % (D / 4);
-                        const float4 o = *reinterpret_cast<const float4*>(
-                            scratch + rr * D + ((chunk ^ (rr & 31)) * 4));
-                        if (complete) {
-                            uint2 w2;
-                            w2.x = pack_bf16x2(o.x, o.y);
-                            w2.y = pack_bf16x2(o.z, o.w);
-                            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
-                                                     out_row(rr) * D)[chunk] = w2;
-                        } else {
-                            reinterpret_cast<float4*>(
-                                x.prm->part_o + ((int64_t)slot * ROWS + rr) * D)[chunk] = o;
-                        }
-                    }
-                    if (row_valid && c == 0) {
-                        if (complete) {
-                            if (a.lse) a.lse[out_row(r)] = lse;
-                        } else {
-                            x.prm->part_lse[(int64_t)slot * ROWS + r] = lse;
-                        }
+                if (ok && row_valid && c == 0) {
+                    if (complete) {
+                        if (a.lse) a.lse[out_row(r)] = lse;
+                    } else {
+                        x.prm->part_lse[(int64_t)slot * ROWS + r] = lse;
                     }
                 }
-                named_bar_sync(1, 128);
-                // restore the zero padding rows the scratch overwrote
-                uint4* q4 = reinterpret_cast<uint4*>(scratch);
-                for (int e = tid; e < R * D * 4 / 16; e += 128) {
-                    const int row = (e % (Q_HALF / 16)) / 8;
-                    if (!q_row_used(row, R, RQ, REP)) q4[e] = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
             }
-            // the Q buffer of this piece may now be reloaded
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[Smem::B_QEMPTY + qb]);
         }
         if (it + 1 < x.n_tiles) cur.next(x.s_ctx, a.Hkv, k);
     }
@@ -514,18 +509,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[Smem::B_KVFULL + s], 1);
+            mbar_init(&bars[Smem::B_KREADY + s], 1);
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
+        mbar_init(&bars[Smem::B_QFULL], 1);
+        mbar_init(&bars[Smem::B_QFREE], 1);
         for (int q = 0; q < 2; ++q) {
-            mbar_init(&bars[Smem::B_QFULL + q], 1);
-            mbar_init(&bars[Smem::B_QEMPTY + q], 1 + 4);  // MMA commit + 4 softmax warps
             mbar_init(&bars[Smem::B_SFULL + q], 1);
             mbar_init(&bars[Smem::B_PFULL + q], 4);
+            mbar_init(&bars[Smem::B_ODONE + q], 1);  // P V of even / odd tiles
+            mbar_init(&bars[Smem::B_DRAIN + q], 1);
         }
-        mbar_init(&bars[Smem::B_ODONE], 1);  // P V of even tiles
-        mbar_init(&bars[Smem::B_ODONE + 1], 1);  // P V of odd tiles
-        mbar_init(&bars[Smem::B_DRAIN], 1);
-        mbar_init(&bars[Smem::B_DRAIN + 1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -536,7 +530,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     {
         // rows that hold no query stay zero in both Q buffers
         uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
-        for (int e = tid; e < 2 * Q_BYTES / 16; e += THREADS) {
+        for (int e = tid; e < Q_BYTES / 16; e += THREADS) {
             const int row = (e % (Q_HALF / 16)) / 8;
             if (!q_row_used(row, R, RQ, REP)) q4[e] = make_uint4(0, 0, 0, 0);
         }
@@ -616,7 +610,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         int pc = -1;
         int n_issued = 0;
-        int issued_q[2] = {0, 0};
+        int issued_q = 0;
         bool ok = true;
         for (int it = 0; it < n_tiles && ok; ++it) {
             if (it + LOOKAHEAD < n_tiles) {
@@ -628,20 +622,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             __syncwarp();
             const bool first = (it == 0) || (cur.lt == 0);
             if (first) {
+                // Q of the next piece once the previous one has been copied to TMEM
                 ++pc;
-                const int qb = pc & 1, use = pc >> 1;
                 if (lane == 0) {
-                    if (use >= 1)
-                        ok = mbar_wait(&bars[Smem::B_QEMPTY + qb], (use - 1) & 1, abort_flag,
-                                       a.dev_err);
+                    if (pc >= 1)
+                        ok = mbar_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag, a.dev_err);
                     if (ok) {
-                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL + qb], REP * 2 * R * 128);
+                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL], REP * 2 * R * 128);
                         for (int c = 0; c < REP; ++c)
                             for (int h = 0; h < 2; ++h)
-                                tma_load_3d(sm + Smem::Q + qb * Q_BYTES + h * Q_HALF + c * RQ * 128,
-                                            &qmap, &bars[Smem::B_QFULL + qb], h * 64, cur.kvh * G,
-                                            cur.b * k);
-                        issued_q[qb] = use + 1;
+                                tma_load_3d(sm + Smem::Q + h * Q_HALF + c * RQ * 128, &qmap,
+                                            &bars[Smem::B_QFULL], h * 64, cur.kvh * G, cur.b * k);
+                        issued_q = pc + 1;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -683,20 +675,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
                 if (uses > 0) mbar_drain(&bars[Smem::B_KVFULL + s], (uses - 1) & 1);
             }
-            for (int q = 0; q < 2; ++q)
-                if (issued_q[q] > 0) mbar_drain(&bars[Smem::B_QFULL + q], (issued_q[q] - 1) & 1);
+            if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
+        }
+    } else if (warp == 7) {
+        // ================= K relayout (warp 7) =================
+        // A K box lands as [h0 rows 0-7 | h0 rows 8-15 | h1 rows 0-7 | h1 rows
+        // 8-15] (1 KB blocks, 128-byte swizzle).  Swapping the middle blocks
+        // gives [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15]: every 8-key group of the
+        // tile then sits 2 KB after the previous one.  A row's swizzle phase is
+        // its index mod 8, which the move keeps.
+        Cursor cur;
+        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            const int s = it % NS;
+            const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
+            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
+            ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
+            if (!ok) break;
+            uint4* kst = reinterpret_cast<uint4*>(sm + Smem::STAGES + s * STAGE_BYTES);
+            for (int bx = 0; bx < nbox; ++bx) {
+                uint4* b1 = kst + bx * (BOX_ROWS * 256 / 16) + 1024 / 16;
+                uint4* b2 = b1 + 1024 / 16;
+                const uint4 x0 = b1[lane], x1 = b1[lane + 32];
+                const uint4 y0 = b2[lane], y1 = b2[lane + 32];
+                b1[lane] = y0;
+                b1[lane + 32] = y1;
+                b2[lane] = x0;
+                b2[lane + 32] = x1;
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Smem::B_KREADY + s]);
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
     } else if (warp == 4 || warp == 5) {
         // ================= tensor-core issue: warp 4 = Q K^T, warp 5 = P V =================
         // A tcgen05.mma takes ~100 cycles to issue from one warp whatever its
         // N, so the two GEMMs of a tile are issued by two warps in parallel.
         //
-        // Warp 4 also relayouts K: a K box lands as [h0 rows 0-7 | h0 rows
-        // 8-15 | h1 rows 0-7 | h1 rows 8-15] (1 KB blocks, 128-byte swizzle);
-        // swapping the middle blocks gives [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15],
-        // so every 8-key group of the tile sits 2 KB after the previous one (one
-        // uniform stride for an N = 64 MMA).  A row's swizzle phase is its index
-        // mod 8, which the move keeps.  V keeps the box layout; P V runs one
+        // K arrives relayouted by warp 7 (8-key groups 2 KB apart, one uniform
+        // stride for an N = 64 MMA); V keeps the box layout and P V runs one
         // K = 16 MMA per box.
         const bool qk_warp = warp == 4;
         if (n_tiles > 0) {
@@ -714,38 +733,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                                      BOX_ROWS * 128, 1024);
             for (int it = 0; it < n_tiles && ok; ++it) {
                 const bool first = (it == 0) || (cur.lt == 0);
-                const bool last = (it == n_tiles - 1) || (cur.lt == cur.nb - 1);
                 if (first) ++pc;
                 const int qb = pc & 1, s = it % NS, sb = it & 1;
                 const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
                 const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
                 if (qk_warp) {
                     if (first)
-                        ok = warp_wait(&bars[Smem::B_QFULL + qb], (pc >> 1) & 1, abort_flag,
-                                       a.dev_err);
+                        ok = warp_wait(&bars[Smem::B_QFULL], pc & 1, abort_flag, a.dev_err);
+                    // K of tile it landed and was relayouted (warp 7)
                     if (ok)
-                        ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag,
+                        ok = warp_wait(&bars[Smem::B_KREADY + s], (it / NS) & 1, abort_flag,
                                        a.dev_err);
                     // S buffer sb is free once the softmax has read tile it-2
                     if (ok && it >= 2)
                         ok = warp_wait(&bars[Smem::B_PFULL + sb], ((it - 2) >> 1) & 1, abort_flag,
                                        a.dev_err);
                     if (!ok) break;
-                    {
-                        // K relayout: swap 1 KB blocks 1 and 2 of every loaded box
-                        uint4* kst = reinterpret_cast<uint4*>(sm + Smem::STAGES + s * STAGE_BYTES);
-                        for (int bx = 0; bx < nbox; ++bx) {
-                            uint4* b1 = kst + bx * (BOX_ROWS * 256 / 16) + 1024 / 16;
-                            uint4* b2 = b1 + 1024 / 16;
-                            const uint4 x0 = b1[lane], x1 = b1[lane + 32];
-                            const uint4 y0 = b2[lane], y1 = b2[lane + 32];
-                            b1[lane] = y0;
-                            b1[lane + 32] = y1;
-                            b2[lane] = x0;
-                            b2[lane + 32] = x1;
-                        }
-                        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-                    }
                     __syncwarp();
                     tc_fence_after();
                     if (lane == 0) {
@@ -753,11 +756,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         if (first) {
                             // Q of this piece: smem (TMA, 128-byte swizzle) -> TMEM once;
                             // k-slice kk = 64-column half kk/4, 32-byte step kk%4
-                            const uint64_t qd = qdesc0 + ((uint32_t)(qb * Q_BYTES) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
                                 tmem_cp_128x256b(qt + kk * 8,
-                                                 qd + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                                                 qdesc0 + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                            // the staging buffer may take the next piece's Q once
+                            // these copies (and everything before them) are done
+                            umma_commit(&bars[Smem::B_QFREE]);
                         }
                         // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
                         const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
@@ -767,7 +772,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                     kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk,
                                     kk > 0 ? 1u : 0u);
                         umma_commit(&bars[Smem::B_SFULL + sb]);
-                        if (last) umma_commit(&bars[Smem::B_QEMPTY + qb]);
                     }
                     __syncwarp();
                 } else {
