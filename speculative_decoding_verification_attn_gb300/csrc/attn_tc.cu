@@ -52,11 +52,13 @@ constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
-constexpr int THREADS = 8 * 32;  // softmax 0-3, QK MMA 4, PV MMA 5, producer 6, K relayout 7
-// TMEM columns: S0 [0,64) S1 [64,128) O [128,256) P0 [256,288) P1 [288,320)
-// Q0 [320,384) Q1 [384,448) (bf16 pairs)
+// warps: softmax 0-3, Q K^T halves 4-5, P V 6, TMA producer 7, K relayout 8
+constexpr int THREADS = 9 * 32;
+// TMEM columns: partial scores of head-dim half 0 / 1, double buffered,
+// SA [0,128) SB [128,256); O [256,384); P0 [384,416) P1 [416,448);
+// Q [448,512) (bf16 pairs)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 256, TM_Q = 320;
+constexpr uint32_t TM_S = 0, TM_SB = 128, TM_O = 256, TM_P = 384, TM_Q = 448;
 constexpr int MAX_BATCH = 1024;
 constexpr int SCRATCH_BYTES = 16 * 1024;  // copy-merge buffer of the epilogue
 constexpr float kLog2e = 1.4426950408889634f;
@@ -74,7 +76,8 @@ struct Smem {
     // barriers (uint64 each)
     static constexpr int B_KVFULL = 0, B_KREADY = NS, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
                          B_QFREE = 3 * NS + 1, B_SFULL = 3 * NS + 2, B_PFULL = 3 * NS + 4,
-                         B_ODONE = 3 * NS + 6, B_DRAIN = 3 * NS + 8, NUM_BARS = 3 * NS + 10;
+                         B_ODONE = 3 * NS + 6, B_DRAIN = 3 * NS + 8, B_QCP = 3 * NS + 11,
+                         NUM_BARS = 3 * NS + 13;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
     static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
     static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
@@ -247,9 +250,13 @@ __device__ void softmax_role(const Cta& x) {
         if (ok) ok = warp_wait(&bars[Smem::B_SFULL + sb], (it >> 1) & 1, x.abort_flag, a.dev_err);
         if (ok && warp_active) {
             tc_fence_after();
-            uint32_t sr[CW];
+            uint32_t sr[CW], sr2[CW];
             load_cols<CW>(lane_base + TM_S + sb * TN + cbase, sr);
+            load_cols<CW>(lane_base + TM_SB + sb * TN + cbase, sr2);
             tmem_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < CW; ++cc)  // S = S(dims 0-63) + S(dims 64-127)
+                sr[cc] = __float_as_uint(__uint_as_float(sr[cc]) + __uint_as_float(sr2[cc]));
             // keys of this row visible in this copy's slice: cc < cmax
             const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
             // branch-free: masked scores become -inf (exp2 -> 0)
@@ -513,13 +520,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
         mbar_init(&bars[Smem::B_QFULL], 1);
-        mbar_init(&bars[Smem::B_QFREE], 1);
+        mbar_init(&bars[Smem::B_QFREE], 2);  // one commit per Q K^T warp
         for (int q = 0; q < 2; ++q) {
-            mbar_init(&bars[Smem::B_SFULL + q], 1);
+            mbar_init(&bars[Smem::B_SFULL + q], 2);  // both head-dim halves of S
             mbar_init(&bars[Smem::B_PFULL + q], 4);
             mbar_init(&bars[Smem::B_ODONE + q], 1);  // P V of even / odd tiles
-            mbar_init(&bars[Smem::B_DRAIN + q], 1);
+            mbar_init(&bars[Smem::B_QCP + q], 1);
         }
+        for (int q = 0; q < 3; ++q) mbar_init(&bars[Smem::B_DRAIN + q], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -573,8 +581,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp == 6) {
-        // ================= TMA producer (warp 6) =================
+    if (warp == 7) {
+        // ================= TMA producer (warp 7) =================
         // One 3-D box per (page, tensor): both 64-column halves of BH keys of
         // one kv-head, 256*BH bytes, landing as [half][key][128 B] with the
         // 128-byte swizzle the MMAs read.  Boxes of a tile are issued by
@@ -677,8 +685,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
         }
-    } else if (warp == 7) {
-        // ================= K relayout (warp 7) =================
+    } else if (warp == 8) {
+        // ================= K relayout (warp 8) =================
         // A K box lands as [h0 rows 0-7 | h0 rows 8-15 | h1 rows 0-7 | h1 rows
         // 8-15] (1 KB blocks, 128-byte swizzle).  Swapping the middle blocks
         // gives [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15]: every 8-key group of the
@@ -709,15 +717,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (lane == 0) mbar_arrive(&bars[Smem::B_KREADY + s]);
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
-    } else if (warp == 4 || warp == 5) {
-        // ================= tensor-core issue: warp 4 = Q K^T, warp 5 = P V =================
+    } else if (warp >= 4 && warp <= 6) {
+        // ================= tensor-core issue: warps 4-5 = Q K^T, warp 6 = P V =================
         // A tcgen05.mma takes ~100 cycles to issue from one warp whatever its
-        // N, so the two GEMMs of a tile are issued by two warps in parallel.
+        // N, so the GEMMs of a tile are issued by three warps in parallel: Q K^T
+        // split by head-dim half into two partial score buffers (the softmax
+        // adds them), and P V.
         //
-        // K arrives relayouted by warp 7 (8-key groups 2 KB apart, one uniform
+        // K arrives relayouted by warp 8 (8-key groups 2 KB apart, one uniform
         // stride for an N = 64 MMA); V keeps the box layout and P V runs one
         // K = 16 MMA per box.
-        const bool qk_warp = warp == 4;
+        const int role = warp - 4;  // 0, 1: Q K^T head-dim half; 2: P V
         if (n_tiles > 0) {
             Cursor cur;
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
@@ -734,13 +744,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             for (int it = 0; it < n_tiles && ok; ++it) {
                 const bool first = (it == 0) || (cur.lt == 0);
                 if (first) ++pc;
-                const int qb = pc & 1, s = it % NS, sb = it & 1;
+                const int s = it % NS, sb = it & 1;
                 const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
                 const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-                if (qk_warp) {
-                    if (first)
+                if (role < 2) {
+                    const int h = role;  // head-dim half: columns 64h .. 64h+63
+                    if (first) {
                         ok = warp_wait(&bars[Smem::B_QFULL], pc & 1, abort_flag, a.dev_err);
-                    // K of tile it landed and was relayouted (warp 7)
+                        if (ok && pc >= 1) {
+                            // the previous piece's MMAs still read this half of
+                            // TMEM Q: wait for them before overwriting it
+                            if (lane == 0) umma_commit(&bars[Smem::B_QCP + h]);
+                            __syncwarp();
+                            ok = warp_wait(&bars[Smem::B_QCP + h], (pc - 1) & 1, abort_flag,
+                                           a.dev_err);
+                        }
+                    }
+                    // K of tile it landed and was relayouted (warp 8)
                     if (ok)
                         ok = warp_wait(&bars[Smem::B_KREADY + s], (it / NS) & 1, abort_flag,
                                        a.dev_err);
@@ -752,25 +772,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     __syncwarp();
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t qt = tmem + TM_Q + qb * (D / 2);
                         if (first) {
-                            // Q of this piece: smem (TMA, 128-byte swizzle) -> TMEM once;
-                            // k-slice kk = 64-column half kk/4, 32-byte step kk%4
+                            // this half of the piece's Q: smem (TMA, 128-byte
+                            // swizzle) -> TMEM; k-slice kk = 32-byte step kk%4
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk)
-                                tmem_cp_128x256b(qt + kk * 8,
-                                                 qdesc0 + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                            for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                                tmem_cp_128x256b(tmem + TM_Q + kk * 8,
+                                                 qdesc0 + h * (Q_HALF >> 4) + (kk & 3) * 2);
                             // the staging buffer may take the next piece's Q once
-                            // these copies (and everything before them) are done
+                            // both halves' copies are done
                             umma_commit(&bars[Smem::B_QFREE]);
                         }
-                        // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
-                        const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                        // S_h = Q_h K_h^T: K half h of 8-key group g at g*2 KB + h*1 KB
+                        const uint64_t kd =
+                            kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4) + h * (1024 >> 4);
+                        const uint32_t dcol = tmem + (h ? TM_SB : TM_S) + sb * TN;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            umma_ts(tmem + TM_S + sb * TN, qt + kk * 8,
-                                    kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk,
-                                    kk > 0 ? 1u : 0u);
+                        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                            umma_ts(dcol, tmem + TM_Q + kk * 8, kd + (kk & 3) * 2, idesc_qk,
+                                    (kk & 3) ? 1u : 0u);
                         umma_commit(&bars[Smem::B_SFULL + sb]);
                     }
                     __syncwarp();
@@ -802,8 +822,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             // every tensor-core op of this warp must finish before TMEM is released
             if (lane == 0) {
-                umma_commit(&bars[Smem::B_DRAIN + (qk_warp ? 0 : 1)]);
-                mbar_drain(&bars[Smem::B_DRAIN + (qk_warp ? 0 : 1)], 0);
+                umma_commit(&bars[Smem::B_DRAIN + role]);
+                mbar_drain(&bars[Smem::B_DRAIN + role], 0);
             }
             __syncwarp();
         }
