@@ -49,8 +49,7 @@ constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
 constexpr int KV_BYTES = TN * D * 2;      // 16 KB per tensor per stage
 constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
-constexpr int LOOKAHEAD = 12;             // tiles of block-table prefetch
-constexpr int PF_DIST = 8;                // tiles of L2 prefetch ahead of the smem loads
+constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
 // warps: softmax 0-3, Q K^T halves 4-5, P V 6, TMA producer 7, K relayout 8
@@ -589,11 +588,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // 128-byte swizzle the MMAs read.  Boxes of a tile are issued by
         // parallel lanes; block-table entries are prefetched LOOKAHEAD tiles
         // ahead with cp.async.
-        Cursor cur, ahead, pf;
+        Cursor cur, ahead;
         if (n_tiles > 0) {
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             ahead = cur;
-            pf = cur;
         }
         const uint64_t pol = l2_policy_evict_first();
         if (lane == 0) {
@@ -609,19 +607,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const int lp = (key0 + lane * BH) / P;
                 cp_async_4(&pid_ring[slot * MAX_BOX + lane],
                            &a.block_table[(int64_t)c.b * a.max_pages + lp]);
-            }
-        };
-        // L2 prefetch of the K and V boxes of tile `t` (ring slot must hold its entries)
-        auto prefetch_boxes = [&](const Cursor& c, int t) {
-            const int key0 = c.lt * TN;
-            const int nvalid = min(TN, s_ctx[c.b] + k - key0);
-            const int nbox = (nvalid + BH - 1) / BH;
-            if (lane < 2 * nbox) {
-                const int tensor = lane & 1, bx = lane >> 1;
-                int page = pid_ring[(t % (LOOKAHEAD + 1)) * MAX_BOX + bx];
-                if (page < 0 || page >= a.num_pages) page = 0;
-                const int row = (page * Hkv + c.kvh) * P + (key0 + bx * BH) % P;
-                tma_prefetch_3d(tensor ? (const void*)&vmap : (const void*)&kmap, 0, row, 0);
             }
         };
         for (int la = 0; la < LOOKAHEAD; ++la) {
@@ -641,9 +626,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
             }
             cp_async_commit();
-            // entries of tiles up to it + PF_DIST + 1 (tile `it` and the one
-            // this iteration prefetches into L2)
-            cp_async_wait<LOOKAHEAD - PF_DIST - 1>();
+            cp_async_wait<LOOKAHEAD>();  // entries of tile `it`
             __syncwarp();
             const bool first = (it == 0) || (cur.lt == 0);
             if (first) {
@@ -690,18 +673,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                  &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
             }
             n_issued = it + 1;
-            // L2 prefetch of the boxes PF_DIST tiles ahead: the smem loads
-            // then hit L2, which keeps more bytes in flight than the smem ring
-            // holds (the HBM latency under load is several thousand cycles)
-            if (it == 0)
-                for (int j = 1; j <= PF_DIST && j < n_tiles; ++j) {
-                    pf.next(s_ctx, Hkv, k);
-                    prefetch_boxes(pf, j);
-                }
-            if (it + PF_DIST + 1 < n_tiles) {
-                pf.next(s_ctx, Hkv, k);
-                prefetch_boxes(pf, it + PF_DIST + 1);
-            }
             __syncwarp();
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }

@@ -133,14 +133,6 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tma
         : "memory");
 }
 
-// Prefetch a tensor-map box into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t c0, int32_t c1,
-                                                int32_t c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 // Plain bulk copy global -> shared (16-byte aligned address and size).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
