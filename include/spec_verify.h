@@ -158,6 +158,34 @@ SPEC_API int spec_accept_greedy(const void *logits, int32_t logits_dtype, const 
                        int32_t batch, int32_t num_draft, int64_t vocab,
                        int32_t *accepted_len, int32_t *next_token, void *stream);
 
+/*
+ * Greedy acceptance that allocates nothing.  (The pages have no counterpart:
+ * this is an interface convenience of this library.)
+ *
+ * Same operation, arguments and results as spec_accept_greedy, for callers
+ * that cannot allocate device memory -- e.g. code recording the step into a
+ * CUDA graph (an allocation cannot be captured, and growing the library
+ * workspace synchronises the device) or a serving loop whose device memory is
+ * reserved up front by its own allocator.  Its scratch (reduction partials
+ * and completion tickets) is a fixed array of this library's device code,
+ * present on every GPU that loads the library until exit:
+ *   - limits: batch <= SPEC_NOALLOC_MAX_BATCH and
+ *     batch * (num_draft + 1) * ceil(vocab / 8192) <= SPEC_NOALLOC_MAX_PARTIALS
+ *     (512 KiB of partials); larger calls return SPEC_ERR_UNSUPPORTED and
+ *     enqueue nothing;
+ *   - the first call on a device looks up the array's device address (and may
+ *     load the library's device code): make it before any stream capture;
+ *   - every call shares the array and it keeps the last call's contents; the
+ *     call clears the tickets itself (an async memset on `stream`), but calls
+ *     that overlap on the GPU race: order them on one stream.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+enum { SPEC_NOALLOC_MAX_PARTIALS = 65536, SPEC_NOALLOC_MAX_BATCH = 4096 };
+SPEC_API int spec_accept_greedy_noalloc(const void *logits, int32_t logits_dtype,
+                                        const int32_t *draft_tokens, int32_t batch,
+                                        int32_t num_draft, int64_t vocab, int32_t *accepted_len,
+                                        int32_t *next_token, void *stream);
+
 /* Read and clear the device error word of the current device (synchronises
  * the device).  0 = no fault seen; otherwise a bitwise OR of SPEC_DEVERR_*. */
 SPEC_API int spec_device_error(int32_t *flags);

@@ -24,7 +24,9 @@ SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT = 1, 2, 4
 
 # every symbol the public header declares
 EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
-            "spec_accept_greedy", "spec_device_error", "spec_release"]
+            "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_device_error",
+            "spec_release"]
+SPEC_NOALLOC_MAX_PARTIALS, SPEC_NOALLOC_MAX_BATCH = 65536, 4096
 
 _TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
              torch.float16: SPEC_DTYPE_F16, torch.int8: SPEC_DTYPE_I8}
@@ -60,6 +62,8 @@ def _open(path: str):
     lib.spec_verify_attn.restype = ctypes.c_int
     lib.spec_accept_greedy.argtypes = [P, i32, P, i32, i32, i64, P, P, P]
     lib.spec_accept_greedy.restype = ctypes.c_int
+    lib.spec_accept_greedy_noalloc.argtypes = [P, i32, P, i32, i32, i64, P, P, P]
+    lib.spec_accept_greedy_noalloc.restype = ctypes.c_int
     lib.spec_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.spec_device_error.restype = ctypes.c_int
     lib.spec_release.restype = ctypes.c_int
@@ -126,6 +130,23 @@ def spec_accept_greedy(logits, draft_tokens, num_draft: int, accepted_len, next_
     _check(load().spec_accept_greedy(_ptr(logits), _TORCH_DT[logits.dtype], _ptr(draft_tokens), B,
                                      num_draft, V, _ptr(accepted_len), _ptr(next_token),
                                      _stream(stream)))
+
+
+def spec_accept_greedy_noalloc(logits, draft_tokens, num_draft: int, accepted_len, next_token,
+                               stream=None) -> None:
+    """spec_accept_greedy without any device allocation (fixed library scratch).
+
+    For callers that cannot allocate device memory, e.g. while recording a
+    CUDA graph.  Sizes are limited (see include/spec_verify.h); calls that
+    overlap on the GPU share the scratch and race.
+    """
+    B, k1, V = logits.shape
+    if k1 != num_draft + 1 or tuple(draft_tokens.shape) != (B, num_draft):
+        raise ValueError("logits must be [B, num_draft+1, V] and drafts [B, num_draft]")
+    _check(load().spec_accept_greedy_noalloc(_ptr(logits), _TORCH_DT[logits.dtype],
+                                             _ptr(draft_tokens), B, num_draft, V,
+                                             _ptr(accepted_len), _ptr(next_token),
+                                             _stream(stream)))
 
 
 def spec_device_error() -> int:

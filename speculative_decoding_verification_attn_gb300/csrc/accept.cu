@@ -11,6 +11,8 @@
 // match and resets the ticket, so no CTA ever waits on another.
 #include <limits.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace specv {
@@ -154,3 +156,103 @@ cudaError_t launch_accept(const AcceptArgs& a, void* workspace, int32_t* tickets
 }
 
 }  // namespace specv
+
+// ---------------------------------------------------------------- no-allocation variant
+//
+// Greedy acceptance for callers that cannot allocate device memory: code that
+// records the verification step into a CUDA graph (an allocation cannot be
+// captured, and growing the library workspace synchronises the device), and
+// serving loops whose device memory is reserved up front by their own
+// allocator, where an extra cudaMalloc may fail or stall the step.  The
+// reduction partials and completion tickets live in one fixed array of this
+// file; every call on a device shares it.
+
+namespace specv {
+namespace {
+
+// (row, vocabulary slice) partials and sequences the fixed scratch holds
+constexpr int64_t kNoAllocMaxPartials = SPEC_NOALLOC_MAX_PARTIALS;
+constexpr int kNoAllocMaxBatch = SPEC_NOALLOC_MAX_BATCH;
+constexpr size_t kNoAllocPartialBytes =
+    (size_t)kNoAllocMaxPartials * (sizeof(float) + sizeof(int));
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[256] = {};  // device address of the scratch, per device
+
+}  // namespace
+}  // namespace specv
+
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[specv::kNoAllocPartialBytes + specv::kNoAllocMaxBatch * sizeof(int32_t)];
+
+namespace specv {
+namespace {
+
+// Device address of the fixed scratch on the current device.  The first call
+// on a device looks it up with cudaGetSymbolAddress (which may load this
+// library's device code); later calls reuse the cached address.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(SPEC_ERR_CUDA, "cudaGetDevice failed");
+    if (dev < 0 || dev >= 256) return set_error(SPEC_ERR_UNSUPPORTED, "device index >= 256");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return set_error(SPEC_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace specv
+
+extern "C" int spec_accept_greedy_noalloc(const void* logits, int32_t logits_dtype,
+                                          const int32_t* draft_tokens, int32_t batch,
+                                          int32_t num_draft, int64_t vocab, int32_t* accepted_len,
+                                          int32_t* next_token, void* stream) {
+    using specv::set_error;
+    set_error(SPEC_OK, "");
+    if (batch < 0) return set_error(SPEC_ERR_INVALID, "batch < 0");
+    if (num_draft < 1 || num_draft > 64)
+        return set_error(SPEC_ERR_INVALID, "num_draft must be in [1, 64]");
+    if (vocab < 1 || vocab >= (1LL << 31))
+        return set_error(SPEC_ERR_INVALID, "vocab must be in [1, 2^31)");
+    if (logits_dtype != SPEC_DTYPE_F32 && logits_dtype != SPEC_DTYPE_BF16)
+        return set_error(SPEC_ERR_INVALID, "logits_dtype must be F32 or BF16");
+    if (batch == 0) return SPEC_OK;
+    if (!logits || !draft_tokens || !accepted_len || !next_token)
+        return set_error(SPEC_ERR_INVALID, "null tensor pointer");
+    if (reinterpret_cast<uintptr_t>(logits) & 15)
+        return set_error(SPEC_ERR_INVALID, "logits must be 16-byte aligned");
+    const int64_t parts = (int64_t)batch * (num_draft + 1) * specv::num_slices(vocab);
+    if (batch > specv::kNoAllocMaxBatch || parts > specv::kNoAllocMaxPartials)
+        return set_error(SPEC_ERR_UNSUPPORTED,
+                         "too large for the fixed no-allocation scratch: needs batch <= "
+                         "SPEC_NOALLOC_MAX_BATCH and batch * (num_draft + 1) * ceil(vocab / 8192) "
+                         "<= SPEC_NOALLOC_MAX_PARTIALS");
+    void* scratch = nullptr;
+    const int rc = specv::noalloc_scratch(&scratch);
+    if (rc) return rc;
+    specv::AcceptArgs a;
+    a.logits = logits;
+    a.dtype = logits_dtype;
+    a.draft = draft_tokens;
+    a.B = batch;
+    a.k = num_draft;
+    a.V = vocab;
+    a.accepted_len = accepted_len;
+    a.next_token = next_token;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) +
+                                                  specv::kNoAllocPartialBytes);
+    // the tickets must start at zero; the array keeps whatever the last call left
+    cudaError_t e = cudaMemsetAsync(tickets, 0, sizeof(int32_t) * (size_t)batch, st);
+    if (e == cudaSuccess) e = specv::launch_accept(a, scratch, tickets, st);
+    if (e != cudaSuccess) return set_error(SPEC_ERR_CUDA, cudaGetErrorString(e));
+    return SPEC_OK;
+}

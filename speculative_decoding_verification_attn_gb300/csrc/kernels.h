@@ -58,4 +58,7 @@ size_t accept_workspace_bytes(const AcceptArgs& a);
 cudaError_t launch_accept(const AcceptArgs& a, void* workspace, int32_t* tickets,
                           cudaStream_t stream);
 
+// Sets the thread-local error message of the C ABI; returns `code`.
+int set_error(int code, const char* msg);
+
 }  // namespace specv

@@ -119,6 +119,12 @@ int validate_tables(const specv::AttnArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+namespace specv {
+// Records `msg` as this thread's last error and returns `code` (for entry
+// points defined in other translation units).
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace specv
+
 extern "C" {
 
 int spec_version(void) { return 100; }
