@@ -69,7 +69,8 @@ enum {
 
 /* Options for spec_set_option (process-wide; default 0 = automatic). */
 enum {
-    /* 0 auto, 1 SIMT (CUDA cores) kernel, 2 tensor-core (tcgen05) kernel */
+    /* 0 auto, 1 SIMT (CUDA cores) kernel, 2 tcgen05 kernel, 3 warp-MMA
+     * (mma.sync) kernel for <= 16 query rows per kv-head */
     SPEC_OPT_ATTN_PATH = 0,
     /* persistent CTAs of the tensor-core kernel; 0 = number of SMs */
     SPEC_OPT_NUM_CTAS = 1,
@@ -118,10 +119,11 @@ SPEC_API int spec_set_option(int32_t option, int64_t value);
  *
  * Limits: 1 <= num_draft <= 64; num_q_heads % num_kv_heads == 0;
  * head_dim % 32 == 0 and head_dim <= 256; page_size >= 1; q, caches and out
- * 16-byte aligned.  A bf16 query over a bf16 or I8 cache with head_dim 128,
- * num_draft * (num_q_heads / num_kv_heads) <= 128, a power-of-two
- * page_size in [8, 256] and batch <= 2048 runs on the tensor-core kernel;
- * every other accepted shape runs on the SIMT kernel.
+ * 16-byte aligned.  A bf16 query over a bf16 cache with head_dim 128, a
+ * power-of-two page_size in [16, 256] and batch <= 1024 runs on a
+ * tensor-core kernel: the warp-MMA kernel when num_draft * (num_q_heads /
+ * num_kv_heads) <= 16, the tcgen05 kernel up to 128; every other accepted
+ * shape runs on the SIMT kernel.
  */
 SPEC_API int spec_verify_attn(const void *q, const void *k_cache, const void *v_cache,
                      const void *k_scale, const void *v_scale,

@@ -1,0 +1,592 @@
+// Verification attention for small query-row sets: k * G <= 16 rows per
+// (sequence, kv-head), bf16 queries over a bf16 paged KV cache, head_dim 128.
+//
+// What it computes: multi-query causal attention of each sequence's k draft
+// queries over its paged cache ("Decoding Speculative Decoding from First
+// Principles", "Parallelizing method 2: sequence parallel" and "Speculating
+// to get sequence parallelism during decode"): query i of sequence b sees
+// keys 0 .. ctx_b + i; kv-head g serves q-heads g*G .. g*G+G-1.
+//
+// Design: the R <= 16 query rows of a (sequence, kv-head) form exactly one
+// 16-row tile of the warp-level tensor-core MMA (m16n8k16, bf16 in, fp32
+// accumulate), so every K/V byte is read from HBM once and used for all rows.
+// Unlike a 128-row tcgen05 tile (mostly padding at 8-16 rows), the softmax
+// lives in registers: no TMEM round trips and no per-tile hand-off between
+// warps, which keeps each K/V stage busy only for its load latency plus a few
+// hundred cycles -- the pipeline depth the load latency needs.
+//
+//  * Work: the same stream-K tile list as the tcgen05 kernel (64-key tiles of
+//    every (sequence, kv-head) segment over a persistent grid); segments cut
+//    by a CTA-range boundary leave (O/l, lse) partials merged by the same
+//    combine kernel.
+//  * Warps: 0-3 compute, warp w owns keys [16w, 16w+16) of every tile (one TMA
+//    page box); warp 4 is the TMA producer (16-key 3-D page boxes of 4 KB,
+//    128-byte swizzle, block-table entries prefetched with cp.async).
+//  * Per warp and tile: S = Q K^T (16 MMAs, K via ldmatrix), masked online
+//    softmax in registers with a lazily moved reference max, P V (16 MMAs,
+//    V via ldmatrix.trans, P straight from the S accumulators).  The four
+//    warps' (max, sum, O) are merged once per segment through shared memory.
+//  * Every mbarrier wait is bounded (1 s); a timeout sets the device error
+//    word and an abort flag after which every role skips its remaining work,
+//    still passing every CTA barrier.
+#include <cuda.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace specv {
+namespace {
+
+constexpr int D = 128;
+constexpr int TN = 64;               // keys per tile
+constexpr int NW = 4;                // compute warps (16 keys each)
+constexpr int NS = 6;                // K/V stages
+constexpr int BOX_ROWS = 16;         // keys per TMA box
+constexpr int BOX_BYTES = BOX_ROWS * D * 2;  // 4 KB
+constexpr int KV_BYTES = TN * D * 2;         // 16 KB per tensor per stage
+constexpr int STAGE_BYTES = 2 * KV_BYTES;
+constexpr int QROWS = 16;
+constexpr int Q_HALF = QROWS * 128;  // 2 KB: 64 head-dim columns of 16 rows
+constexpr int LOOKAHEAD = 6;
+constexpr int MAX_BOX = TN / BOX_ROWS;
+constexpr int THREADS = (NW + 1) * 32;
+constexpr int MAX_BATCH = 1024;
+constexpr int OSTRIDE = D + 4;       // merge scratch row stride (floats)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+using Cursor = CursorT<TN>;
+
+struct Smem {
+    static constexpr int STAGES = 0;
+    static constexpr int Q = STAGES + NS * STAGE_BYTES;       // 2 halves x 2 KB
+    static constexpr int SCRATCH = Q + 2 * Q_HALF;            // [16][OSTRIDE] float
+    static constexpr int BARS = SCRATCH + QROWS * OSTRIDE * 4;
+    static constexpr int B_KVFULL = 0, B_KVEMPTY = NS, B_QFULL = 2 * NS, B_QFREE = 2 * NS + 1,
+                         NUM_BARS = 2 * NS + 2;
+    static constexpr int MISC = BARS + NUM_BARS * 8;          // abort flag
+    static constexpr int STAT = MISC + 16;                     // [NW][16] (m, l)
+    static constexpr int PIDS = STAT + 2 * NW * QROWS * 4;
+    static constexpr int CTX = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;
+    static constexpr int PRE = CTX + MAX_BATCH * 4;
+    static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
+};
+constexpr size_t SMEM_BYTES = Smem::END + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+struct MmaParams {
+    AttnArgs a;
+    float* part_o;    // [2*C][128][D]
+    float* part_lse;  // [2*C][128]
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of (row, 16-byte chunk c of the 256-byte row) in a block laid
+// out as [2 halves][rows][128 B] with the 128-byte swizzle (chunk ^ row%8).
+__device__ __forceinline__ uint32_t sw_off(int row, int c, int half_bytes) {
+    return (c >> 3) * half_bytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap, const MmaParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const AttnArgs& a = prm.a;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC);
+    int* pid_ring = reinterpret_cast<int*>(sm + Smem::PIDS);
+    int* s_ctx = reinterpret_cast<int*>(sm + Smem::CTX);
+    int* s_pre = reinterpret_cast<int*>(sm + Smem::PRE);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.B, k = a.k, Hkv = a.Hkv, G = a.Hq / a.Hkv, R = k * G, P = a.P;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars[Smem::B_KVFULL + s], 1);
+            mbar_init(&bars[Smem::B_KVEMPTY + s], NW);
+        }
+        mbar_init(&bars[Smem::B_QFULL], 1);
+        mbar_init(&bars[Smem::B_QFREE], NW);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    {
+        // Q rows R..15 stay zero (the TMA writes rows 0..R-1 only)
+        uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
+        for (int e = tid; e < 2 * Q_HALF / 16; e += THREADS) q4[e] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == NW) {
+        const int per = (B + 31) / 32, lo = lane * per, hi = min(B, lo + per);
+        int sum = 0;
+        for (int b = lo; b < hi; ++b) {
+            int c = a.ctx_lens[b];
+            const int64_t cap = (int64_t)a.max_pages * P - k;
+            if (c < 0 || (int64_t)c > cap) {
+                raise_device_error(a.dev_err, SPEC_DEVERR_CTX);
+                c = c < 0 ? 0 : (int)(cap < 0 ? 0 : cap);
+            }
+            s_ctx[b] = c;
+            sum += (c + k + TN - 1) / TN;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int b = lo; b < hi; ++b) {
+            s_pre[b] = run;
+            run += (s_ctx[b] + k + TN - 1) / TN;
+        }
+        if (lane == 31) s_pre[B] = incl;
+    }
+    __syncthreads();
+
+    const int64_t T = (int64_t)s_pre[B] * Hkv;
+    const int64_t C = gridDim.x;
+    const int64_t t_begin = (int64_t)blockIdx.x * T / C;
+    const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
+    const int n_tiles = (int)(t_end - t_begin);
+
+    if (warp == NW) {
+        // ================= TMA producer =================
+        Cursor cur, ahead;
+        if (n_tiles > 0) {
+            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            ahead = cur;
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        if (lane == 0) {
+            prefetch_tmap(&qmap);
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
+        auto fetch_pids = [&](int slot, const Cursor& c) {
+            const int key0 = c.lt * TN;
+            const int nvalid = min(TN, s_ctx[c.b] + k - key0);
+            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
+            if (lane < nbox) {
+                const int lp = (key0 + lane * BOX_ROWS) / P;
+                cp_async_4(&pid_ring[slot * MAX_BOX + lane],
+                           &a.block_table[(int64_t)c.b * a.max_pages + lp]);
+            }
+        };
+        for (int la = 0; la < LOOKAHEAD; ++la) {
+            if (la < n_tiles) {
+                fetch_pids(la % (LOOKAHEAD + 1), ahead);
+                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+        }
+        int pc = -1, n_issued = 0, issued_q = 0;
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            if (it + LOOKAHEAD < n_tiles) {
+                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
+                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+            cp_async_wait<LOOKAHEAD>();  // entries of tile `it`
+            __syncwarp();
+            if (it == 0 || cur.lt == 0) {
+                // Q of the next piece once the compute warps hold the previous one
+                ++pc;
+                if (lane == 0) {
+                    if (pc >= 1)
+                        ok = mbar_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag, a.dev_err);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL], 2 * R * 128);
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(sm + Smem::Q + h * Q_HALF, &qmap, &bars[Smem::B_QFULL],
+                                        h * 64, cur.kvh * G, cur.b * k);
+                        issued_q = pc + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            const int s = it % NS, use = it / NS;
+            const int key0 = cur.lt * TN;
+            const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
+            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
+            if (lane == 0) {
+                if (use >= 1)
+                    ok = mbar_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag,
+                                   a.dev_err);
+                if (ok) mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s], 2u * nbox * BOX_BYTES);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane < 2 * nbox) {
+                const int tensor = lane & 1, bx = lane >> 1;
+                int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
+                if (page < 0 || page >= a.num_pages) {
+                    raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                    page = 0;
+                }
+                const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BOX_ROWS) % P;
+                tma_load_3d_hint(sm + Smem::STAGES + s * STAGE_BYTES + tensor * KV_BYTES +
+                                     bx * BOX_BYTES,
+                                 tensor ? (const void*)&vmap : (const void*)&kmap,
+                                 &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
+            }
+            n_issued = it + 1;
+            __syncwarp();
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+        cp_async_wait<0>();
+        if (!ok && lane == 0) {
+            for (int s = 0; s < NS; ++s) {
+                const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
+                if (uses > 0) mbar_drain(&bars[Smem::B_KVFULL + s], (uses - 1) & 1);
+            }
+            if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
+        }
+    } else {
+        // ================= compute warps: keys [16w, 16w+16) of every tile =================
+        const int g = lane >> 2, t4 = lane & 3;  // MMA fragment group / thread in group
+        const float sl2 = a.scale * kLog2e;
+        const uint32_t q_base = smem_u32(sm + Smem::Q);
+        float* s_m = reinterpret_cast<float*>(sm + Smem::STAT);
+        float* s_l = s_m + NW * QROWS;
+        float* scratch = reinterpret_cast<float*>(sm + Smem::SCRATCH);
+        // the two rows this thread holds in every fragment: g and g + 8
+        int irow[2];
+        irow[0] = g < R ? g / G : k - 1;
+        irow[1] = g + 8 < R ? (g + 8) / G : k - 1;
+
+        uint32_t qf[D / 16][4];
+        float o[D / 8][4];
+        float m_ref[2], lsum[2];
+        Cursor cur;
+        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+        bool ok = true;
+        int pc = -1;
+        for (int it = 0; it < n_tiles; ++it) {
+            const bool first = (it == 0) || (cur.lt == 0);
+            const bool last = (it == n_tiles - 1) || (cur.lt == cur.nb - 1);
+            const int s = it % NS;
+            const int ctx = s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
+            const int nvalid = min(TN, L - key0);
+            if (first) {
+                ++pc;
+                if (ok) ok = warp_wait(&bars[Smem::B_QFULL], pc & 1, abort_flag, a.dev_err);
+                if (ok) {
+                    // Q fragments: 16 rows x 16 columns per k-slice, from the
+                    // 128-byte-swizzled staging buffer
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const int chunk = kk * 2 + (lane >> 4);
+                        ldsm_x4(q_base + sw_off(row, chunk, Q_HALF), qf[kk][0], qf[kk][1],
+                                qf[kk][2], qf[kk][3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[Smem::B_QFREE]);
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+                m_ref[0] = m_ref[1] = -INFINITY;
+                lsum[0] = lsum[1] = 0.f;
+            }
+            if (ok) ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
+            const int kv0 = warp * BOX_ROWS;  // this warp's first key in the tile
+            if (ok && kv0 < nvalid) {
+                const uint32_t kb = smem_u32(sm + Smem::STAGES + s * STAGE_BYTES) + warp * BOX_BYTES;
+                const uint32_t vb = kb + KV_BYTES;
+                if (nvalid - kv0 < BOX_ROWS) {
+                    // keys past the sequence end in this box: zero their V rows
+                    // so that 0 * (stale or canary) never reaches O
+                    uint8_t* vrow = sm + Smem::STAGES + s * STAGE_BYTES + KV_BYTES + warp * BOX_BYTES;
+                    for (int e = (nvalid - kv0) * 16 + lane; e < BOX_ROWS * 16; e += 32) {
+                        const int r = e >> 4, c = e & 15;
+                        *reinterpret_cast<uint4*>(vrow + sw_off(r, c, BOX_BYTES / 2)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();  // before the next TMA write of this stage
+                    __syncwarp();
+                }
+                // S = Q K^T over this warp's 16 keys: n-tile 0 = keys 0-7, 1 = keys 8-15
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t b00, b01, b10, b11;
+                    const int key = (lane & 7) + (lane >> 4) * 8;
+                    const int chunk = kk * 2 + ((lane >> 3) & 1);
+                    ldsm_x4(kb + sw_off(key, chunk, BOX_BYTES / 2), b00, b01, b10, b11);
+                    mma16816(sc[0], qf[kk], b00, b01);
+                    mma16816(sc[1], qf[kk], b10, b11);
+                }
+                // masked scores (log2 units); -inf where the key is invisible
+                float v[2][4];
+                float mt[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int hr = e >> 1;  // 0: row g, 1: row g + 8
+                        const int kr = kv0 + nt * 8 + t4 * 2 + (e & 1);
+                        const bool vis = kr < nvalid && key0 + kr <= ctx + irow[hr];
+                        v[nt][e] = vis ? sc[nt][e] * sl2 : -INFINITY;
+                        mt[hr] = fmaxf(mt[hr], v[nt][e]);
+                    }
+                float alpha[2];
+                bool moved = false;
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    mt[hr] = fmaxf(mt[hr], __shfl_xor_sync(0xffffffffu, mt[hr], 1));
+                    mt[hr] = fmaxf(mt[hr], __shfl_xor_sync(0xffffffffu, mt[hr], 2));
+                    const float m_new = fmaxf(m_ref[hr], mt[hr]);
+                    alpha[hr] = 1.f;
+                    if (m_new > m_ref[hr] + kRescaleThreshold) {
+                        alpha[hr] = m_ref[hr] == -INFINITY ? 0.f : fast_exp2(m_ref[hr] - m_new);
+                        m_ref[hr] = m_new;
+                        lsum[hr] *= alpha[hr];
+                        moved = true;
+                    }
+                }
+                if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+                    for (int j = 0; j < D / 8; ++j) {
+                        o[j][0] *= alpha[0];
+                        o[j][1] *= alpha[0];
+                        o[j][2] *= alpha[1];
+                        o[j][3] *= alpha[1];
+                    }
+                }
+                const float mu0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
+                const float mu1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
+                float p[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    p[nt][0] = fast_exp2(v[nt][0] - mu0);
+                    p[nt][1] = fast_exp2(v[nt][1] - mu0);
+                    p[nt][2] = fast_exp2(v[nt][2] - mu1);
+                    p[nt][3] = fast_exp2(v[nt][3] - mu1);
+                    lsum[0] += p[nt][0] + p[nt][1];
+                    lsum[1] += p[nt][2] + p[nt][3];
+                }
+                // P as the A operand of P V: the two 8-key accumulator tiles
+                // are exactly the two 8-column halves of a 16x16 A fragment
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+                pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+                pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+                pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+                // O += P V: 16 output n-tiles of 8 head-dim columns
+#pragma unroll
+                for (int j = 0; j < D / 8; j += 2) {
+                    uint32_t b00, b01, b10, b11;
+                    const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int chunk = j + (lane >> 4);
+                    ldsm_x4_t(vb + sw_off(key, chunk, BOX_BYTES / 2), b00, b01, b10, b11);
+                    mma16816(o[j], pa, b00, b01);
+                    mma16816(o[j + 1], pa, b10, b11);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Smem::B_KVEMPTY + s]);
+
+            if (last) {
+                // ---- merge the four warps' (max, sum, O) of this segment piece
+                float lrow[2];
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    lrow[hr] = lsum[hr];
+                    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
+                    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
+                }
+                if (t4 == 0) {
+                    s_m[warp * QROWS + g] = m_ref[0];
+                    s_m[warp * QROWS + g + 8] = m_ref[1];
+                    s_l[warp * QROWS + g] = lrow[0];
+                    s_l[warp * QROWS + g + 8] = lrow[1];
+                }
+                named_bar_sync(1, NW * 32);
+                float wgt[2], lse[2];
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int row = g + 8 * hr;
+                    float mt = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) mt = fmaxf(mt, s_m[w * QROWS + row]);
+                    float Ls = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) {
+                        const float mw = s_m[w * QROWS + row];
+                        if (mw != -INFINITY) Ls += s_l[w * QROWS + row] * fast_exp2(mw - mt);
+                    }
+                    wgt[hr] = (Ls > 0.f && m_ref[hr] != -INFINITY) ? fast_exp2(m_ref[hr] - mt) / Ls
+                                                                   : 0.f;
+                    lse[hr] = Ls > 0.f ? (mt + log2f(Ls)) * kLn2 : -INFINITY;
+                }
+#pragma unroll 1
+                for (int w = 0; w < NW; ++w) {
+                    if (warp == w) {
+#pragma unroll
+                        for (int j = 0; j < D / 8; ++j) {
+                            float2* r0 = reinterpret_cast<float2*>(scratch + g * OSTRIDE + j * 8 + t4 * 2);
+                            float2* r1 =
+                                reinterpret_cast<float2*>(scratch + (g + 8) * OSTRIDE + j * 8 + t4 * 2);
+                            float2 x0 = make_float2(o[j][0] * wgt[0], o[j][1] * wgt[0]);
+                            float2 x1 = make_float2(o[j][2] * wgt[1], o[j][3] * wgt[1]);
+                            if (w > 0) {
+                                const float2 p0 = *r0, p1 = *r1;
+                                x0.x += p0.x;
+                                x0.y += p0.y;
+                                x1.x += p1.x;
+                                x1.y += p1.y;
+                            }
+                            *r0 = x0;
+                            *r1 = x1;
+                        }
+                    }
+                    named_bar_sync(1, NW * 32);
+                }
+                const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
+                const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
+                if (ok) {
+                    // 16 rows x 16 chunks of 8 columns over the 128 compute threads
+                    for (int idx = tid; idx < R * (D / 8); idx += NW * 32) {
+                        const int rr = idx / (D / 8), c8 = idx % (D / 8);
+                        const float* src = scratch + rr * OSTRIDE + c8 * 8;
+                        const int64_t orow =
+                            ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+                        if (complete) {
+                            uint4 w4;
+                            w4.x = pack_bf16x2(src[0], src[1]);
+                            w4.y = pack_bf16x2(src[2], src[3]);
+                            w4.z = pack_bf16x2(src[4], src[5]);
+                            w4.w = pack_bf16x2(src[6], src[7]);
+                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
+                                                      c8 * 8) = w4;
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(
+                                prm.part_o + ((int64_t)slot * 128 + rr) * D + c8 * 8);
+                            dst[0] = make_float4(src[0], src[1], src[2], src[3]);
+                            dst[1] = make_float4(src[4], src[5], src[6], src[7]);
+                        }
+                    }
+                    if (warp == 0 && t4 == 0) {
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int rr = g + 8 * hr;
+                            if (rr >= R) continue;
+                            const int64_t orow =
+                                ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+                            if (complete) {
+                                if (a.lse) a.lse[orow] = lse[hr];
+                            } else {
+                                prm.part_lse[(int64_t)slot * 128 + rr] = lse[hr];
+                            }
+                        }
+                    }
+                }
+                named_bar_sync(1, NW * 32);  // scratch reused by the next piece
+            }
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+    }
+    __syncthreads();
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+bool mma_supported(const AttnArgs& a) {
+    const int G = a.Hq / a.Hkv;
+    const bool pow2 = (a.P & (a.P - 1)) == 0;
+    return a.q_dtype == SPEC_DTYPE_BF16 && a.kv_dtype == SPEC_DTYPE_BF16 && a.D == D &&
+           a.k * G <= QROWS && pow2 && a.P >= 16 && a.P <= 256 && a.B <= MAX_BATCH &&
+           (int64_t)a.num_pages * a.Hkv * a.P < (1LL << 31) && (int64_t)a.B * a.k < (1LL << 31);
+}
+
+cudaError_t launch_attn_mma(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream) {
+    if (a.B == 0) return cudaSuccess;
+    EncodeTiledFn encode = get_encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const int G = a.Hq / a.Hkv;
+    CUtensorMap qmap, kmap, vmap;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.k};
+        cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)a.k};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
+    for (int t = 0; t < 2; ++t) {
+        cuuint64_t dims[3] = {64, rows, 2};
+        cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)BOX_ROWS, 2};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    MmaParams prm;
+    prm.a = a;
+    prm.part_o = static_cast<float*>(workspace);
+    prm.part_lse = prm.part_o + (size_t)2 * num_ctas * 128 * D;
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attn_mma_kernel<<<num_ctas, THREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, stream);
+}
+
+}  // namespace specv

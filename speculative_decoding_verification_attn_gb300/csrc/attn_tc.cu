@@ -66,6 +66,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 constexpr uint32_t IDESC_PV = umma_idesc_bf16(ROWS, D, 0, 1);   // B (V) MN-major
+using Cursor = CursorT<TN>;
 
 struct Smem {
     // offsets from the 1024-aligned base
@@ -102,67 +103,6 @@ __host__ __device__ constexpr int num_copies(int R) {
 // Row `row` of the 128-row Q tile holds real query data.
 __device__ __forceinline__ bool q_row_used(int row, int R, int RQ, int REP) {
     return row / RQ < REP && row % RQ < R;
-}
-
-// Walks a CTA's tile range: tile -> (sequence b, kv-head, tile-in-segment).
-struct Cursor {
-    int b, kvh, lt, nb;
-    int64_t seg_start;  // global index of the segment's first tile
-    __device__ void init(int64_t t, const int* pre, const int* ctx, int B, int Hkv, int k) {
-        int lo = 0, hi = B - 1;  // largest b with pre[b]*Hkv <= t
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)pre[mid] * Hkv <= t) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-        nb = (ctx[b] + k + TN - 1) / TN;
-        const int64_t off = t - (int64_t)pre[b] * Hkv;
-        kvh = (int)(off / nb);
-        lt = (int)(off % nb);
-        seg_start = (int64_t)pre[b] * Hkv + (int64_t)kvh * nb;
-    }
-    __device__ void next(const int* ctx, int Hkv, int k) {
-        if (++lt == nb) {
-            lt = 0;
-            seg_start += nb;
-            if (++kvh == Hkv) {
-                kvh = 0;
-                ++b;
-                nb = (ctx[b] + k + TN - 1) / TN;
-            }
-        }
-    }
-};
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Warp-uniform bounded wait: lane 0 polls, the whole warp gets its verdict.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* dev_err) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, dev_err);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
-// Bounded wait used only while draining after an abort (ignores the flag).
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
 }
 
 // What every role of a CTA shares.
@@ -1014,9 +954,14 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
     attn_tc_kernel<<<num_ctas, THREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int R = a.k * G;
+    return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, stream);
+}
+
+cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float* part_o,
+                                    const float* part_lse, cudaStream_t stream) {
+    const int R = a.k * (a.Hq / a.Hkv);
     dim3 cgrid(a.B * a.Hkv, (R + 7) / 8);
-    combine_tc_kernel<<<cgrid, 256, 0, stream>>>(a, num_ctas, prm.part_o, prm.part_lse);
+    combine_tc_kernel<<<cgrid, 256, 0, stream>>>(a, num_ctas, part_o, part_lse);
     return cudaGetLastError();
 }
 

@@ -315,6 +315,74 @@ __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t start, uint32_t lb
     return d;
 }
 
+// ------------------------------------------------------------------ persistent tile walk
+
+// Verification work is the list of TILE_KEYS-key tiles of every (sequence,
+// kv-head) segment, sequences in order, kv-heads inside a sequence.  pre[b]
+// = tiles of sequences 0..b-1 (per kv-head), ctx[b] = clamped context.
+// Walks a CTA's tile range: tile -> (sequence b, kv-head, tile-in-segment).
+template <int TILE_KEYS>
+struct CursorT {
+    int b, kvh, lt, nb;
+    int64_t seg_start;  // global index of the segment's first tile
+    __device__ void init(int64_t t, const int* pre, const int* ctx, int B, int Hkv, int k) {
+        int lo = 0, hi = B - 1;  // largest b with pre[b]*Hkv <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)pre[mid] * Hkv <= t) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        nb = (ctx[b] + k + TILE_KEYS - 1) / TILE_KEYS;
+        const int64_t off = t - (int64_t)pre[b] * Hkv;
+        kvh = (int)(off / nb);
+        lt = (int)(off % nb);
+        seg_start = (int64_t)pre[b] * Hkv + (int64_t)kvh * nb;
+    }
+    __device__ void next(const int* ctx, int Hkv, int k) {
+        if (++lt == nb) {
+            lt = 0;
+            seg_start += nb;
+            if (++kvh == Hkv) {
+                kvh = 0;
+                ++b;
+                nb = (ctx[b] + k + TILE_KEYS - 1) / TILE_KEYS;
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the whole warp gets its verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* dev_err) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, dev_err);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Bounded wait used only while draining after an abort (ignores the flag).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+}
+
+
 // ------------------------------------------------------------------ reductions
 
 __device__ __forceinline__ float warp_max(float v) {

@@ -134,7 +134,7 @@ const char* spec_last_error(void) { return g_err.c_str(); }
 int spec_set_option(int32_t option, int64_t value) {
     switch (option) {
     case SPEC_OPT_ATTN_PATH:
-        if (value < 0 || value > 2) return fail(SPEC_ERR_INVALID, "attn path must be 0, 1 or 2");
+        if (value < 0 || value > 3) return fail(SPEC_ERR_INVALID, "attn path must be 0, 1, 2 or 3");
         g_opt_path = value;
         return SPEC_OK;
     case SPEC_OPT_NUM_CTAS:
@@ -197,16 +197,19 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
     a.out = out; a.lse = lse;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    // kernels: 1 SIMT, 2 tcgen05, 3 warp MMA; automatic = warp MMA for <= 16
+    // query rows per kv-head, tcgen05 above, SIMT for everything else
     const int64_t path = g_opt_path.load();
-    const bool tc_ok = specv::tc_supported(a);
-    bool use_tc;
-    if (path == 1) use_tc = false;
-    else if (path == 2) {
-        if (!tc_ok)
-            return fail(SPEC_ERR_UNSUPPORTED, "tensor-core path forced but this shape/dtype is "
-                        "not supported by it");
-        use_tc = true;
-    } else use_tc = tc_ok;
+    const bool tc_ok = specv::tc_supported(a), mma_ok = specv::mma_supported(a);
+    int kernel;
+    if (path == 1) kernel = 1;
+    else if (path == 2 || path == 3) {
+        if ((path == 2 && !tc_ok) || (path == 3 && !mma_ok))
+            return fail(SPEC_ERR_UNSUPPORTED, "forced attention kernel %d does not support this "
+                        "shape/dtype", (int)path);
+        kernel = (int)path;
+    } else kernel = mma_ok ? 3 : tc_ok ? 2 : 1;
+    const bool use_tc = kernel != 1;
 
     Workspace* ws = nullptr;
     int rc = get_workspace(0, &ws);
@@ -222,7 +225,8 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
         rc = get_workspace(specv::tc_workspace_bytes(a, ctas), &ws);
         if (rc) return rc;
         a.dev_err = static_cast<int*>(ws->base);
-        e = specv::launch_attn_tc(a, ctas, static_cast<char*>(ws->base) + kHeader, st);
+        e = kernel == 3 ? specv::launch_attn_mma(a, ctas, static_cast<char*>(ws->base) + kHeader, st)
+                        : specv::launch_attn_tc(a, ctas, static_cast<char*>(ws->base) + kHeader, st);
         if (e != cudaSuccess) return cuda_fail(e, "verify_attn (tensor-core) launch");
     } else {
         const specv::SimtPlan p = specv::simt_plan(a, ws->sms, (int)g_opt_simt_chunk.load());

@@ -163,3 +163,35 @@ def test_misaligned_pointer_rejected():
     with pytest.raises(binding.SpecError, match="aligned"):
         binding.spec_verify_attn(q_bad, t["k_cache"], t["v_cache"], t["block_table"],
                                  t["ctx_lens"], inp.spec.num_draft, inp.scale, o["out"], o["lse"])
+
+
+MMA_CASES = [k for k in SMALL_BF16
+             if k.get("num_draft", 4) * (k.get("num_q_heads", 8) // k.get("num_kv_heads", 2)) <= 16]
+
+
+@pytest.mark.parametrize("kw", MMA_CASES, ids=[str(i) for i in range(len(MMA_CASES))])
+def test_warp_mma_small(oracle_mod, kw):
+    inp = make_inputs(small_spec(**kw), seed=31)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 3)
+    check_attn_full(oracle_mod, inp, "mma %s" % kw)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 37, 152, 400])
+def test_warp_mma_stream_k_splits(oracle_mod, ctas):
+    inp = make_inputs(small_spec(batch=5, num_q_heads=16, num_kv_heads=4, num_draft=4,
+                                 ctx=(0, 900)), seed=32)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 3)
+    binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
+    check_attn_full(oracle_mod, inp, "mma ctas=%d" % ctas)
+
+
+def test_warp_mma_matches_tcgen05():
+    inp = make_inputs(small_spec(batch=6, num_q_heads=12, num_kv_heads=3, num_draft=4,
+                                 ctx=(0, 700)), seed=33)
+    t = binding.inputs_to_torch(inp)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 3)
+    a_out, a_lse = gpu_attn(inp, t)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    b_out, b_lse = gpu_attn(inp, t)
+    assert np.abs(a_out - b_out).max() < 2e-2
+    assert np.abs(a_lse - b_lse).max() < 2e-3
