@@ -97,7 +97,8 @@ def test_accept_rejects_bad_arguments(lib, bad, needle):
 
 
 def test_options(lib):
-    assert lib.spec_set_option(0, 3) == -1
+    assert lib.spec_set_option(0, 4) == -1
+    assert lib.spec_set_option(0, 3) == 0
     assert lib.spec_set_option(99, 0) == -1
     assert lib.spec_set_option(0, 0) == 0
     assert lib.spec_set_option(1, 0) == 0
