@@ -350,8 +350,15 @@ def run_gpu(args, inp, world, rank, local):
 
 
 def launches_per_step(inp) -> int:
-    # attention kernel + split-KV combine kernel + acceptance kernel
-    return 3
+    """Kernels one step launches: the warp-MMA attention kernel (bf16, head_dim
+    128, <= 16 query rows per kv-head, page size 16..256) merges its split-KV
+    partials itself; the tcgen05 and SIMT kernels are followed by a combine
+    kernel; plus the acceptance kernel."""
+    s = inp.spec
+    rows = s.num_draft * (s.num_q_heads // s.num_kv_heads)
+    warp_mma = (s.q_dtype == "bf16" and s.kv_dtype == "bf16" and s.head_dim == 128 and rows <= 16
+                and 16 <= s.page_size <= 256 and s.page_size & (s.page_size - 1) == 0)
+    return (1 if warp_mma else 2) + 1
 
 
 def main(argv=None):

@@ -16,9 +16,10 @@
 // hundred cycles -- the pipeline depth the load latency needs.
 //
 //  * Work: the same stream-K tile list as the tcgen05 kernel (64-key tiles of
-//    every (sequence, kv-head) segment over a persistent grid); segments cut
-//    by a CTA-range boundary leave (O/l, lse) partials merged by the same
-//    combine kernel.
+//    every (sequence, kv-head) segment over a persistent grid); a segment cut
+//    by a CTA-range boundary leaves (O/l, lse) partials, and the last of its
+//    pieces to finish merges them (atomic arrival count per segment, no
+//    waiting), so one launch does the whole call.
 //  * Warps: 0-3 compute, warp w owns keys [16w, 16w+16) of every tile (one TMA
 //    page box); warp 4 is the TMA producer (16-key 3-D page boxes of 4 KB,
 //    128-byte swizzle, block-table entries prefetched with cp.async).
@@ -118,6 +119,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const AttnArgs& a = prm.a;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC);
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC + 4);
     int* pid_ring = reinterpret_cast<int*>(sm + Smem::PIDS);
     int* s_ctx = reinterpret_cast<int*>(sm + Smem::CTX);
     int* s_pre = reinterpret_cast<int*>(sm + Smem::PRE);
@@ -509,6 +511,64 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         }
                     }
                 }
+                if (!complete) {
+                    // fused split-KV merge: the last piece of a segment to arrive
+                    // merges all its pieces' partials (no CTA ever waits)
+                    __threadfence();
+                    named_bar_sync(1, NW * 32);
+                    const int64_t s0 = cur.seg_start, s1 = s0 + cur.nb;
+                    auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
+                    auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
+                    const int c_first = cta_of(s0), c_last = cta_of(s1 - 1);
+                    const int seg = cur.b * Hkv + cur.kvh;
+                    if (tid == 0) {
+                        int npieces = 0;
+                        for (int c = c_first; c <= c_last; ++c) npieces += empty(c) ? 0 : 1;
+                        const int old = atomicAdd(&a.seg_counters[seg], 1);
+                        *merge_flag = (old == npieces - 1);
+                    }
+                    named_bar_sync(1, NW * 32);
+                    if (*merge_flag) {
+                        __threadfence();
+                        for (int idx = tid; idx < R * (D / 8); idx += NW * 32) {
+                            const int rr = idx / (D / 8), c8 = idx % (D / 8);
+                            float mx = -INFINITY;
+                            for (int c = c_first; c <= c_last; ++c) {
+                                if (empty(c)) continue;
+                                const int sl = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
+                                mx = fmaxf(mx, __ldcg(prm.part_lse + (int64_t)sl * 128 + rr));
+                            }
+                            float tot = 0.f;
+                            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            for (int c = c_first; c <= c_last; ++c) {
+                                if (empty(c)) continue;
+                                const int sl = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
+                                const float lw = __ldcg(prm.part_lse + (int64_t)sl * 128 + rr);
+                                const float w = lw == -INFINITY ? 0.f : __expf(lw - mx);
+                                tot += w;
+                                const float4* src = reinterpret_cast<const float4*>(
+                                    prm.part_o + ((int64_t)sl * 128 + rr) * D + c8 * 8);
+                                const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+                                acc[0] += w * x0.x; acc[1] += w * x0.y;
+                                acc[2] += w * x0.z; acc[3] += w * x0.w;
+                                acc[4] += w * x1.x; acc[5] += w * x1.y;
+                                acc[6] += w * x1.z; acc[7] += w * x1.w;
+                            }
+                            const float inv = tot > 0.f ? 1.f / tot : 0.f;
+                            const int64_t orow =
+                                ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+                            uint4 w4;
+                            w4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                            w4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                            w4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+                            w4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
+                                                      c8 * 8) = w4;
+                            if (c8 == 0 && a.lse) a.lse[orow] = mx + logf(tot);
+                        }
+                        if (tid == 0) a.seg_counters[seg] = 0;  // ready for the next call
+                    }
+                }
                 named_bar_sync(1, NW * 32);  // scratch reused by the next piece
             }
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
@@ -584,9 +644,7 @@ cudaError_t launch_attn_mma(const AttnArgs& a, int num_ctas, void* workspace, cu
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attn_mma_kernel<<<num_ctas, THREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, prm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, stream);
+    return cudaGetLastError();
 }
 
 }  // namespace specv

@@ -23,7 +23,8 @@ struct AttnArgs {
     float scale;
     void* out;
     float* lse;
-    int* dev_err;  // device error word
+    int* dev_err;       // device error word
+    int* seg_counters;  // [B*Hkv] zeroed arrival counters (fused split-KV merge)
 };
 
 // ---- SIMT kernel (CUDA cores; any supported dtype / shape) ----

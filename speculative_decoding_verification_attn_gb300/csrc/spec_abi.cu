@@ -33,9 +33,13 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<int64_t> g_opt_path{0}, g_opt_ctas{0}, g_opt_validate{0}, g_opt_simt_chunk{0};
 
-// Per-device workspace: [error word + tickets | scratch].
-constexpr size_t kHeader = 64 * 1024;   // error word at 0, acceptance tickets at 256
-constexpr int kMaxTickets = (int)((kHeader - 256) / 4);
+// Per-device workspace: [error word | acceptance tickets | segment counters |
+// scratch].  The header is zeroed at allocation; tickets and counters are
+// reset by the kernels that use them.
+constexpr size_t kHeader = 128 * 1024;
+constexpr size_t kTicketsOff = 256, kCountersOff = 64 * 1024;
+constexpr int kMaxTickets = (int)((kCountersOff - kTicketsOff) / 4);
+constexpr int kMaxCounters = (int)((kHeader - kCountersOff) / 4);
 struct Workspace {
     void* base = nullptr;
     size_t bytes = 0;
@@ -195,6 +199,7 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
     a.P = page_size; a.num_pages = num_pages; a.max_pages = max_pages_per_seq;
     a.q_dtype = q_dtype; a.kv_dtype = kv_dtype; a.scale = scale;
     a.out = out; a.lse = lse;
+    a.dev_err = nullptr; a.seg_counters = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // kernels: 1 SIMT, 2 tcgen05, 3 warp MMA; automatic = warp MMA for <= 16
@@ -209,6 +214,9 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
                         "shape/dtype", (int)path);
         kernel = (int)path;
     } else kernel = mma_ok ? 3 : tc_ok ? 2 : 1;
+    if (kernel == 3 && (int64_t)batch * num_kv_heads > kMaxCounters)
+        return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads > %d for the warp-MMA kernel",
+                    kMaxCounters);
     const bool use_tc = kernel != 1;
 
     Workspace* ws = nullptr;
@@ -225,6 +233,7 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
         rc = get_workspace(specv::tc_workspace_bytes(a, ctas), &ws);
         if (rc) return rc;
         a.dev_err = static_cast<int*>(ws->base);
+        a.seg_counters = reinterpret_cast<int*>(static_cast<char*>(ws->base) + kCountersOff);
         e = kernel == 3 ? specv::launch_attn_mma(a, ctas, static_cast<char*>(ws->base) + kHeader, st)
                         : specv::launch_attn_tc(a, ctas, static_cast<char*>(ws->base) + kHeader, st);
         if (e != cudaSuccess) return cuda_fail(e, "verify_attn (tensor-core) launch");
@@ -264,7 +273,7 @@ int spec_accept_greedy(const void* logits, int32_t logits_dtype, const int32_t* 
     Workspace* ws = nullptr;
     int rc = get_workspace(specv::accept_workspace_bytes(a), &ws);
     if (rc) return rc;
-    int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws->base) + 256);
+    int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws->base) + kTicketsOff);
     cudaError_t e = specv::launch_accept(a, static_cast<char*>(ws->base) + kHeader, tickets,
                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "accept_greedy launch");
