@@ -96,9 +96,10 @@ def test_page_size_8_runs_on_simt(oracle_mod):
     # per box; smaller pages go to the SIMT kernel under the automatic path
     inp = make_inputs(small_spec(page_size=8, ctx=(1, 200)), seed=29)
     check_attn_full(oracle_mod, inp, "page_size=8")
-    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
-    with pytest.raises(binding.SpecError, match="not supported"):
-        gpu_attn(inp)
+    for path in (2, 3):
+        binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, path)
+        with pytest.raises(binding.SpecError, match="does not support"):
+            gpu_attn(inp)
 
 
 def test_tensor_core_matches_simt():
