@@ -12,24 +12,31 @@
 // accumulate), so every K/V byte is read from HBM once and used for all rows.
 // Unlike a 128-row tcgen05 tile (mostly padding at 8-16 rows), the softmax
 // lives in registers: no TMEM round trips and no per-tile hand-off between
-// warps, which keeps each K/V stage busy only for its load latency plus a few
-// hundred cycles -- the pipeline depth the load latency needs.
+// warps.
 //
-//  * Work: the same stream-K tile list as the tcgen05 kernel (64-key tiles of
-//    every (sequence, kv-head) segment over a persistent grid); a segment cut
-//    by a CTA-range boundary leaves (O/l, lse) partials, and the last of its
-//    pieces to finish merges them (atomic arrival count per segment, no
-//    waiting), so one launch does the whole call.
-//  * Warps: 0-3 compute, warp w owns keys [16w, 16w+16) of every tile (one TMA
-//    page box); warp 4 is the TMA producer (16-key 3-D page boxes of 4 KB,
-//    128-byte swizzle, block-table entries prefetched with cp.async).
+//  * Work: a stream-K list of 128-key tiles of every (sequence, kv-head)
+//    segment over a persistent grid; a segment cut by a CTA-range boundary
+//    leaves (O/l, lse) partials, and the last of its pieces to finish merges
+//    them (atomic arrival count per segment, no waiting), so one launch does
+//    the whole call.
+//  * Warps: eight, two per SM sub-partition so that one hides the other's
+//    MMA and shared-memory latency.  Warp w owns keys [16w, 16w+16) of every
+//    tile -- one 4 KB TMA page box of K and one of V -- and keeps a private
+//    ring of NS such box pairs: it refills a stage with its box NS tiles
+//    ahead as soon as it has used it, so there is no producer warp, no
+//    "stage empty" barrier and no serial TMA issue loop (each warp issues two
+//    boxes per tile).  The block-table entry of that box is read at the start
+//    of the tile and used after it, hiding its latency behind the MMAs.
+//    Warp 0 also loads each piece's query rows, one piece ahead, into two
+//    staging buffers.
 //  * Per warp and tile: S = Q K^T (16 MMAs, K via ldmatrix), masked online
 //    softmax in registers with a lazily moved reference max, P V (16 MMAs,
-//    V via ldmatrix.trans, P straight from the S accumulators).  The four
-//    warps' (max, sum, O) are merged once per segment through shared memory.
+//    V via ldmatrix.trans, P straight from the S accumulators).  The eight
+//    warps' (max, sum, O) are merged once per segment piece in shared memory.
 //  * Every mbarrier wait is bounded (1 s); a timeout sets the device error
-//    word and an abort flag after which every role skips its remaining work,
-//    still passing every CTA barrier.
+//    word and an abort flag after which every warp skips its remaining work,
+//    still passing every CTA barrier, and waits (bounded) for its own loads
+//    in flight before the CTA exits.
 #include <cuda.h>
 #include <math.h>
 
@@ -39,18 +46,16 @@ namespace specv {
 namespace {
 
 constexpr int D = 128;
-constexpr int TN = 64;               // keys per tile
-constexpr int NW = 4;                // compute warps (16 keys each)
-constexpr int NS = 6;                // K/V stages
-constexpr int BOX_ROWS = 16;         // keys per TMA box
+constexpr int NW = 8;                // compute warps
+constexpr int BOX_ROWS = 16;         // keys per TMA box = keys of one warp in a tile
+constexpr int TN = NW * BOX_ROWS;    // 128 keys per tile
+constexpr int NS = 3;                // stages of each warp's private K/V ring
 constexpr int BOX_BYTES = BOX_ROWS * D * 2;  // 4 KB
-constexpr int KV_BYTES = TN * D * 2;         // 16 KB per tensor per stage
-constexpr int STAGE_BYTES = 2 * KV_BYTES;
+constexpr int WSTAGE_BYTES = 2 * BOX_BYTES;  // one warp's K box + V box
 constexpr int QROWS = 16;
 constexpr int Q_HALF = QROWS * 128;  // 2 KB: 64 head-dim columns of 16 rows
-constexpr int LOOKAHEAD = 6;
-constexpr int MAX_BOX = TN / BOX_ROWS;
-constexpr int THREADS = (NW + 1) * 32;
+constexpr int Q_BUF = 2 * Q_HALF;
+constexpr int THREADS = NW * 32;
 constexpr int MAX_BATCH = 1024;
 constexpr int OSTRIDE = D + 4;       // merge scratch row stride (floats)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -60,21 +65,20 @@ constexpr float kRescaleThreshold = 8.0f;
 using Cursor = CursorT<TN>;
 
 struct Smem {
-    static constexpr int STAGES = 0;
-    static constexpr int Q = STAGES + NS * STAGE_BYTES;       // 2 halves x 2 KB
-    static constexpr int SCRATCH = Q + 2 * Q_HALF;            // [16][OSTRIDE] float
+    static constexpr int RING = 0;                              // [NS][NW][K box, V box]
+    static constexpr int Q = RING + NS * NW * WSTAGE_BYTES;     // 2 buffers x 2 halves x 2 KB
+    static constexpr int SCRATCH = Q + 2 * Q_BUF;               // [16][OSTRIDE] float
     static constexpr int BARS = SCRATCH + QROWS * OSTRIDE * 4;
-    static constexpr int B_KVFULL = 0, B_KVEMPTY = NS, B_QFULL = 2 * NS, B_QFREE = 2 * NS + 1,
-                         NUM_BARS = 2 * NS + 2;
-    static constexpr int MISC = BARS + NUM_BARS * 8;          // abort flag
-    static constexpr int STAT = MISC + 16;                     // [NW][16] (m, l)
-    static constexpr int PIDS = STAT + 2 * NW * QROWS * 4;
-    static constexpr int CTX = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;
+    static constexpr int B_KVFULL = 0, B_QFULL = NS * NW, NUM_BARS = NS * NW + 2;
+    static constexpr int MISC = BARS + NUM_BARS * 8;            // abort and merge flags
+    static constexpr int STAT = MISC + 16;                      // [NW][16] (m, l)
+    static constexpr int CTX = STAT + 2 * NW * QROWS * 4;
     static constexpr int PRE = CTX + MAX_BATCH * 4;
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
 };
 constexpr size_t SMEM_BYTES = Smem::END + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(NS <= 32, "stage bit masks");
 
 struct MmaParams {
     AttnArgs a;
@@ -120,7 +124,6 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC);
     volatile int* merge_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC + 4);
-    int* pid_ring = reinterpret_cast<int*>(sm + Smem::PIDS);
     int* s_ctx = reinterpret_cast<int*>(sm + Smem::CTX);
     int* s_pre = reinterpret_cast<int*>(sm + Smem::PRE);
 
@@ -128,22 +131,19 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const int B = a.B, k = a.k, Hkv = a.Hkv, G = a.Hq / a.Hkv, R = k * G, P = a.P;
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars[Smem::B_KVFULL + s], 1);
-            mbar_init(&bars[Smem::B_KVEMPTY + s], NW);
-        }
+        for (int i = 0; i < NS * NW; ++i) mbar_init(&bars[Smem::B_KVFULL + i], 1);
         mbar_init(&bars[Smem::B_QFULL], 1);
-        mbar_init(&bars[Smem::B_QFREE], NW);
+        mbar_init(&bars[Smem::B_QFULL + 1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     {
         // Q rows R..15 stay zero (the TMA writes rows 0..R-1 only)
         uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
-        for (int e = tid; e < 2 * Q_HALF / 16; e += THREADS) q4[e] = make_uint4(0, 0, 0, 0);
+        for (int e = tid; e < 2 * Q_BUF / 16; e += THREADS) q4[e] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
-    if (warp == NW) {
+    if (warp == 0) {
         const int per = (B + 31) / 32, lo = lane * per, hi = min(B, lo + per);
         int sum = 0;
         for (int b = lo; b < hi; ++b) {
@@ -177,102 +177,11 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp == NW) {
-        // ================= TMA producer =================
-        Cursor cur, ahead;
-        if (n_tiles > 0) {
-            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
-            ahead = cur;
-        }
-        const uint64_t pol = l2_policy_evict_first();
-        if (lane == 0) {
-            prefetch_tmap(&qmap);
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
-        }
-        auto fetch_pids = [&](int slot, const Cursor& c) {
-            const int key0 = c.lt * TN;
-            const int nvalid = min(TN, s_ctx[c.b] + k - key0);
-            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-            if (lane < nbox) {
-                const int lp = (key0 + lane * BOX_ROWS) / P;
-                cp_async_4(&pid_ring[slot * MAX_BOX + lane],
-                           &a.block_table[(int64_t)c.b * a.max_pages + lp]);
-            }
-        };
-        for (int la = 0; la < LOOKAHEAD; ++la) {
-            if (la < n_tiles) {
-                fetch_pids(la % (LOOKAHEAD + 1), ahead);
-                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
-            }
-            cp_async_commit();
-        }
-        int pc = -1, n_issued = 0, issued_q = 0;
-        bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            if (it + LOOKAHEAD < n_tiles) {
-                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
-                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
-            }
-            cp_async_commit();
-            cp_async_wait<LOOKAHEAD>();  // entries of tile `it`
-            __syncwarp();
-            if (it == 0 || cur.lt == 0) {
-                // Q of the next piece once the compute warps hold the previous one
-                ++pc;
-                if (lane == 0) {
-                    if (pc >= 1)
-                        ok = mbar_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag, a.dev_err);
-                    if (ok) {
-                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL], 2 * R * 128);
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_3d(sm + Smem::Q + h * Q_HALF, &qmap, &bars[Smem::B_QFULL],
-                                        h * 64, cur.kvh * G, cur.b * k);
-                        issued_q = pc + 1;
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-            const int s = it % NS, use = it / NS;
-            const int key0 = cur.lt * TN;
-            const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
-            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-            if (lane == 0) {
-                if (use >= 1)
-                    ok = mbar_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag,
-                                   a.dev_err);
-                if (ok) mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s], 2u * nbox * BOX_BYTES);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane < 2 * nbox) {
-                const int tensor = lane & 1, bx = lane >> 1;
-                int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
-                if (page < 0 || page >= a.num_pages) {
-                    raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
-                    page = 0;
-                }
-                const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BOX_ROWS) % P;
-                tma_load_3d_hint(sm + Smem::STAGES + s * STAGE_BYTES + tensor * KV_BYTES +
-                                     bx * BOX_BYTES,
-                                 tensor ? (const void*)&vmap : (const void*)&kmap,
-                                 &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
-            }
-            n_issued = it + 1;
-            __syncwarp();
-            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
-        }
-        cp_async_wait<0>();
-        if (!ok && lane == 0) {
-            for (int s = 0; s < NS; ++s) {
-                const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
-                if (uses > 0) mbar_drain(&bars[Smem::B_KVFULL + s], (uses - 1) & 1);
-            }
-            if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
-        }
-    } else {
-        // ================= compute warps: keys [16w, 16w+16) of every tile =================
+    {
+        // ===== warp w owns keys [16w, 16w+16) of every tile and keeps its own
+        // ring of NS K/V boxes, refilling a stage as soon as it is done with
+        // it (no other warp reads this warp's boxes); warp 0 also loads the
+        // query rows of each segment piece, one piece ahead, into two buffers
         const int g = lane >> 2, t4 = lane & 3;  // MMA fragment group / thread in group
         const float sl2 = a.scale * kLog2e;
         const uint32_t q_base = smem_u32(sm + Smem::Q);
@@ -283,12 +192,87 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         int irow[2];
         irow[0] = g < R ? g / G : k - 1;
         irow[1] = g + 8 < R ? (g + 8) / G : k - 1;
+        const int kv0 = warp * BOX_ROWS;  // this warp's first key in every tile
+        uint8_t* ring = sm + Smem::RING + warp * WSTAGE_BYTES;  // stage s at + s * NW * WSTAGE_BYTES
+        uint64_t* full = &bars[Smem::B_KVFULL + warp];           // stage s at full[s * NW]
+        const uint64_t pol = l2_policy_evict_first();
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+            if (warp == 0) prefetch_tmap(&qmap);
+        }
+        // does this warp's box of tile c hold any key of the sequence (warp-uniform)
+        auto box_valid = [&](const Cursor& c) { return c.lt * TN + kv0 < s_ctx[c.b] + k; };
+        auto table_entry = [&](const Cursor& c) {
+            return a.block_table + (int64_t)c.b * a.max_pages + (c.lt * TN + kv0) / P;
+        };
+        // lane 0: load this warp's K and V boxes of tile c into stage st
+        auto issue = [&](int st, const Cursor& c, int page) {
+            if (page < 0 || page >= a.num_pages) {
+                raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                page = 0;
+            }
+            const int row = (page * Hkv + c.kvh) * P + (c.lt * TN + kv0) % P;
+            uint8_t* dst = ring + st * NW * WSTAGE_BYTES;
+            mbar_arrive_expect_tx(&full[st * NW], 2u * BOX_BYTES);
+            tma_load_3d_hint(dst, &kmap, &full[st * NW], 0, row, 0, pol);
+            tma_load_3d_hint(dst + BOX_BYTES, &vmap, &full[st * NW], 0, row, 0, pol);
+        };
+
+        // warp 0, lane 0: query rows of piece j (sequence b, kv-head kvh) into buffer j % 2
+        auto issue_q = [&](int j, int b, int kvh) {
+            uint64_t* bar = &bars[Smem::B_QFULL + (j & 1)];
+            mbar_arrive_expect_tx(bar, 2 * R * 128);
+            for (int h = 0; h < 2; ++h)
+                tma_load_3d(sm + Smem::Q + (j & 1) * Q_BUF + h * Q_HALF, &qmap, bar, h * 64,
+                            kvh * G, b * k);
+        };
+        // does a piece follow the one of cursor c in this CTA's range
+        auto has_next_piece = [&](const Cursor& c) { return c.seg_start + c.nb < t_end; };
+
+        Cursor cur, ahead;  // ahead: the tile NS past cur, the next one to load
+        uint32_t pending = 0, phase = 0;  // per stage: a load in flight / the parity it completes
+        int q_issued = 0;                 // warp 0: pieces whose query rows were loaded
+        if (n_tiles > 0) {
+            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            ahead = cur;
+            if (warp == 0) {
+                q_issued = has_next_piece(cur) ? 2 : 1;
+                if (lane == 0) {
+                    issue_q(0, cur.b, cur.kvh);
+                    if (q_issued == 2)
+                        issue_q(1, cur.kvh + 1 < Hkv ? cur.b : cur.b + 1,
+                                cur.kvh + 1 < Hkv ? cur.kvh + 1 : 0);
+                }
+            }
+            // prologue: block-table entries of tiles 0..NS-1 first, then their loads
+            int pg[NS];
+            {
+                Cursor c = cur;
+#pragma unroll
+                for (int j = 0; j < NS; ++j) {
+                    pg[j] = -1;
+                    if (j < n_tiles) {
+                        if (lane == 0 && box_valid(c)) pg[j] = __ldg(table_entry(c));
+                        if (j + 1 < n_tiles) c.next(s_ctx, Hkv, k);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                if (j < n_tiles) {
+                    if (box_valid(ahead)) {
+                        if (lane == 0) issue(j, ahead, pg[j]);
+                        pending |= 1u << j;
+                    }
+                    if (j + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+                }
+            }
+        }
 
         uint32_t qf[D / 16][4];
         float o[D / 8][4];
         float m_ref[2], lsum[2];
-        Cursor cur;
-        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
         bool ok = true;
         int pc = -1;
         for (int it = 0; it < n_tiles; ++it) {
@@ -297,9 +281,23 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int s = it % NS;
             const int ctx = s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
             const int nvalid = min(TN, L - key0);
+            // block-table entry of the box NS tiles ahead: read now, used after this tile
+            const bool refill = it + NS < n_tiles && box_valid(ahead);
+            int pg_next = -1;
+            if (refill && lane == 0) pg_next = __ldg(table_entry(ahead));
             if (first) {
                 ++pc;
-                if (ok) ok = warp_wait(&bars[Smem::B_QFULL], pc & 1, abort_flag, a.dev_err);
+                // the next piece's rows go to the buffer of piece pc - 1, which
+                // every warp read before the barriers that closed piece pc - 1
+                if (warp == 0 && ok && pc >= 1 && has_next_piece(cur)) {
+                    if (lane == 0)
+                        issue_q(pc + 1, cur.kvh + 1 < Hkv ? cur.b : cur.b + 1,
+                                cur.kvh + 1 < Hkv ? cur.kvh + 1 : 0);
+                    q_issued = pc + 2;
+                }
+                if (ok)
+                    ok = warp_wait(&bars[Smem::B_QFULL + (pc & 1)], (pc >> 1) & 1, abort_flag,
+                                   a.dev_err);
                 if (ok) {
                     // Q fragments: 16 rows x 16 columns per k-slice, from the
                     // 128-byte-swizzled staging buffer
@@ -307,26 +305,29 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
                         const int chunk = kk * 2 + (lane >> 4);
-                        ldsm_x4(q_base + sw_off(row, chunk, Q_HALF), qf[kk][0], qf[kk][1],
-                                qf[kk][2], qf[kk][3]);
+                        ldsm_x4(q_base + (pc & 1) * Q_BUF + sw_off(row, chunk, Q_HALF), qf[kk][0],
+                                qf[kk][1], qf[kk][2], qf[kk][3]);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[Smem::B_QFREE]);
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
                 m_ref[0] = m_ref[1] = -INFINITY;
                 lsum[0] = lsum[1] = 0.f;
             }
-            if (ok) ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
-            const int kv0 = warp * BOX_ROWS;  // this warp's first key in the tile
+            if (kv0 < nvalid) {
+                if (ok) ok = warp_wait(&full[s * NW], (phase >> s) & 1, abort_flag, a.dev_err);
+                if (ok) {
+                    pending &= ~(1u << s);
+                    phase ^= 1u << s;
+                }
+            }
             if (ok && kv0 < nvalid) {
-                const uint32_t kb = smem_u32(sm + Smem::STAGES + s * STAGE_BYTES) + warp * BOX_BYTES;
-                const uint32_t vb = kb + KV_BYTES;
+                const uint32_t kb = smem_u32(ring + s * NW * WSTAGE_BYTES);
+                const uint32_t vb = kb + BOX_BYTES;
                 if (nvalid - kv0 < BOX_ROWS) {
                     // keys past the sequence end in this box: zero their V rows
                     // so that 0 * (stale or canary) never reaches O
-                    uint8_t* vrow = sm + Smem::STAGES + s * STAGE_BYTES + KV_BYTES + warp * BOX_BYTES;
+                    uint8_t* vrow = ring + s * NW * WSTAGE_BYTES + BOX_BYTES;
                     for (int e = (nvalid - kv0) * 16 + lane; e < BOX_ROWS * 16; e += 32) {
                         const int r = e >> 4, c = e & 15;
                         *reinterpret_cast<uint4*>(vrow + sw_off(r, c, BOX_BYTES / 2)) =
@@ -414,10 +415,16 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[Smem::B_KVEMPTY + s]);
+            // every read of stage s is done (its values fed the MMAs): refill it
+            // with this warp's box NS tiles ahead
+            if (refill && ok) {
+                if (lane == 0) issue(s, ahead, pg_next);
+                pending |= 1u << s;
+            }
+            if (it + NS + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
 
             if (last) {
-                // ---- merge the four warps' (max, sum, O) of this segment piece
+                // ---- merge the warps' (max, sum, O) of this segment piece
                 float lrow[2];
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
@@ -572,6 +579,15 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 named_bar_sync(1, NW * 32);  // scratch reused by the next piece
             }
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+        // loads still in flight (only after an abort) land before the CTA exits
+        if (lane == 0) {
+            for (int st = 0; st < NS; ++st)
+                if ((pending >> st) & 1) mbar_drain(&full[st * NW], (phase >> st) & 1);
+            // warp 0 issued piece j only after waiting for piece j - 2 of the
+            // same buffer, so at most the last load of each buffer is in flight
+            for (int j = q_issued - 2; j < q_issued; ++j)
+                if (j >= 0) mbar_drain(&bars[Smem::B_QFULL + (j & 1)], (j >> 1) & 1);
         }
     }
     __syncthreads();
