@@ -57,7 +57,6 @@ constexpr int Q_HALF = QROWS * 128;  // 2 KB: 64 head-dim columns of 16 rows
 constexpr int Q_BUF = 2 * Q_HALF;
 constexpr int THREADS = NW * 32;
 constexpr int MAX_BATCH = 1024;
-constexpr int OSTRIDE = D + 4;       // merge scratch row stride (floats)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -67,8 +66,7 @@ using Cursor = CursorT<TN>;
 struct Smem {
     static constexpr int RING = 0;                              // [NS][NW][K box, V box]
     static constexpr int Q = RING + NS * NW * WSTAGE_BYTES;     // 2 buffers x 2 halves x 2 KB
-    static constexpr int SCRATCH = Q + 2 * Q_BUF;               // [16][OSTRIDE] float
-    static constexpr int BARS = SCRATCH + QROWS * OSTRIDE * 4;
+    static constexpr int BARS = Q + 2 * Q_BUF;
     static constexpr int B_KVFULL = 0, B_QFULL = NS * NW, NUM_BARS = NS * NW + 2;
     static constexpr int MISC = BARS + NUM_BARS * 8;            // abort and merge flags
     static constexpr int STAT = MISC + 16;                      // [NW][16] (m, l)
@@ -187,7 +185,6 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const uint32_t q_base = smem_u32(sm + Smem::Q);
         float* s_m = reinterpret_cast<float*>(sm + Smem::STAT);
         float* s_l = s_m + NW * QROWS;
-        float* scratch = reinterpret_cast<float*>(sm + Smem::SCRATCH);
         // the two rows this thread holds in every fragment: g and g + 8
         int irow[2];
         irow[0] = g < R ? g / G : k - 1;
@@ -416,12 +413,12 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             }
             __syncwarp();
             // every read of stage s is done (its values fed the MMAs): refill it
-            // with this warp's box NS tiles ahead
-            if (refill && ok) {
+            // with this warp's box NS tiles ahead -- after the merge when this
+            // tile ends a segment piece, since the merge stages O in it
+            if (refill && ok && !last) {
                 if (lane == 0) issue(s, ahead, pg_next);
                 pending |= 1u << s;
             }
-            if (it + NS + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
 
             if (last) {
                 // ---- merge the warps' (max, sum, O) of this segment piece
@@ -456,64 +453,67 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                                                                    : 0.f;
                     lse[hr] = Ls > 0.f ? (mt + log2f(Ls)) * kLn2 : -INFINITY;
                 }
-#pragma unroll 1
-                for (int w = 0; w < NW; ++w) {
-                    if (warp == w) {
+                // every warp stages its weighted O (fp32 [16][128], 8-column
+                // blocks XOR-swizzled by row) in its own stage s, free until the
+                // deferred refill below
+                {
+                    float* ob = reinterpret_cast<float*>(ring + s * NW * WSTAGE_BYTES);
 #pragma unroll
-                        for (int j = 0; j < D / 8; ++j) {
-                            float2* r0 = reinterpret_cast<float2*>(scratch + g * OSTRIDE + j * 8 + t4 * 2);
-                            float2* r1 =
-                                reinterpret_cast<float2*>(scratch + (g + 8) * OSTRIDE + j * 8 + t4 * 2);
-                            float2 x0 = make_float2(o[j][0] * wgt[0], o[j][1] * wgt[0]);
-                            float2 x1 = make_float2(o[j][2] * wgt[1], o[j][3] * wgt[1]);
-                            if (w > 0) {
-                                const float2 p0 = *r0, p1 = *r1;
-                                x0.x += p0.x;
-                                x0.y += p0.y;
-                                x1.x += p1.x;
-                                x1.y += p1.y;
-                            }
-                            *r0 = x0;
-                            *r1 = x1;
-                        }
+                    for (int j = 0; j < D / 8; ++j) {
+                        const int col = ((j ^ g) << 3) + t4 * 2;
+                        *reinterpret_cast<float2*>(ob + g * D + col) =
+                            make_float2(o[j][0] * wgt[0], o[j][1] * wgt[0]);
+                        *reinterpret_cast<float2*>(ob + (g + 8) * D + col) =
+                            make_float2(o[j][2] * wgt[1], o[j][3] * wgt[1]);
                     }
-                    named_bar_sync(1, NW * 32);
+                    fence_proxy_async_smem();  // before the refill TMA writes this stage
+                }
+                named_bar_sync(1, NW * 32);
+                // warp w sums the eight staged blocks of output columns
+                // [16w, 16w+16): lane -> row lane/2, 8 columns
+                const int rr = lane >> 1, jb = 2 * warp + (lane & 1);
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float4* src = reinterpret_cast<const float4*>(
+                        sm + Smem::RING + (s * NW + w) * WSTAGE_BYTES +
+                        (rr * D + ((jb ^ (rr & 7)) << 3)) * 4);
+                    const float4 x0 = src[0], x1 = src[1];
+                    acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
+                    acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
                 }
                 const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
                 const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
                 if (ok) {
-                    // 16 rows x 16 chunks of 8 columns over the 128 compute threads
-                    for (int idx = tid; idx < R * (D / 8); idx += NW * 32) {
-                        const int rr = idx / (D / 8), c8 = idx % (D / 8);
-                        const float* src = scratch + rr * OSTRIDE + c8 * 8;
+                    if (rr < R) {
                         const int64_t orow =
                             ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
                         if (complete) {
                             uint4 w4;
-                            w4.x = pack_bf16x2(src[0], src[1]);
-                            w4.y = pack_bf16x2(src[2], src[3]);
-                            w4.z = pack_bf16x2(src[4], src[5]);
-                            w4.w = pack_bf16x2(src[6], src[7]);
+                            w4.x = pack_bf16x2(acc[0], acc[1]);
+                            w4.y = pack_bf16x2(acc[2], acc[3]);
+                            w4.z = pack_bf16x2(acc[4], acc[5]);
+                            w4.w = pack_bf16x2(acc[6], acc[7]);
                             *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
-                                                      c8 * 8) = w4;
+                                                      jb * 8) = w4;
                         } else {
                             float4* dst = reinterpret_cast<float4*>(
-                                prm.part_o + ((int64_t)slot * 128 + rr) * D + c8 * 8);
-                            dst[0] = make_float4(src[0], src[1], src[2], src[3]);
-                            dst[1] = make_float4(src[4], src[5], src[6], src[7]);
+                                prm.part_o + ((int64_t)slot * 128 + rr) * D + jb * 8);
+                            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
                         }
                     }
                     if (warp == 0 && t4 == 0) {
 #pragma unroll
                         for (int hr = 0; hr < 2; ++hr) {
-                            const int rr = g + 8 * hr;
-                            if (rr >= R) continue;
+                            const int r2 = g + 8 * hr;
+                            if (r2 >= R) continue;
                             const int64_t orow =
-                                ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+                                ((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G;
                             if (complete) {
                                 if (a.lse) a.lse[orow] = lse[hr];
                             } else {
-                                prm.part_lse[(int64_t)slot * 128 + rr] = lse[hr];
+                                prm.part_lse[(int64_t)slot * 128 + r2] = lse[hr];
                             }
                         }
                     }
@@ -521,8 +521,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (!complete) {
                     // fused split-KV merge: the last piece of a segment to arrive
                     // merges all its pieces' partials (no CTA ever waits)
-                    __threadfence();
-                    named_bar_sync(1, NW * 32);
+                    named_bar_sync(1, NW * 32);  // this piece's partials are written
                     const int64_t s0 = cur.seg_start, s1 = s0 + cur.nb;
                     auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
                     auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
@@ -531,53 +530,60 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     if (tid == 0) {
                         int npieces = 0;
                         for (int c = c_first; c <= c_last; ++c) npieces += empty(c) ? 0 : 1;
+                        __threadfence();  // release the CTA's partials (ordered by the barrier)
                         const int old = atomicAdd(&a.seg_counters[seg], 1);
-                        *merge_flag = (old == npieces - 1);
+                        const bool merger = old == npieces - 1;
+                        if (merger) __threadfence();  // acquire the other pieces' partials
+                        *merge_flag = merger;
                     }
                     named_bar_sync(1, NW * 32);
                     if (*merge_flag) {
-                        __threadfence();
+                        // one pass over the pieces with a running maximum
                         for (int idx = tid; idx < R * (D / 8); idx += NW * 32) {
-                            const int rr = idx / (D / 8), c8 = idx % (D / 8);
-                            float mx = -INFINITY;
+                            const int r2 = idx / (D / 8), c8 = idx % (D / 8);
+                            float mx = -INFINITY, tot = 0.f;
+                            float m8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
                             for (int c = c_first; c <= c_last; ++c) {
                                 if (empty(c)) continue;
                                 const int sl = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
-                                mx = fmaxf(mx, __ldcg(prm.part_lse + (int64_t)sl * 128 + rr));
-                            }
-                            float tot = 0.f;
-                            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            for (int c = c_first; c <= c_last; ++c) {
-                                if (empty(c)) continue;
-                                const int sl = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
-                                const float lw = __ldcg(prm.part_lse + (int64_t)sl * 128 + rr);
-                                const float w = lw == -INFINITY ? 0.f : __expf(lw - mx);
-                                tot += w;
+                                const float lw = __ldcg(prm.part_lse + (int64_t)sl * 128 + r2);
                                 const float4* src = reinterpret_cast<const float4*>(
-                                    prm.part_o + ((int64_t)sl * 128 + rr) * D + c8 * 8);
+                                    prm.part_o + ((int64_t)sl * 128 + r2) * D + c8 * 8);
                                 const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-                                acc[0] += w * x0.x; acc[1] += w * x0.y;
-                                acc[2] += w * x0.z; acc[3] += w * x0.w;
-                                acc[4] += w * x1.x; acc[5] += w * x1.y;
-                                acc[6] += w * x1.z; acc[7] += w * x1.w;
+                                if (lw == -INFINITY) continue;
+                                const float mn = fmaxf(mx, lw);
+                                const float sa = mx == -INFINITY ? 0.f : __expf(mx - mn);
+                                const float sb = __expf(lw - mn);
+                                mx = mn;
+                                tot = tot * sa + sb;
+                                m8[0] = m8[0] * sa + sb * x0.x; m8[1] = m8[1] * sa + sb * x0.y;
+                                m8[2] = m8[2] * sa + sb * x0.z; m8[3] = m8[3] * sa + sb * x0.w;
+                                m8[4] = m8[4] * sa + sb * x1.x; m8[5] = m8[5] * sa + sb * x1.y;
+                                m8[6] = m8[6] * sa + sb * x1.z; m8[7] = m8[7] * sa + sb * x1.w;
                             }
                             const float inv = tot > 0.f ? 1.f / tot : 0.f;
                             const int64_t orow =
-                                ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+                                ((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G;
                             uint4 w4;
-                            w4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-                            w4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-                            w4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-                            w4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+                            w4.x = pack_bf16x2(m8[0] * inv, m8[1] * inv);
+                            w4.y = pack_bf16x2(m8[2] * inv, m8[3] * inv);
+                            w4.z = pack_bf16x2(m8[4] * inv, m8[5] * inv);
+                            w4.w = pack_bf16x2(m8[6] * inv, m8[7] * inv);
                             *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
                                                       c8 * 8) = w4;
-                            if (c8 == 0 && a.lse) a.lse[orow] = mx + logf(tot);
+                            if (c8 == 0 && a.lse) a.lse[orow] = tot > 0.f ? mx + logf(tot) : -INFINITY;
                         }
                         if (tid == 0) a.seg_counters[seg] = 0;  // ready for the next call
                     }
                 }
-                named_bar_sync(1, NW * 32);  // scratch reused by the next piece
+                named_bar_sync(1, NW * 32);  // every read of the staged O is done
+                if (refill && ok) {
+                    if (lane == 0) issue(s, ahead, pg_next);
+                    pending |= 1u << s;
+                }
             }
+            if (it + NS + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
         // loads still in flight (only after an abort) land before the CTA exits
