@@ -66,9 +66,11 @@ using Cursor = CursorT<TN>;
 struct Smem {
     static constexpr int RING = 0;                              // [NS][NW][K box, V box]
     static constexpr int Q = RING + NS * NW * WSTAGE_BYTES;     // 2 buffers x 2 halves x 2 KB
-    static constexpr int BARS = Q + 2 * Q_BUF;
+    static constexpr int PREF = Q + 2 * Q_BUF;                   // [16][D] float: other piece's O
+    static constexpr int PREF_LSE = PREF + QROWS * D * 4;       // [128] float: its lse slot
+    static constexpr int BARS = PREF_LSE + 128 * 4;
     static constexpr int B_KVFULL = 0, B_QFULL = NS * NW, NUM_BARS = NS * NW + 2;
-    static constexpr int MISC = BARS + NUM_BARS * 8;            // abort and merge flags
+    static constexpr int MISC = BARS + NUM_BARS * 8;            // abort flag, prefetch state/slot
     static constexpr int STAT = MISC + 16;                      // [NW][16] (m, l)
     static constexpr int CTX = STAT + 2 * NW * QROWS * 4;
     static constexpr int PRE = CTX + MAX_BATCH * 4;
@@ -121,7 +123,8 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const AttnArgs& a = prm.a;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC);
-    volatile int* merge_flag = reinterpret_cast<volatile int*>(sm + Smem::MISC + 4);
+    volatile int* s_pf = reinterpret_cast<volatile int*>(sm + Smem::MISC + 4);
+    volatile int* s_pf_slot = reinterpret_cast<volatile int*>(sm + Smem::MISC + 8);
     int* s_ctx = reinterpret_cast<int*>(sm + Smem::CTX);
     int* s_pre = reinterpret_cast<int*>(sm + Smem::PRE);
 
@@ -267,6 +270,30 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             }
         }
 
+        // pieces of a segment split over CTA ranges: CTA of tile t, empty
+        // ranges, partial slot of CTA c's piece of the segment starting at s0
+        auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
+        auto empty_cta = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
+        auto slot_of = [&](int c, int64_t s0) { return 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1); };
+        // End-of-range prefetch (warp 0).  The piece that ends this CTA's range
+        // in a segment that continues in the next CTA is normally the last of
+        // the segment's two pieces to finish (the other one ran at the start of
+        // that CTA).  At its first tile warp 0 reads the segment's arrival
+        // count; one tile later, if the other piece has arrived, it copies that
+        // piece's partial into shared memory, and the merge then needs neither
+        // this piece's partial in global memory nor another round trip.
+        int pf_state = 0;  // 0 none, 1 count read issued, 2 partial copy issued, 3 unavailable,
+                           // 4 other piece arrived (read its partial from global memory)
+        int pf_cnt = 0, pf_slot = 0;
+        float* pref = reinterpret_cast<float*>(sm + Smem::PREF);
+        float* pref_lse = reinterpret_cast<float*>(sm + Smem::PREF_LSE);
+        auto pf_ready = [&]() {  // warp 0, warp-uniform; acquires the other piece's partial
+            const int ready = __shfl_sync(0xffffffffu, pf_cnt == 1 ? 1 : 0, 0);
+            if (ready && lane == 0) __threadfence();
+            __syncwarp();
+            return ready != 0;
+        };
+
         uint32_t qf[D / 16][4];
         float o[D / 8][4];
         float m_ref[2], lsum[2];
@@ -310,6 +337,30 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
                 m_ref[0] = m_ref[1] = -INFINITY;
                 lsum[0] = lsum[1] = 0.f;
+                if (warp == 0 && ok && !has_next_piece(cur) && cur.seg_start + cur.nb > t_end) {
+                    const int64_t s0 = cur.seg_start;
+                    int npieces = 0, other = -1;
+                    for (int c = cta_of(s0); c <= cta_of(s0 + cur.nb - 1); ++c)
+                        if (!empty_cta(c)) {
+                            ++npieces;
+                            if (c != (int)blockIdx.x) other = c;
+                        }
+                    if (npieces == 2) {
+                        pf_slot = slot_of(other, s0);
+                        if (lane == 0) pf_cnt = ld_acquire_gpu(&a.seg_counters[cur.b * Hkv + cur.kvh]);
+                        pf_state = 1;
+                    }
+                }
+            } else if (warp == 0 && pf_state == 1) {
+                if (pf_ready()) {
+                    const float* so = prm.part_o + (int64_t)pf_slot * 128 * D;
+                    for (int c = lane; c < R * D / 4; c += 32) cp_async_16_cg(pref + c * 4, so + c * 4);
+                    cp_async_16_cg(pref_lse + lane * 4, prm.part_lse + (int64_t)pf_slot * 128 + lane * 4);
+                    cp_async_commit();
+                    pf_state = 2;
+                } else {
+                    pf_state = 3;
+                }
             }
             if (kv0 < nvalid) {
                 if (ok) ok = warp_wait(&full[s * NW], (phase >> s) & 1, abort_flag, a.dev_err);
@@ -422,6 +473,14 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 
             if (last) {
                 // ---- merge the warps' (max, sum, O) of this segment piece
+                if (warp == 0) {
+                    if (pf_state == 1) pf_state = pf_ready() ? 4 : 3;
+                    if (pf_state == 2) cp_async_wait<0>();
+                    if (lane == 0) {
+                        *s_pf = pf_state;
+                        *s_pf_slot = pf_slot;
+                    }
+                }
                 float lrow[2];
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
@@ -436,6 +495,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     s_l[warp * QROWS + g + 8] = lrow[1];
                 }
                 named_bar_sync(1, NW * 32);
+                const int pf = *s_pf;
                 float wgt[2], lse[2];
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
@@ -470,83 +530,138 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 named_bar_sync(1, NW * 32);
                 // warp w sums the eight staged blocks of output columns
-                // [16w, 16w+16): lane -> row lane/2, 8 columns
-                const int rr = lane >> 1, jb = 2 * warp + (lane & 1);
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // [16w, 16w+16): lane -> row lane/2, 8 columns as two 16-byte
+                // halves, odd rows reading the upper half first so that each
+                // quarter-warp touches eight distinct bank groups
+                const int rr = lane >> 1, jb = 2 * warp + (lane & 1), hf = rr & 1;
+                float acc[8];
+                {
+                    float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const float4* src = reinterpret_cast<const float4*>(
-                        sm + Smem::RING + (s * NW + w) * WSTAGE_BYTES +
-                        (rr * D + ((jb ^ (rr & 7)) << 3)) * 4);
-                    const float4 x0 = src[0], x1 = src[1];
-                    acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
-                    acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+                    for (int w = 0; w < NW; ++w) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            sm + Smem::RING + (s * NW + w) * WSTAGE_BYTES +
+                            (rr * D + ((jb ^ (rr & 7)) << 3)) * 4);
+                        const float4 x = src[hf], y = src[hf ^ 1];
+                        sa.x += x.x; sa.y += x.y; sa.z += x.z; sa.w += x.w;
+                        sb.x += y.x; sb.y += y.y; sb.z += y.z; sb.w += y.w;
+                    }
+                    const float4 lo4 = hf ? sb : sa, hi4 = hf ? sa : sb;
+                    acc[0] = lo4.x; acc[1] = lo4.y; acc[2] = lo4.z; acc[3] = lo4.w;
+                    acc[4] = hi4.x; acc[5] = hi4.y; acc[6] = hi4.z; acc[7] = hi4.w;
                 }
                 const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
-                const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
-                if (ok) {
-                    if (rr < R) {
-                        const int64_t orow =
-                            ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
-                        if (complete) {
-                            uint4 w4;
-                            w4.x = pack_bf16x2(acc[0], acc[1]);
-                            w4.y = pack_bf16x2(acc[2], acc[3]);
-                            w4.z = pack_bf16x2(acc[4], acc[5]);
-                            w4.w = pack_bf16x2(acc[6], acc[7]);
-                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
-                                                      jb * 8) = w4;
+                const int seg = cur.b * Hkv + cur.kvh;
+                const int64_t orow_rr =
+                    ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
+                auto store_out = [&](int64_t orow, int c8, const float* v, float scale_) {
+                    uint4 w4;
+                    w4.x = pack_bf16x2(v[0] * scale_, v[1] * scale_);
+                    w4.y = pack_bf16x2(v[2] * scale_, v[3] * scale_);
+                    w4.z = pack_bf16x2(v[4] * scale_, v[5] * scale_);
+                    w4.w = pack_bf16x2(v[6] * scale_, v[7] * scale_);
+                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + c8 * 8) = w4;
+                };
+                bool count_arrival = false;
+                if (complete) {
+                    if (ok) {
+                        if (rr < R) store_out(orow_rr, jb, acc, 1.f);
+                        if (warp == 0 && t4 == 0 && a.lse) {
+#pragma unroll
+                            for (int hr = 0; hr < 2; ++hr) {
+                                const int r2 = g + 8 * hr;
+                                if (r2 < R)
+                                    a.lse[((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G] =
+                                        lse[hr];
+                            }
+                        }
+                    }
+                } else if (pf == 2 || pf == 4) {
+                    // every other piece of the segment has arrived: merge with
+                    // its partial here, without publishing this one
+                    if (ok && rr < R) {
+                        float mt = -INFINITY;
+#pragma unroll
+                        for (int w = 0; w < NW; ++w) mt = fmaxf(mt, s_m[w * QROWS + rr]);
+                        float Ls = 0.f;
+#pragma unroll
+                        for (int w = 0; w < NW; ++w) {
+                            const float mw = s_m[w * QROWS + rr];
+                            if (mw != -INFINITY) Ls += s_l[w * QROWS + rr] * fast_exp2(mw - mt);
+                        }
+                        const float l_own = Ls > 0.f ? (mt + log2f(Ls)) * kLn2 : -INFINITY;
+                        const int oslot = *s_pf_slot;
+                        float l_oth;
+                        float4 y0, y1;
+                        if (pf == 2) {
+                            l_oth = pref_lse[rr];
+                            y0 = *reinterpret_cast<const float4*>(pref + rr * D + jb * 8);
+                            y1 = *reinterpret_cast<const float4*>(pref + rr * D + jb * 8 + 4);
                         } else {
+                            l_oth = __ldcg(prm.part_lse + (int64_t)oslot * 128 + rr);
+                            const float4* src = reinterpret_cast<const float4*>(
+                                prm.part_o + ((int64_t)oslot * 128 + rr) * D + jb * 8);
+                            y0 = __ldcg(src);
+                            y1 = __ldcg(src + 1);
+                        }
+                        const float mx = fmaxf(l_own, l_oth);
+                        const float w1 = l_own == -INFINITY ? 0.f : __expf(l_own - mx);
+                        const float w2 = l_oth == -INFINITY ? 0.f : __expf(l_oth - mx);
+                        const float tot = w1 + w2, inv = tot > 0.f ? 1.f / tot : 0.f;
+                        float v8[8] = {w1 * acc[0] + w2 * y0.x, w1 * acc[1] + w2 * y0.y,
+                                       w1 * acc[2] + w2 * y0.z, w1 * acc[3] + w2 * y0.w,
+                                       w1 * acc[4] + w2 * y1.x, w1 * acc[5] + w2 * y1.y,
+                                       w1 * acc[6] + w2 * y1.z, w1 * acc[7] + w2 * y1.w};
+                        store_out(orow_rr, jb, v8, inv);
+                        if (jb == 0 && a.lse) a.lse[orow_rr] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+                    }
+                    if (tid == 0) a.seg_counters[seg] = 0;  // ready for the next call
+                } else {
+                    // publish this piece's partial; warp 0 then counts the
+                    // arrival, and the last piece of the segment merges them all
+                    const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
+                    if (ok) {
+                        if (rr < R) {
                             float4* dst = reinterpret_cast<float4*>(
                                 prm.part_o + ((int64_t)slot * 128 + rr) * D + jb * 8);
                             dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
                             dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
                         }
-                    }
-                    if (warp == 0 && t4 == 0) {
+                        if (warp == 0 && t4 == 0) {
 #pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            const int r2 = g + 8 * hr;
-                            if (r2 >= R) continue;
-                            const int64_t orow =
-                                ((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G;
-                            if (complete) {
-                                if (a.lse) a.lse[orow] = lse[hr];
-                            } else {
-                                prm.part_lse[(int64_t)slot * 128 + r2] = lse[hr];
-                            }
+                            for (int hr = 0; hr < 2; ++hr)
+                                if (g + 8 * hr < R) prm.part_lse[(int64_t)slot * 128 + g + 8 * hr] = lse[hr];
                         }
                     }
+                    count_arrival = true;
                 }
-                if (!complete) {
-                    // fused split-KV merge: the last piece of a segment to arrive
-                    // merges all its pieces' partials (no CTA ever waits)
-                    named_bar_sync(1, NW * 32);  // this piece's partials are written
-                    const int64_t s0 = cur.seg_start, s1 = s0 + cur.nb;
-                    auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
-                    auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
-                    const int c_first = cta_of(s0), c_last = cta_of(s1 - 1);
-                    const int seg = cur.b * Hkv + cur.kvh;
-                    if (tid == 0) {
+                named_bar_sync(1, NW * 32);  // staged O read, partials written
+                if (refill && ok) {
+                    if (lane == 0) issue(s, ahead, pg_next);
+                    pending |= 1u << s;
+                }
+                if (count_arrival && warp == 0) {
+                    const int64_t s0 = cur.seg_start;
+                    const int c_first = cta_of(s0), c_last = cta_of(s0 + cur.nb - 1);
+                    int merger = 0;
+                    if (lane == 0) {
                         int npieces = 0;
-                        for (int c = c_first; c <= c_last; ++c) npieces += empty(c) ? 0 : 1;
-                        __threadfence();  // release the CTA's partials (ordered by the barrier)
-                        const int old = atomicAdd(&a.seg_counters[seg], 1);
-                        const bool merger = old == npieces - 1;
+                        for (int c = c_first; c <= c_last; ++c) npieces += empty_cta(c) ? 0 : 1;
+                        __threadfence();  // release the partials (ordered by the barrier)
+                        merger = atomicAdd(&a.seg_counters[seg], 1) == npieces - 1;
                         if (merger) __threadfence();  // acquire the other pieces' partials
-                        *merge_flag = merger;
                     }
-                    named_bar_sync(1, NW * 32);
-                    if (*merge_flag) {
-                        // one pass over the pieces with a running maximum
-                        for (int idx = tid; idx < R * (D / 8); idx += NW * 32) {
+                    merger = __shfl_sync(0xffffffffu, merger, 0);
+                    if (merger) {
+                        // warp 0 merges every piece's partial; the other warps go on
+                        for (int idx = lane; idx < R * (D / 8); idx += 32) {
                             const int r2 = idx / (D / 8), c8 = idx % (D / 8);
                             float mx = -INFINITY, tot = 0.f;
                             float m8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
                             for (int c = c_first; c <= c_last; ++c) {
-                                if (empty(c)) continue;
-                                const int sl = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
+                                if (empty_cta(c)) continue;
+                                const int sl = slot_of(c, s0);
                                 const float lw = __ldcg(prm.part_lse + (int64_t)sl * 128 + r2);
                                 const float4* src = reinterpret_cast<const float4*>(
                                     prm.part_o + ((int64_t)sl * 128 + r2) * D + c8 * 8);
@@ -562,25 +677,13 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                                 m8[4] = m8[4] * sa + sb * x1.x; m8[5] = m8[5] * sa + sb * x1.y;
                                 m8[6] = m8[6] * sa + sb * x1.z; m8[7] = m8[7] * sa + sb * x1.w;
                             }
-                            const float inv = tot > 0.f ? 1.f / tot : 0.f;
                             const int64_t orow =
                                 ((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G;
-                            uint4 w4;
-                            w4.x = pack_bf16x2(m8[0] * inv, m8[1] * inv);
-                            w4.y = pack_bf16x2(m8[2] * inv, m8[3] * inv);
-                            w4.z = pack_bf16x2(m8[4] * inv, m8[5] * inv);
-                            w4.w = pack_bf16x2(m8[6] * inv, m8[7] * inv);
-                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
-                                                      c8 * 8) = w4;
+                            store_out(orow, c8, m8, tot > 0.f ? 1.f / tot : 0.f);
                             if (c8 == 0 && a.lse) a.lse[orow] = tot > 0.f ? mx + logf(tot) : -INFINITY;
                         }
-                        if (tid == 0) a.seg_counters[seg] = 0;  // ready for the next call
+                        if (lane == 0) a.seg_counters[seg] = 0;  // ready for the next call
                     }
-                }
-                named_bar_sync(1, NW * 32);  // every read of the staged O is done
-                if (refill && ok) {
-                    if (lane == 0) issue(s, ahead, pg_next);
-                    pending |= 1u << s;
                 }
             }
             if (it + NS + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
@@ -595,6 +698,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             for (int j = q_issued - 2; j < q_issued; ++j)
                 if (j >= 0) mbar_drain(&bars[Smem::B_QFULL + (j & 1)], (j >> 1) & 1);
         }
+        cp_async_wait<0>();  // a prefetch an abort left unconsumed
     }
     __syncthreads();
 }
