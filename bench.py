@@ -221,7 +221,9 @@ def workload_config(inp, l2_note):
     return {"workload": s.name, "batch": s.batch, "q_heads": s.num_q_heads,
             "kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "ctx": ctx,
             "num_draft": s.num_draft, "page_size": s.page_size, "vocab": s.vocab,
-            "kv_dtype": s.kv_dtype, "seed": inp.seed, "l2": l2_note, "parallelism": "replicas"}
+            "kv_dtype": s.kv_dtype, "seed": inp.seed, "l2": l2_note,
+            "queue": "prefilled (spin kernel while the host enqueues the timed steps)",
+            "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------- GPU run
@@ -269,6 +271,11 @@ def run_gpu(args, inp, world, rank, local):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        # hold the stream with a spin kernel while the host enqueues every
+        # timed step, so no interval includes host submission time (the e2e
+        # figure below keeps the host in the loop)
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(min(2e8, 1e5 * args.steps)))
         for j in range(args.steps):
             t, o = sets[j % n_sets], outs[j % n_sets]
             ev[j][0].record(stream)
