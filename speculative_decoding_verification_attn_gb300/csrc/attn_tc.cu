@@ -843,25 +843,38 @@ combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
     // CTA c covers tiles [c*T/C, (c+1)*T/C); a CTA with an empty range wrote
     // nothing and is skipped
     auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
+    auto slot_of = [&](int c) { return 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1); };
+    // log-sum-exp of the pieces' lse: one piece per lane, all loads in flight
     float m = -INFINITY;
-    for (int c = c_first; c <= c_last; ++c) {
-        if (empty(c)) continue;
-        const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
-        m = fmaxf(m, part_lse[(int64_t)slot * ROWS + row]);
+    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
+        const int c = c0 + lane;
+        const bool use = c <= c_last && !empty(c);
+        const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
+        m = fmaxf(m, lw);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float tsum = 0.f;
-    for (int c = c_first; c <= c_last; ++c) {
-        if (empty(c)) continue;
-        const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
-        tsum += expf(part_lse[(int64_t)slot * ROWS + row] - m);
+    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
+        const int c = c0 + lane;
+        const bool use = c <= c_last && !empty(c);
+        const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
+        if (lw != -INFINITY) tsum += expf(lw - m);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
     const float lse_tot = m + logf(tsum);
+    // weighted O rows: lane -> 4 columns; the loads of consecutive pieces are
+    // independent, so the unrolled loop keeps several in flight
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int c = c_first; c <= c_last; ++c) {
-        if (empty(c)) continue;
-        const int slot = 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1);
-        const float w = expf(part_lse[(int64_t)slot * ROWS + row] - lse_tot);
-        const float4 v = reinterpret_cast<const float4*>(part_o + ((int64_t)slot * ROWS + row) * D)[lane];
+        const bool use = !empty(c);
+        const int slot = slot_of(c);
+        const float lw = use ? __ldg(part_lse + (int64_t)slot * ROWS + row) : -INFINITY;
+        const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)slot * ROWS + row) * D);
+        const float4 v = use ? __ldg(src + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float w = lw == -INFINITY ? 0.f : expf(lw - lse_tot);
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
