@@ -52,8 +52,6 @@ constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
-// warps: softmax 0-3, Q K^T halves 4-5, P V 6, TMA producer 7, K relayout 8
-constexpr int THREADS = 9 * 32;
 // TMEM columns: partial scores of head-dim half 0 / 1, double buffered,
 // SA [0,128) SB [128,256); O [256,384); P0 [384,416) P1 [416,448);
 // Q [448,512) (bf16 pairs)
@@ -65,20 +63,48 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr uint32_t IDESC_PV = umma_idesc_bf16(ROWS, D, 0, 1);   // B (V) MN-major
+// INT8 cache: raw boxes (16 keys x 128 int8 = 2 KB per tensor) and their
+// fp16 scales land in NSR stages; four converter warps widen each tile into
+// one of NCV fp16 operand stages.
+constexpr int NSR = 6;
+constexpr int NCV = 2;
+constexpr int RAW8_KV = TN * D;                       // 8 KB of int8 per tensor per tile
+constexpr int RAW8_STAGE = 2 * RAW8_KV + 2 * TN * 2;  // K, V, then k / v scales (fp16)
+
+// A / B operand formats of tcgen05.mma kind::f16 (bf16 cache: bf16; INT8
+// cache widened to fp16, so q and P are fp16 there too)
+template <bool KV8>
+__host__ __device__ constexpr uint32_t idesc_qk() {
+    return KV8 ? umma_idesc_f16(ROWS, TN, 0, 0) : umma_idesc_bf16(ROWS, TN, 0, 0);
+}
+template <bool KV8>
+__host__ __device__ constexpr uint32_t idesc_pv() {  // B (V) MN-major
+    return KV8 ? umma_idesc_f16(ROWS, D, 0, 1) : umma_idesc_bf16(ROWS, D, 0, 1);
+}
 using Cursor = CursorT<TN>;
 
-struct Smem {
-    // offsets from the 1024-aligned base
-    static constexpr int Q = 0;                                // one Q staging buffer
+// Shared-memory plan (offsets from the 1024-aligned base).  bf16 cache: TMA
+// boxes land directly in NS operand stages [K 16 KB | V 16 KB].  INT8 cache:
+// boxes land in NSR raw stages, converted tiles go to NCV operand stages,
+// with one fp32 row of per-key k / v scales per operand stage.
+template <bool KV8>
+struct SmemT {
+    static constexpr int NL = KV8 ? NSR : NS;  // stages TMA lands in
+    static constexpr int NM = KV8 ? NCV : NS;  // stages the MMAs read
+    static constexpr int Q = 0;                // one Q staging buffer
     static constexpr int STAGES = Q + Q_BYTES;
-    static constexpr int SCRATCH = STAGES + NS * STAGE_BYTES;
-    static constexpr int BARS = SCRATCH + SCRATCH_BYTES;
-    // barriers (uint64 each)
-    static constexpr int B_KVFULL = 0, B_KREADY = NS, B_KVEMPTY = 2 * NS, B_QFULL = 3 * NS,
-                         B_QFREE = 3 * NS + 1, B_SFULL = 3 * NS + 2, B_PFULL = 3 * NS + 4,
-                         B_ODONE = 3 * NS + 6, B_DRAIN = 3 * NS + 8, B_QCP = 3 * NS + 11,
-                         NUM_BARS = 3 * NS + 13;
+    static constexpr int RAW = KV8 ? STAGES + NM * STAGE_BYTES : STAGES;
+    static constexpr int RAW_STAGE = KV8 ? RAW8_STAGE : STAGE_BYTES;
+    static constexpr int SCRATCH = RAW + NL * RAW_STAGE;
+    static constexpr int SCALES = SCRATCH + SCRATCH_BYTES;  // [NM][k, v][TN] float
+    static constexpr int BARS = SCALES + (KV8 ? NM * 2 * TN * 4 : 0);
+    // barriers (uint64 each): landed (TMA), operands ready (K relayout /
+    // INT8 conversion), operand stage free (P V done), raw stage free (INT8)
+    static constexpr int B_KVFULL = 0, B_KREADY = NL, B_KVEMPTY = NL + NM,
+                         B_RAWFREE = KV8 ? NL + 2 * NM : B_KVEMPTY,
+                         B_QFULL = (KV8 ? 2 * NL : NL) + 2 * NM, B_QFREE = B_QFULL + 1,
+                         B_SFULL = B_QFULL + 2, B_PFULL = B_QFULL + 4, B_ODONE = B_QFULL + 6,
+                         B_DRAIN = B_QFULL + 8, B_QCP = B_QFULL + 11, NUM_BARS = B_QFULL + 13;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
     static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
     static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
@@ -86,8 +112,16 @@ struct Smem {
     static constexpr int PRE = CTX + MAX_BATCH * 4;           // [MAX_BATCH+1] int
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
 };
-constexpr size_t SMEM_BYTES = Smem::END + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+template <bool KV8>
+constexpr size_t smem_bytes() { return SmemT<KV8>::END + 1024; }  // + alignment slack
+static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory budget (bf16)");
+static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory budget (INT8)");
+static_assert(SmemT<true>::RAW % 128 == 0 && RAW8_STAGE % 128 == 0, "TMA destination alignment");
+// warps: softmax 0-3, Q K^T halves 4-5, P V 6, TMA producer 7, then K relayout
+// (bf16: warp 8) or INT8 conversion (warps 8-11)
+template <bool KV8>
+__host__ __device__ constexpr int threads() { return KV8 ? 12 * 32 : 9 * 32; }
+
 
 struct TcParams {
     AttnArgs a;
@@ -146,8 +180,14 @@ __device__ __forceinline__ void store_cols(uint32_t taddr, const uint32_t* v) {
 }
 
 // ================= softmax / rescale / epilogue (warps 0-3) =================
-template <int REP>
+// INT8 cache: S holds q . c_j (c_j the stored integers, exact in fp16); the
+// key's scale turns it into the score (s_j = scale * s_k,j * S_j, s_k,j
+// pre-multiplied by scale*log2(e) in the operand stage), and P V takes
+// p_j * s_v,j, so that O = sum_j p_j s_v,j c_j = sum_j p_j v_j while the row
+// sum keeps the plain p_j.
+template <int REP, bool KV8>
 __device__ void softmax_role(const Cta& x) {
+    using Smem = SmemT<KV8>;
     constexpr int RQ = REP == 4 ? 32 : REP == 2 ? 64 : ROWS;
     constexpr int CW = TN / REP;  // key columns of a tile owned by one copy
     const AttnArgs& a = *x.a;
@@ -199,12 +239,17 @@ __device__ void softmax_role(const Cta& x) {
                 sr[cc] = __float_as_uint(__uint_as_float(sr[cc]) + __uint_as_float(sr2[cc]));
             // keys of this row visible in this copy's slice: cc < cmax
             const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
+            // INT8: per-key fp32 scales of this operand stage (k row, then v row)
+            const float* sc_k = reinterpret_cast<const float*>(
+                x.sm + Smem::SCALES + (it % Smem::NM) * 2 * TN * 4) + cbase;
+            const float* sc_v = sc_k + TN;
             // branch-free: masked scores become -inf (exp2 -> 0)
             float v[CW];
             float mt = -INFINITY;
 #pragma unroll
             for (int cc = 0; cc < CW; ++cc) {
-                v[cc] = cc < cmax ? __uint_as_float(sr[cc]) * sl2 : -INFINITY;
+                const float f = KV8 ? sc_k[cc] : sl2;
+                v[cc] = cc < cmax ? __uint_as_float(sr[cc]) * f : -INFINITY;
                 mt = fmaxf(mt, v[cc]);
             }
             const float m_new = fmaxf(m_ref, mt);
@@ -224,7 +269,10 @@ __device__ void softmax_role(const Cta& x) {
                 const float p1 = fast_exp2(v[2 * c2 + 1] - m_use);
                 psum0 += p0;
                 psum1 += p1;
-                pk[c2] = pack_bf16x2(p0, p1);
+                if constexpr (KV8)
+                    pk[c2] = pack_f16x2(p0 * sc_v[2 * c2], p1 * sc_v[2 * c2 + 1]);
+                else
+                    pk[c2] = pack_bf16x2(p0, p1);
             }
             l += psum0 + psum1;
             // P buffer sb is free once P V(it-2) has finished.  P V of tile j
@@ -258,11 +306,11 @@ __device__ void softmax_role(const Cta& x) {
                 }
             }
         }
-        if (ok && nvalid % BH != 0 && warp == 0) {
+        if (!KV8 && ok && nvalid % BH != 0 && warp == 0) {
             // keys past the sequence end inside its last page: zero their V
             // rows so that 0 * (stale or canary) never reaches O
             ok = warp_wait(&bars[Smem::B_KVFULL + it % NS], (it / NS) & 1, x.abort_flag,
-                           a.dev_err);
+                           a.dev_err);  // bf16: landing stage == operand stage
             if (ok) {
                 uint8_t* vst = x.sm + Smem::STAGES + (it % NS) * STAGE_BYTES + KV_BYTES;
                 const int bx = nvalid / BH, r_end = BH;
@@ -433,9 +481,40 @@ __device__ void softmax_role(const Cta& x) {
     }
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// Widens 16 int8 (one 16-byte chunk) to 16 fp16 (two chunks), exactly: the
+// byte u = c + 128 placed under the fp16 exponent of 1024 reads as 1024 + u,
+// and subtracting 1152 leaves c (every step exact in fp16).
+__device__ __forceinline__ void i8x16_to_f16(const uint4 r, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {r.x ^ 0x80808080u, r.y ^ 0x80808080u, r.z ^ 0x80808080u,
+                           r.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t e01 = __byte_perm(w[i], 0x64646464u, 0x4140);
+        const uint32_t e23 = __byte_perm(w[i], 0x64646464u, 0x4342);
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i]) : "r"(e01), "r"(0x64806480u));
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i + 1]) : "r"(e23), "r"(0x64806480u));
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// bf16 -> fp16 in place (8 values per 16-byte chunk), round to nearest even.
+__device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 r) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <bool KV8>
+__global__ void __launch_bounds__(threads<KV8>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const TcParams prm) {
+    using Smem = SmemT<KV8>;
+    constexpr int NL = Smem::NL, NM = Smem::NM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -454,9 +533,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     // ---- setup: barriers, TMEM, zero Q pad rows, per-sequence tile prefix
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NL; ++s) {
             mbar_init(&bars[Smem::B_KVFULL + s], 1);
-            mbar_init(&bars[Smem::B_KREADY + s], 1);
+            if (KV8) mbar_init(&bars[Smem::B_RAWFREE + s], 4);  // one per converter warp
+        }
+        for (int s = 0; s < NM; ++s) {
+            mbar_init(&bars[Smem::B_KREADY + s], KV8 ? 4 : 1);
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
         mbar_init(&bars[Smem::B_QFULL], 1);
@@ -478,7 +560,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     {
         // rows that hold no query stay zero in both Q buffers
         uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
-        for (int e = tid; e < Q_BYTES / 16; e += THREADS) {
+        for (int e = tid; e < Q_BYTES / 16; e += threads<KV8>()) {
             const int row = (e % (Q_HALF / 16)) / 8;
             if (!q_row_used(row, R, RQ, REP)) q4[e] = make_uint4(0, 0, 0, 0);
         }
@@ -587,30 +669,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
             }
-            const int s = it % NS, use = it / NS;
+            const int s = it % NL, use = it / NL;
             const int key0 = cur.lt * TN;
             const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
             const int nbox = (nvalid + BH - 1) / BH;
             if (lane == 0) {
+                // bf16: the stage is free once P V has read it; INT8: once the
+                // converter warps have widened it
                 if (use >= 1)
-                    ok = mbar_wait(&bars[Smem::B_KVEMPTY + s], (use - 1) & 1, abort_flag,
+                    ok = mbar_wait(&bars[Smem::B_RAWFREE + s], (use - 1) & 1, abort_flag,
                                    a.dev_err);
-                if (ok) mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s], 2u * nbox * BH * 256);
+                if (ok)
+                    mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
+                                          KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
+                                              : 2u * nbox * BH * 256);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (lane < 2 * nbox) {
-                const int tensor = lane & 1, bx = lane >> 1;
+            if (lane < (KV8 ? 4 : 2) * nbox) {
+                const int bx = KV8 ? lane >> 2 : lane >> 1;
                 int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
                 if (page < 0 || page >= a.num_pages) {
                     raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
                     page = 0;
                 }
                 const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BH) % P;
-                tma_load_3d_hint(sm + Smem::STAGES + s * STAGE_BYTES + tensor * KV_BYTES +
-                                     bx * BH * 256,
-                                 tensor ? (const void*)&vmap : (const void*)&kmap,
-                                 &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
+                uint8_t* st = sm + Smem::RAW + s * Smem::RAW_STAGE;
+                if constexpr (KV8) {
+                    // lane & 3: K box, V box (16 rows x 128 int8), k / v scales (16 fp16)
+                    const int what = lane & 3;
+                    if (what < 2)
+                        tma_load_2d(st + what * RAW8_KV + bx * BH * D,
+                                    what ? (const void*)&vmap : (const void*)&kmap,
+                                    &bars[Smem::B_KVFULL + s], 0, row, pol);
+                    else
+                        bulk_load(st + 2 * RAW8_KV + (what - 2) * TN * 2 + bx * BH * 2,
+                                  (what == 2 ? a.k_scale : a.v_scale) + row, BH * 2,
+                                  &bars[Smem::B_KVFULL + s]);
+                } else {
+                    const int tensor = lane & 1;
+                    tma_load_3d_hint(st + tensor * KV_BYTES + bx * BH * 256,
+                                     tensor ? (const void*)&vmap : (const void*)&kmap,
+                                     &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
+                }
             }
             n_issued = it + 1;
             __syncwarp();
@@ -619,13 +720,73 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         cp_async_wait<0>();
         if (!ok && lane == 0) {
             // drain: wait (bounded) for the copies this CTA issued
-            for (int s = 0; s < NS; ++s) {
-                const int uses = n_issued > s ? (n_issued - 1 - s) / NS + 1 : 0;
+            for (int s = 0; s < NL; ++s) {
+                const int uses = n_issued > s ? (n_issued - 1 - s) / NL + 1 : 0;
                 if (uses > 0) mbar_drain(&bars[Smem::B_KVFULL + s], (uses - 1) & 1);
             }
             if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
         }
-    } else if (warp == 8) {
+    } else if (KV8 && warp >= 8) {
+        // ================= INT8 widening (warps 8-11) =================
+        // Raw stage -> operand stage: K lands in the relayouted order the N = 64
+        // Q K^T reads (8-key groups 2 KB apart), V in the box order of P V
+        // (16-key boxes 4 KB apart), both as fp16 with the 128-byte swizzle;
+        // the per-key scales become fp32 rows (k pre-multiplied by
+        // scale*log2(e)), zero past the sequence end.  Whole 16-key boxes are
+        // widened; keys past the end hold finite values that P = 0 cancels.
+        const int ct = tid - 8 * 32;  // 0..127
+        const float sl2 = a.scale * kLog2e;
+        Cursor cur;
+        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            const int s = it % NL, m = it % NM;
+            const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
+            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
+            ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NL) & 1, abort_flag, a.dev_err);
+            // the operand stage is free once P V of tile it - NM has finished
+            if (ok && it >= NM)
+                ok = warp_wait(&bars[Smem::B_KVEMPTY + m], ((it / NM) - 1) & 1, abort_flag,
+                               a.dev_err);
+            if (!ok) break;
+            const uint8_t* raw = sm + Smem::RAW + s * Smem::RAW_STAGE;
+            uint8_t* kc = sm + Smem::STAGES + m * STAGE_BYTES;
+            uint8_t* vc = kc + KV_BYTES;
+            for (int id = ct; id < nbox * BOX_ROWS * 8; id += 128) {
+                // 16-byte chunk c16 (head-dim 16*c16 .. +15) of key j
+                const int j = id >> 3, c16 = id & 7, h = c16 >> 2, sw = j & 7;
+                const uint4 rk = *reinterpret_cast<const uint4*>(raw + id * 16);
+                const uint4 rv = *reinterpret_cast<const uint4*>(raw + RAW8_KV + id * 16);
+                uint4 k0, k1, v0, v1;
+                i8x16_to_f16(rk, k0, k1);
+                i8x16_to_f16(rv, v0, v1);
+                // fp16 chunks cc, cc+1 of half h; lanes of half 1 store their
+                // odd chunk first so that 8 consecutive lanes hit 8 bank groups
+                const int cc = (c16 & 3) * 2;
+                const int o0 = ((cc + h) ^ sw) << 4, o1 = ((cc + 1 - h) ^ sw) << 4;
+                uint8_t* kr = kc + (j >> 3) * 2048 + h * 1024 + (j & 7) * 128;
+                uint8_t* vr = vc + (j >> 4) * 4096 + h * 2048 + (j & 15) * 128;
+                *reinterpret_cast<uint4*>(kr + o0) = h ? k1 : k0;
+                *reinterpret_cast<uint4*>(kr + o1) = h ? k0 : k1;
+                *reinterpret_cast<uint4*>(vr + o0) = h ? v1 : v0;
+                *reinterpret_cast<uint4*>(vr + o1) = h ? v0 : v1;
+            }
+            {
+                const int j = ct & (TN - 1), which = ct >> 6;  // 0: k scales, 1: v scales
+                const __half hs =
+                    reinterpret_cast<const __half*>(raw + 2 * RAW8_KV + which * TN * 2)[j];
+                const float f = j < nvalid ? __half2float(hs) * (which ? 1.f : sl2) : 0.f;
+                reinterpret_cast<float*>(sm + Smem::SCALES + m * 2 * TN * 4)[which * TN + j] = f;
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[Smem::B_RAWFREE + s]);
+                mbar_arrive(&bars[Smem::B_KREADY + m]);
+            }
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+    } else if (!KV8 && warp == 8) {
         // ================= K relayout (warp 8) =================
         // A K box lands as [h0 rows 0-7 | h0 rows 8-15 | h1 rows 0-7 | h1 rows
         // 8-15] (1 KB blocks, 128-byte swizzle).  Swapping the middle blocks
@@ -664,16 +825,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // split by head-dim half into two partial score buffers (the softmax
         // adds them), and P V.
         //
-        // K arrives relayouted by warp 8 (8-key groups 2 KB apart, one uniform
-        // stride for an N = 64 MMA); V keeps the box layout and P V runs one
-        // K = 16 MMA per box.
+        // K arrives relayouted by warp 8 (INT8: widened by warps 8-11) with
+        // 8-key groups 2 KB apart, one uniform stride for an N = 64 MMA; V
+        // keeps the box layout and P V runs one K = 16 MMA per box.
         const int role = warp - 4;  // 0, 1: Q K^T head-dim half; 2: P V
         if (n_tiles > 0) {
             Cursor cur;
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             int pc = -1;
             bool ok = true;
-            const uint32_t idesc_qk = umma_idesc_bf16(ROWS, TN, 0, 0);
+            constexpr uint32_t kIdescQK = idesc_qk<KV8>(), kIdescPV = idesc_pv<KV8>();
             // smem descriptors are built once; an operand's start address
             // lives in the low 14 bits (in 16-byte units), so stepping to
             // another k-slice, box or stage is one 64-bit add
@@ -684,7 +845,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             for (int it = 0; it < n_tiles && ok; ++it) {
                 const bool first = (it == 0) || (cur.lt == 0);
                 if (first) ++pc;
-                const int s = it % NS, sb = it & 1;
+                const int s = it % NM, sb = it & 1;
                 const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
                 const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
                 if (role < 2) {
@@ -700,9 +861,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                            a.dev_err);
                         }
                     }
-                    // K of tile it landed and was relayouted (warp 8)
+                    if (KV8 && first && ok) {
+                        // this half of the piece's Q to fp16, in place (the
+                        // MMAs read fp16 operands when the cache is INT8)
+                        uint4* qh = reinterpret_cast<uint4*>(sm + Smem::Q + h * Q_HALF);
+#pragma unroll 4
+                        for (int e = lane; e < Q_HALF / 16; e += 32) qh[e] = bf16x8_to_f16(qh[e]);
+                        fence_proxy_async_smem();
+                    }
+                    // K of tile it landed and was relayouted / widened
                     if (ok)
-                        ok = warp_wait(&bars[Smem::B_KREADY + s], (it / NS) & 1, abort_flag,
+                        ok = warp_wait(&bars[Smem::B_KREADY + s], (it / NM) & 1, abort_flag,
                                        a.dev_err);
                     // S buffer sb is free once the softmax has read tile it-2
                     if (ok && it >= 2)
@@ -729,7 +898,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const uint32_t dcol = tmem + (h ? TM_SB : TM_S) + sb * TN;
 #pragma unroll
                         for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-                            umma_ts(dcol, tmem + TM_Q + kk * 8, kd + (kk & 3) * 2, idesc_qk,
+                            umma_ts(dcol, tmem + TM_Q + kk * 8, kd + (kk & 3) * 2, kIdescQK,
                                     (kk & 3) ? 1u : 0u);
                         umma_commit(&bars[Smem::B_SFULL + sb]);
                     }
@@ -738,9 +907,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     // O += P V over the first nbox boxes of tile it (the rest are
                     // past the sequence end and hold no probability mass)
                     ok = warp_wait(&bars[Smem::B_PFULL + sb], (it >> 1) & 1, abort_flag, a.dev_err);
+                    // V landed (bf16) / was widened (INT8)
                     if (ok)
-                        ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag,
-                                       a.dev_err);
+                        ok = warp_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_KVFULL + s],
+                                       (it / NM) & 1, abort_flag, a.dev_err);
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
@@ -751,7 +921,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         for (int bx = 0; bx < MAX_BOX; ++bx)
                             if (bx < nbox)
                                 umma_ts(tmem + TM_O, pcol + bx * (BOX_ROWS / 2),
-                                        vd + ((bx * BOX_ROWS * 256) >> 4), IDESC_PV,
+                                        vd + ((bx * BOX_ROWS * 256) >> 4), kIdescPV,
                                         (bx > 0 || !first) ? 1u : 0u);
                         umma_commit(&bars[Smem::B_KVEMPTY + s]);
                         umma_commit(&bars[Smem::B_ODONE + sb]);
@@ -783,9 +953,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         x.R = R;
         x.G = G;
         x.BH = BH;
-        if (REP == 4) softmax_role<4>(x);
-        else if (REP == 2) softmax_role<2>(x);
-        else softmax_role<1>(x);
+        if (REP == 4) softmax_role<4, KV8>(x);
+        else if (REP == 2) softmax_role<2, KV8>(x);
+        else softmax_role<1, KV8>(x);
     }
 
     tc_fence_before();
@@ -914,7 +1084,14 @@ EncodeTiledFn get_encode_fn() {
 bool tc_supported(const AttnArgs& a) {
     const int G = a.Hq / a.Hkv;
     const bool pow2 = (a.P & (a.P - 1)) == 0;
-    return a.q_dtype == SPEC_DTYPE_BF16 && a.kv_dtype == SPEC_DTYPE_BF16 && a.D == D &&
+    // INT8 cache: the scales are fetched 16 keys (32 bytes) at a time with
+    // bulk copies, which need 16-byte aligned sources
+    const bool kv_ok =
+        a.kv_dtype == SPEC_DTYPE_BF16 ||
+        (a.kv_dtype == SPEC_DTYPE_I8 && a.k_scale && a.v_scale &&
+         (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(a.v_scale) & 15) == 0);
+    return a.q_dtype == SPEC_DTYPE_BF16 && kv_ok && a.D == D &&
            a.k * G <= ROWS && G <= 256 && pow2 && a.P >= 16 && a.P <= 256 && a.B <= MAX_BATCH &&
            (int64_t)a.num_pages * a.Hkv * a.P < (1LL << 31) && (int64_t)a.B * a.k < (1LL << 31);
 }
@@ -941,10 +1118,24 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
             return cudaErrorInvalidValue;
     }
     // K/V: [rows = num_pages*Hkv*P] x [2 halves] x [64 columns]; one box =
-    // BH consecutive rows of one page, both halves
+    // BH consecutive rows of one page, both halves.  INT8: [rows] x [128
+    // bytes], one unswizzled box of BH rows (the converter warps swizzle)
     const int BH = BOX_ROWS;
     const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
-    for (int t = 0; t < 2; ++t) {
+    const bool kv8 = a.kv_dtype == SPEC_DTYPE_I8;
+    for (int t = 0; t < 2 && kv8; ++t) {
+        cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+        cuuint64_t strides[1] = {(cuuint64_t)D};
+        cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)BH};
+        cuuint32_t es[2] = {1, 1};
+        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int t = 0; t < 2 && !kv8; ++t) {
         cuuint64_t dims[3] = {64, rows, 2};
         cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
         cuuint32_t box[3] = {64, (cuuint32_t)BH, 2};
@@ -960,11 +1151,21 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
     prm.a = a;
     prm.part_o = static_cast<float*>(workspace);
     prm.part_lse = prm.part_o + (size_t)2 * num_ctas * ROWS * D;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attn_tc_kernel<<<num_ctas, THREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, prm);
+    cudaError_t e;
+    if (kv8) {
+        e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes<true>());
+        if (e != cudaSuccess) return e;
+        attn_tc_kernel<true><<<num_ctas, threads<true>(), smem_bytes<true>(), stream>>>(
+            qmap, kmap, vmap, prm);
+    } else {
+        e = cudaFuncSetAttribute(attn_tc_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes<false>());
+        if (e != cudaSuccess) return e;
+        attn_tc_kernel<false><<<num_ctas, threads<false>(), smem_bytes<false>(), stream>>>(
+            qmap, kmap, vmap, prm);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, stream);

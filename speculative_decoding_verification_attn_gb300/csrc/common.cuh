@@ -303,6 +303,16 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn_ma
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// Same for fp16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn_major,
+                                                      int b_mn_major) {
+    return (1u << 4)                          // D format: f32
+           | ((uint32_t)a_mn_major << 15)     // A major
+           | ((uint32_t)b_mn_major << 16)     // B major
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
 // Shared-memory matrix descriptor (tcgen05 format), 128-byte swizzle.
 //   start: smem byte address; lbo / sbo: leading / stride byte offsets.
 __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t start, uint32_t lbo, uint32_t sbo) {
@@ -354,6 +364,12 @@ struct CursorT {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {

@@ -69,6 +69,68 @@ def test_tensor_core_stream_k_splits(oracle_mod, ctas):
     check_attn_full(oracle_mod, inp, "ctas=%d" % ctas)
 
 
+SMALL_I8 = [
+    dict(kv_dtype="i8"),                                                  # 16 rows
+    dict(kv_dtype="i8", num_q_heads=4, num_kv_heads=4, num_draft=1),      # 1 row per kv-head
+    dict(kv_dtype="i8", num_q_heads=16, num_kv_heads=2, num_draft=8),     # 64 rows
+    dict(kv_dtype="i8", num_q_heads=28, num_kv_heads=4, num_draft=16, page_size=32),  # 112
+    dict(kv_dtype="i8", num_q_heads=4, num_kv_heads=2, num_draft=64),     # 128 rows
+    dict(kv_dtype="i8", ctx=[0, 1, 63, 64, 65], batch=5, num_draft=3),    # tile edges
+    dict(kv_dtype="i8", page_size=64, ctx=(1, 400)),
+    dict(kv_dtype="i8", page_size=256, ctx=(250, 700), batch=2),
+    dict(kv_dtype="i8", batch=1, num_q_heads=8, num_kv_heads=1, ctx=[3000]),
+]
+
+
+@pytest.mark.parametrize("kw", SMALL_I8, ids=[str(i) for i in range(len(SMALL_I8))])
+def test_tensor_core_int8_small(oracle_mod, kw):
+    # INT8 cache widened to fp16 on chip; scales folded into scores and P
+    inp = make_inputs(small_spec(**kw), seed=41)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    check_attn_full(oracle_mod, inp, "i8 %s" % kw)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 37, 152, 400])
+def test_tensor_core_int8_stream_k_splits(oracle_mod, ctas):
+    inp = make_inputs(small_spec(batch=4, num_q_heads=32, num_kv_heads=4, num_draft=8,
+                                 kv_dtype="i8", ctx=(0, 900)), seed=42)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
+    check_attn_full(oracle_mod, inp, "i8 ctas=%d" % ctas)
+
+
+def test_tensor_core_int8_matches_simt():
+    inp = make_inputs(small_spec(batch=5, num_q_heads=24, num_kv_heads=4, num_draft=6,
+                                 kv_dtype="i8", ctx=(0, 700)), seed=43)
+    t = binding.inputs_to_torch(inp)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    a_out, a_lse = gpu_attn(inp, t)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 1)
+    b_out, b_lse = gpu_attn(inp, t)
+    assert np.abs(a_out - b_out).max() < 2e-2
+    assert np.abs(a_lse - b_lse).max() < 2e-3
+
+
+def test_int8_unaligned_scales_use_simt(oracle_mod):
+    # scale arrays that are not 16-byte aligned cannot feed the bulk copies of
+    # the tensor-core kernel: the automatic path runs the SIMT kernel, a
+    # forced tensor-core path is refused
+    inp = make_inputs(small_spec(kv_dtype="i8", num_q_heads=16, num_kv_heads=2, num_draft=8),
+                      seed=44)
+    t = binding.inputs_to_torch(inp)
+    for key in ("k_scale", "v_scale"):
+        flat = torch.empty(t[key].numel() + 8, dtype=t[key].dtype, device="cuda")
+        shifted = flat[1:1 + t[key].numel()].view(t[key].shape)
+        shifted.copy_(t[key])
+        t[key] = shifted
+    out, lse = gpu_attn(inp, t)
+    ref_out, ref_lse = oracle_attn(oracle_mod, inp)
+    assert_attn_close(out, lse, ref_out, ref_lse, tol_for(inp), "unaligned scales")
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    with pytest.raises(binding.SpecError, match="does not support"):
+        gpu_attn(inp, t)
+
+
 @pytest.mark.parametrize("kw", [
     dict(),
     dict(kv_dtype="i8"),
