@@ -22,11 +22,14 @@
 //    walks a contiguous tile range that may cross segment boundaries; a
 //    segment cut by a range boundary leaves (O/l, lse) partials that the
 //    combine kernel merges with log-sum-exp weights (split-KV).
-//  * Warp roles: warp 4 = TMA producer (page-table driven: one 2-D box per
-//    (page, head-dim half)), warp 5 = MMA issuer and TMEM owner, warps 0-3 =
-//    softmax / rescale / epilogue, one (copy, query row) per thread.
-//  * S = Q K^T lands in TMEM (double buffered), the softmax warps turn it into
-//    bf16 P in place, and O += P V takes P straight from TMEM.  The running
+//  * Warp roles: 0-3 softmax / rescale / epilogue / P V issue (one (copy,
+//    query row) per thread), 4 Q K^T issue, 5 and 7 idle, 6 TMA producer
+//    (page-table driven), 8-11 a second set of softmax warps taking every
+//    other tile with an O of its own (bf16 cache, one copy) or the INT8
+//    widening warps.
+//  * S = Q K^T lands in one of two TMEM buffers (freed as soon as the
+//    softmax has loaded it), the softmax warps write bf16 P to TMEM, and
+//    O += P V takes P from there.  The running
 //    max only moves when it grows by more than 2^8, so O is rarely rescaled
 //    (exact in real arithmetic: O and l share the reference max), and a tile's
 //    P is released without waiting for the previous tile's P V.
@@ -52,11 +55,12 @@ constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
 constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
-// TMEM columns: partial scores of head-dim half 0 / 1, double buffered,
-// SA [0,128) SB [128,256); O [256,384); P0 [384,416) P1 [416,448);
-// Q [448,512) (bf16 pairs)
+// TMEM columns: S buffers [0,128) (2 x 64 fp32); O [128,256) and, for the
+// second softmax set, [256,384); P0 [384,416) P1 [416,448) (bf16 pairs); Q
+// [448,512) (bf16 pairs)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0, TM_SB = 128, TM_O = 256, TM_P = 384, TM_Q = 448;
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 384, TM_Q = 448;
+constexpr int NSB = 2;  // S buffers (ping-pong: one per softmax warp set)
 constexpr int MAX_BATCH = 1024;
 constexpr int SCRATCH_BYTES = 16 * 1024;  // copy-merge buffer of the epilogue
 constexpr float kLog2e = 1.4426950408889634f;
@@ -98,13 +102,14 @@ struct SmemT {
     static constexpr int SCRATCH = RAW + NL * RAW_STAGE;
     static constexpr int SCALES = SCRATCH + SCRATCH_BYTES;  // [NM][k, v][TN] float
     static constexpr int BARS = SCALES + (KV8 ? NM * 2 * TN * 4 : 0);
-    // barriers (uint64 each): landed (TMA), operands ready (K relayout /
-    // INT8 conversion), operand stage free (P V done), raw stage free (INT8)
+    // barriers (uint64 each): landed (TMA), operands ready (INT8 widening),
+    // operand stage free (P V done), raw stage free (INT8)
     static constexpr int B_KVFULL = 0, B_KREADY = NL, B_KVEMPTY = NL + NM,
                          B_RAWFREE = KV8 ? NL + 2 * NM : B_KVEMPTY,
                          B_QFULL = (KV8 ? 2 * NL : NL) + 2 * NM, B_QFREE = B_QFULL + 1,
-                         B_SFULL = B_QFULL + 2, B_PFULL = B_QFULL + 4, B_ODONE = B_QFULL + 6,
-                         B_DRAIN = B_QFULL + 8, B_QCP = B_QFULL + 11, NUM_BARS = B_QFULL + 13;
+                         B_SFULL = B_QFULL + 2, B_SFREE = B_SFULL + NSB, B_ODONE = B_SFREE + NSB,
+                         B_DRAIN = B_ODONE + 2, B_QCP = B_DRAIN + 3,
+                         NUM_BARS = B_QCP + 1;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
     static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
     static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
@@ -117,10 +122,11 @@ constexpr size_t smem_bytes() { return SmemT<KV8>::END + 1024; }  // + alignment
 static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory budget (bf16)");
 static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory budget (INT8)");
 static_assert(SmemT<true>::RAW % 128 == 0 && RAW8_STAGE % 128 == 0, "TMA destination alignment");
-// warps: softmax 0-3, Q K^T halves 4-5, P V 6, TMA producer 7, then K relayout
-// (bf16: warp 8) or INT8 conversion (warps 8-11)
+// warps: softmax and P V issue 0-3, Q K^T 4, TMA producer 6 (5 and 7 idle),
+// then a second set of softmax warps 8-11 (bf16) or the INT8 widening warps
+// 8-11
 template <bool KV8>
-__host__ __device__ constexpr int threads() { return KV8 ? 12 * 32 : 9 * 32; }
+__host__ __device__ constexpr int threads() { return 12 * 32; }
 
 
 struct TcParams {
@@ -179,19 +185,29 @@ __device__ __forceinline__ void store_cols(uint32_t taddr, const uint32_t* v) {
     }
 }
 
-// ================= softmax / rescale / epilogue (warps 0-3) =================
+// ================= softmax / rescale / epilogue / P V issue =================
 // INT8 cache: S holds q . c_j (c_j the stored integers, exact in fp16); the
 // key's scale turns it into the score (s_j = scale * s_k,j * S_j, s_k,j
 // pre-multiplied by scale*log2(e) in the operand stage), and P V takes
 // p_j * s_v,j, so that O = sum_j p_j s_v,j c_j = sum_j p_j v_j while the row
 // sum keeps the plain p_j.
-template <int REP, bool KV8>
+//
+// PP (bf16 cache, one copy): two sets of softmax warps, 0-3 and 8-11, take
+// alternate tiles ("ping-pong"), each with its own running max, row sum and
+// O accumulator in TMEM, so that one set's barrier, TMEM and MUFU latencies
+// hide behind the other's work.  The two states of a row are merged by
+// log-sum-exp weights once per piece; each set writes half of the columns.
+template <int REP, bool KV8, bool PP>
 __device__ void softmax_role(const Cta& x) {
     using Smem = SmemT<KV8>;
+    static_assert(!PP || REP == 1, "ping-pong only with one copy");
     constexpr int RQ = REP == 4 ? 32 : REP == 2 ? 64 : ROWS;
-    constexpr int CW = TN / REP;  // key columns of a tile owned by one copy
+    constexpr int CW = TN / REP;  // key columns of a tile owned by one thread
     const AttnArgs& a = *x.a;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int warp = (tid >> 5) & 3;                // TMEM lane quadrant
+    const int set = PP && tid >= 8 * 32 ? 1 : 0;    // PP: this set takes tiles of parity `set`
+    const int ltid = tid - set * 8 * 32;            // 0..127 inside the set
     const int R = x.R, G = x.G, k = a.k, BH = x.BH;
     const int c = (warp * 32) / RQ;                 // copy of this thread
     const int r = warp * 32 + lane - c * RQ;        // query row inside the copy
@@ -201,11 +217,14 @@ __device__ void softmax_role(const Cta& x) {
     const int cbase = c * CW;
     const float sl2 = a.scale * kLog2e;
     const uint32_t lane_base = x.tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t o_mine = TM_O + set * D;         // this set's O columns
     float* s_stat_m = reinterpret_cast<float*>(x.sm + Smem::STAT);
     float* s_stat_l = s_stat_m + 4 * ROWS;
     uint64_t* bars = x.bars;
+    const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(x.sm + Smem::STAGES + KV_BYTES),
+                                             BOX_ROWS * 128, 1024);
 
-    {
+    if (REP > 1) {
         // both P buffers start at zero: a lane only ever rewrites its copy's slice
         const uint32_t zero[32] = {};
         tmem_st32(lane_base + TM_P, zero);
@@ -213,129 +232,191 @@ __device__ void softmax_role(const Cta& x) {
         tmem_wait_st();
     }
     float m_ref = -INFINITY, l = 0.f;
+    bool has = false;  // this set has taken a tile of the current piece
     Cursor cur;
     if (x.n_tiles > 0) cur.init(x.t_begin, x.s_pre, x.s_ctx, a.B, a.Hkv, k);
     bool ok = true;
     for (int it = 0; it < x.n_tiles; ++it) {
         const bool first = (it == 0) || (cur.lt == 0);
         const bool last = (it == x.n_tiles - 1) || (cur.lt == cur.nb - 1);
-        const int sb = it & 1;
+        const int sb = it & 1, sq = it % NSB;  // P buffer / P V barrier, S buffer
+        const bool mine = !PP || sb == set;
         const int ctx = x.s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
         const int nvalid = min(TN, L - key0);
         if (first) {
             m_ref = -INFINITY;
             l = 0.f;
+            has = false;
         }
-        // s_full(it) also implies every P V up to tile it-2 has finished
-        if (ok) ok = warp_wait(&bars[Smem::B_SFULL + sb], (it >> 1) & 1, x.abort_flag, a.dev_err);
-        if (ok && warp_active) {
-            tc_fence_after();
-            uint32_t sr[CW], sr2[CW];
-            load_cols<CW>(lane_base + TM_S + sb * TN + cbase, sr);
-            load_cols<CW>(lane_base + TM_SB + sb * TN + cbase, sr2);
-            tmem_wait_ld();
-#pragma unroll
-            for (int cc = 0; cc < CW; ++cc)  // S = S(dims 0-63) + S(dims 64-127)
-                sr[cc] = __float_as_uint(__uint_as_float(sr[cc]) + __uint_as_float(sr2[cc]));
-            // keys of this row visible in this copy's slice: cc < cmax
-            const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
-            // INT8: per-key fp32 scales of this operand stage (k row, then v row)
-            const float* sc_k = reinterpret_cast<const float*>(
-                x.sm + Smem::SCALES + (it % Smem::NM) * 2 * TN * 4) + cbase;
-            const float* sc_v = sc_k + TN;
-            // branch-free: masked scores become -inf (exp2 -> 0)
-            float v[CW];
-            float mt = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < CW; ++cc) {
-                const float f = KV8 ? sc_k[cc] : sl2;
-                v[cc] = cc < cmax ? __uint_as_float(sr[cc]) * f : -INFINITY;
-                mt = fmaxf(mt, v[cc]);
-            }
-            const float m_new = fmaxf(m_ref, mt);
-            float alpha = 1.f;
-            const bool move = m_new > m_ref + kRescaleThreshold;  // also -inf -> finite
-            if (move) {
-                alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
-                m_ref = m_new;
-                l *= alpha;
-            }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // keeps -inf - m finite
-            uint32_t pk[CW / 2];
-            float psum0 = 0.f, psum1 = 0.f;
-#pragma unroll
-            for (int c2 = 0; c2 < CW / 2; ++c2) {
-                const float p0 = fast_exp2(v[2 * c2] - m_use);
-                const float p1 = fast_exp2(v[2 * c2 + 1] - m_use);
-                psum0 += p0;
-                psum1 += p1;
-                if constexpr (KV8)
-                    pk[c2] = pack_f16x2(p0 * sc_v[2 * c2], p1 * sc_v[2 * c2 + 1]);
-                else
-                    pk[c2] = pack_bf16x2(p0, p1);
-            }
-            l += psum0 + psum1;
-            // P buffer sb is free once P V(it-2) has finished.  P V of tile j
-            // completes a phase of o_done[j & 1]; the next phase of that
-            // barrier needs this tile's P, so the parity wait is unambiguous
-            if (it >= 2) {
-                ok = warp_wait(&bars[Smem::B_ODONE + (it & 1)], ((it - 2) >> 1) & 1, x.abort_flag,
-                               a.dev_err);
+        if (mine) {
+            if (ok)
+                ok = warp_wait(&bars[Smem::B_SFULL + sq], (it / NSB) & 1, x.abort_flag, a.dev_err);
+            uint32_t sr[CW];
+            if (ok && warp_active) {
                 tc_fence_after();
+                load_cols<CW>(lane_base + TM_S + sq * TN + cbase, sr);
+                tmem_wait_ld();
             }
-            // this copy's slice of P; the other slices of this lane stay zero
-            store_cols<CW / 2>(lane_base + TM_P + sb * (TN / 2) + c * (CW / 2), pk);
-            tmem_wait_st();
-            if (!first && __any_sync(0xffffffffu, move)) {
-                // O must hold every earlier P V before it is rescaled
-                ok = warp_wait(&bars[Smem::B_ODONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1,
-                                   x.abort_flag, a.dev_err);
-                if (ok) {
-                    tc_fence_after();
+            // S buffer sq may take tile it + NSB once every warp of the set has loaded it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Smem::B_SFREE + sq]);
+            if (ok && warp_active) {
+                // keys of this row visible in this copy's slice: cc < cmax
+                const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
+                // INT8: per-key fp32 scales of this operand stage (k row, then v row)
+                const float* sc_k = reinterpret_cast<const float*>(
+                    x.sm + Smem::SCALES + (it % Smem::NM) * 2 * TN * 4) + cbase;
+                const float* sc_v = sc_k + TN;
+                // branch-free masking (masked scores become -inf, exp2 -> 0);
+                // four running maxima for ILP
+                float v[CW];
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int c4 = 0; c4 < D / 32; ++c4) {
-                        uint32_t ov[32];
-                        tmem_ld32(lane_base + TM_O + c4 * 32, ov);
-                        tmem_wait_ld();
+                for (int c4 = 0; c4 < CW / 4; ++c4) {
+                    float4 f4 = make_float4(sl2, sl2, sl2, sl2);
+                    if constexpr (KV8) f4 = reinterpret_cast<const float4*>(sc_k)[c4];
+                    const float f[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(lane_base + TM_O + c4 * 32, ov);
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = 4 * c4 + e;
+                        v[cc] = cc < cmax ? __uint_as_float(sr[cc]) * f[e] : -INFINITY;
+                        mx[e] = fmaxf(mx[e], v[cc]);
                     }
-                    tmem_wait_st();
+                }
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                const float m_new = fmaxf(m_ref, mt);
+                float alpha = 1.f;
+                const bool move = m_new > m_ref + kRescaleThreshold;  // also -inf -> finite
+                if (move) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+                    m_ref = m_new;
+                    l *= alpha;
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // keeps -inf - m finite
+                uint32_t pk[CW / 2];
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c4 = 0; c4 < CW / 4; ++c4) {
+                    float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
+                    if constexpr (KV8) g4 = reinterpret_cast<const float4*>(sc_v)[c4];
+                    const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+                    float pe[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        pe[e] = fast_exp2(v[4 * c4 + e] - m_use);
+                        ps[e] += pe[e];
+                    }
+                    if constexpr (KV8) {
+                        pk[2 * c4] = pack_f16x2(pe[0] * g[0], pe[1] * g[1]);
+                        pk[2 * c4 + 1] = pack_f16x2(pe[2] * g[2], pe[3] * g[3]);
+                    } else {
+                        pk[2 * c4] = pack_bf16x2(pe[0], pe[1]);
+                        pk[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
+                    }
+                }
+                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                // P buffer sb is free once P V(it-2) has finished (PP: this
+                // set's previous P V).  P V of tile j completes a phase of
+                // o_done[j & 1]; the next phase of that barrier needs this
+                // tile's P, so the parity wait is unambiguous
+                if (it >= 2) {
+                    ok = warp_wait(&bars[Smem::B_ODONE + sb], ((it - 2) >> 1) & 1, x.abort_flag,
+                                   a.dev_err);
+                    tc_fence_after();
+                }
+                // this copy's slice of P; the other slices of this lane stay zero
+                store_cols<CW / 2>(lane_base + TM_P + sb * (TN / 2) + cbase / 2, pk);
+                tmem_wait_st();
+                if (has && __any_sync(0xffffffffu, move)) {
+                    // O must hold every earlier P V before it is rescaled (PP:
+                    // the set's previous P V, tile it-2, was observed above)
+                    if (!PP)
+                        ok = warp_wait(&bars[Smem::B_ODONE + ((it - 1) & 1)],
+                                       ((it - 1) >> 1) & 1, x.abort_flag, a.dev_err);
+                    if (ok) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c4 = 0; c4 < D / 32; ++c4) {
+                            uint32_t ov[32];
+                            tmem_ld32(lane_base + o_mine + c4 * 32, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tmem_st32(lane_base + o_mine + c4 * 32, ov);
+                        }
+                        tmem_wait_st();
+                    }
                 }
             }
-        }
-        if (!KV8 && ok && nvalid % BH != 0 && warp == 0) {
-            // keys past the sequence end inside its last page: zero their V
-            // rows so that 0 * (stale or canary) never reaches O
-            ok = warp_wait(&bars[Smem::B_KVFULL + it % NS], (it / NS) & 1, x.abort_flag,
-                           a.dev_err);  // bf16: landing stage == operand stage
-            if (ok) {
-                uint8_t* vst = x.sm + Smem::STAGES + (it % NS) * STAGE_BYTES + KV_BYTES;
-                const int bx = nvalid / BH, r_end = BH;
-                for (int e = (nvalid % BH) * 16 + lane; e < r_end * 16; e += 32) {
-                    const int rr = e / 16, h = (e / 8) & 1, ch = e % 8;
-                    *reinterpret_cast<uint4*>(vst + bx * BH * 256 + h * BH * 128 + rr * 128 +
-                                              ch * 16) = make_uint4(0, 0, 0, 0);
+            if (!KV8 && ok && nvalid % BH != 0 && ltid < 32) {
+                // keys past the sequence end inside its last page: zero their V
+                // rows so that 0 * (stale or canary) never reaches O
+                ok = warp_wait(&bars[Smem::B_KVFULL + it % NS], (it / NS) & 1, x.abort_flag,
+                               a.dev_err);  // bf16: landing stage == operand stage
+                if (ok) {
+                    uint8_t* vst = x.sm + Smem::STAGES + (it % NS) * STAGE_BYTES + KV_BYTES;
+                    const int bx = nvalid / BH, r_end = BH;
+                    for (int e = (nvalid % BH) * 16 + lane; e < r_end * 16; e += 32) {
+                        const int rr = e / 16, h = (e / 8) & 1, ch = e % 8;
+                        *reinterpret_cast<uint4*>(vst + bx * BH * 256 + h * BH * 128 + rr * 128 +
+                                                  ch * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
             }
+            // O += P V of tile it, issued from here: once every warp of the set
+            // has stored its slice of P (and its warp 0 zeroed the V tail),
+            // the set's thread 0 issues the MMAs -- not a warp of its own,
+            // which the softmax warps would starve of issue slots
+            tc_fence_before();
+            named_bar_sync(6 + set, 128);
+            if (ltid == 0) {
+                tc_fence_after();
+                const int s = it % Smem::NM;
+                // V landed (bf16) / was widened (INT8); the wait that led to S
+                // already implies it, this one makes the ordering explicit
+                if (ok)
+                    ok = mbar_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_KVFULL + s],
+                                   (it / Smem::NM) & 1, x.abort_flag, a.dev_err);
+                if (ok) {
+                    // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
+                    const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
+                    const uint64_t vd = vdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                    const uint32_t pcol = x.tmem + TM_P + sb * (TN / 2);
+#pragma unroll
+                    for (int bx = 0; bx < MAX_BOX; ++bx)
+                        if (bx < nbox)
+                            umma_ts(x.tmem + o_mine, pcol + bx * (BOX_ROWS / 2),
+                                    vd + ((bx * BOX_ROWS * 256) >> 4), idesc_pv<KV8>(),
+                                    (bx > 0 || has) ? 1u : 0u);
+                    umma_commit(&bars[Smem::B_KVEMPTY + s]);
+                    umma_commit(&bars[Smem::B_ODONE + sb]);
+                }
+            }
+            if (ltid < 32) ok = __shfl_sync(0xffffffffu, ok, 0);
+            has = true;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[Smem::B_PFULL + sb]);
 
         if (last) {
             // ---- epilogue of the piece that ends at this tile
-            if (ok && warp_active) {
-                // observe P V(it-1) before P V(it) so the parity wait is unambiguous
-                if (!first)
-                    ok = warp_wait(&bars[Smem::B_ODONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1,
+            if (ok && warp_active && has) {
+                if (PP) {
+                    // this set's latest P V (tile it or it-1); its previous one
+                    // was observed before that tile's P was stored
+                    const int itm = mine ? it : it - 1;
+                    ok = warp_wait(&bars[Smem::B_ODONE + (itm & 1)], (itm >> 1) & 1,
                                    x.abort_flag, a.dev_err);
-                if (ok)
-                    ok = warp_wait(&bars[Smem::B_ODONE + (it & 1)], (it >> 1) & 1, x.abort_flag,
-                                   a.dev_err);
+                } else {
+                    // observe P V(it-1) before P V(it) so the parity wait is unambiguous
+                    if (!first)
+                        ok = warp_wait(&bars[Smem::B_ODONE + ((it - 1) & 1)],
+                                       ((it - 1) >> 1) & 1, x.abort_flag, a.dev_err);
+                    if (ok)
+                        ok = warp_wait(&bars[Smem::B_ODONE + (it & 1)], (it >> 1) & 1,
+                                       x.abort_flag, a.dev_err);
+                }
                 tc_fence_after();
             }
             const bool complete = cur.seg_start >= x.t_begin && cur.seg_start + cur.nb <= x.t_end;
@@ -344,14 +425,44 @@ __device__ void softmax_role(const Cta& x) {
                 return ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
             };
             if constexpr (REP == 1) {
+                // weights of the two sets' O (PP) or of the single O
+                float w_mine = 1.f, w_other = 0.f, lt = l, mt = m_ref;
+                if constexpr (PP) {
+                    if (warp_active) {  // both sets' warps of a quadrant, every piece
+                        s_stat_m[set * ROWS + warp * 32 + lane] = has ? m_ref : -INFINITY;
+                        s_stat_l[set * ROWS + warp * 32 + lane] = has ? l : 0.f;
+                        tc_fence_before();
+                        named_bar_sync(2 + warp, 64);
+                        tc_fence_after();
+                        const float mo = s_stat_m[(1 - set) * ROWS + warp * 32 + lane];
+                        const float lo = s_stat_l[(1 - set) * ROWS + warp * 32 + lane];
+                        const float mm = has ? m_ref : -INFINITY;
+                        mt = fmaxf(mm, mo);
+                        w_mine = mm == -INFINITY ? 0.f : fast_exp2(mm - mt);
+                        w_other = mo == -INFINITY ? 0.f : fast_exp2(mo - mt);
+                        lt = w_mine * (has ? l : 0.f) + w_other * lo;
+                    }
+                }
                 if (ok && warp_active) {
-                    const float inv_l = l > 0.f ? 1.f / l : 0.f;
-                    const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+                    const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+                    const float lse = lt > 0.f ? (mt + log2f(lt)) * kLn2 : -INFINITY;
+                    const float wm = w_mine * inv_l, wo = w_other * inv_l;
+                    const uint32_t o_other = TM_O + (1 - set) * D;
+                    // PP: set s writes output columns [64 s, 64 s + 64) from both O
 #pragma unroll
-                    for (int c4 = 0; c4 < D / 32; ++c4) {
-                        uint32_t ov[32];
-                        tmem_ld32(lane_base + TM_O + c4 * 32, ov);
+                    for (int c4 = (PP ? set * 2 : 0); c4 < (PP ? set * 2 + 2 : D / 32); ++c4) {
+                        uint32_t ov[32], ow[32];
+                        tmem_ld32(lane_base + o_mine + c4 * 32, ov);
+                        if (PP) tmem_ld32(lane_base + o_other + c4 * 32, ow);
                         tmem_wait_ld();
+                        float o[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            // a set without a tile of this piece holds stale O: weight 0, never read
+                            const float a0 = wm > 0.f ? __uint_as_float(ov[e]) * wm : 0.f;
+                            const float a1 = PP && wo > 0.f ? __uint_as_float(ow[e]) * wo : 0.f;
+                            o[e] = a0 + a1;
+                        }
                         if (!row_valid) continue;
                         if (complete) {
                             uint4* dst = reinterpret_cast<uint4*>(
@@ -359,14 +470,10 @@ __device__ void softmax_role(const Cta& x) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
                                 uint4 w;
-                                w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l,
-                                                  __uint_as_float(ov[8 * v + 1]) * inv_l);
-                                w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l,
-                                                  __uint_as_float(ov[8 * v + 3]) * inv_l);
-                                w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l,
-                                                  __uint_as_float(ov[8 * v + 5]) * inv_l);
-                                w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l,
-                                                  __uint_as_float(ov[8 * v + 7]) * inv_l);
+                                w.x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
+                                w.y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
+                                w.z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
+                                w.w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
                                 dst[v] = w;
                             }
                         } else {
@@ -374,18 +481,25 @@ __device__ void softmax_role(const Cta& x) {
                                 x.prm->part_o + ((int64_t)slot * ROWS + r) * D + c4 * 32);
 #pragma unroll
                             for (int v = 0; v < 8; ++v)
-                                dst[v] = make_float4(__uint_as_float(ov[4 * v + 0]) * inv_l,
-                                                     __uint_as_float(ov[4 * v + 1]) * inv_l,
-                                                     __uint_as_float(ov[4 * v + 2]) * inv_l,
-                                                     __uint_as_float(ov[4 * v + 3]) * inv_l);
+                                dst[v] = make_float4(o[4 * v + 0], o[4 * v + 1], o[4 * v + 2],
+                                                     o[4 * v + 3]);
                         }
                     }
-                    if (row_valid) {
+                    if (row_valid && set == 0) {
                         if (complete) {
                             if (a.lse) a.lse[out_row(r)] = lse;
                         } else {
                             x.prm->part_lse[(int64_t)slot * ROWS + r] = lse;
                         }
+                    }
+                }
+                if constexpr (PP) {
+                    // the other set reads this set's O: neither starts the next
+                    // piece's P V (which overwrites O) before both are done
+                    if (warp_active) {
+                        tc_fence_before();
+                        named_bar_sync(2 + warp, 64);
+                        tc_fence_after();
                     }
                 }
             } else {
@@ -479,6 +593,12 @@ __device__ void softmax_role(const Cta& x) {
         }
         if (it + 1 < x.n_tiles) cur.next(x.s_ctx, a.Hkv, k);
     }
+    // every P V issued from here must finish before TMEM is released
+    if (ltid == 0 && x.n_tiles > 0) {
+        umma_commit(&bars[Smem::B_DRAIN + 1 + set]);
+        mbar_drain(&bars[Smem::B_DRAIN + 1 + set], 0);
+    }
+    __syncwarp();
 }
 
 // Widens 16 int8 (one 16-byte chunk) to 16 fp16 (two chunks), exactly: the
@@ -542,14 +662,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
         mbar_init(&bars[Smem::B_QFULL], 1);
-        mbar_init(&bars[Smem::B_QFREE], 2);  // one commit per Q K^T warp
-        for (int q = 0; q < 2; ++q) {
-            mbar_init(&bars[Smem::B_SFULL + q], 2);  // both head-dim halves of S
-            mbar_init(&bars[Smem::B_PFULL + q], 4);
-            mbar_init(&bars[Smem::B_ODONE + q], 1);  // P V of even / odd tiles
-            mbar_init(&bars[Smem::B_QCP + q], 1);
+        mbar_init(&bars[Smem::B_QFREE], 1);
+        mbar_init(&bars[Smem::B_QCP], 1);
+        for (int q = 0; q < NSB; ++q) {
+            mbar_init(&bars[Smem::B_SFULL + q], 1);
+            mbar_init(&bars[Smem::B_SFREE + q], 4);  // the 4 warps of the set that took the tile
         }
-        for (int q = 0; q < 3; ++q) mbar_init(&bars[Smem::B_DRAIN + q], 1);
+        for (int q = 0; q < 2; ++q) mbar_init(&bars[Smem::B_ODONE + q], 1);  // even / odd tiles
+        for (int q = 0; q < 3; ++q) mbar_init(&bars[Smem::B_DRAIN + q], 1);  // Q K^T, P V x2
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -603,8 +723,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp == 7) {
-        // ================= TMA producer (warp 7) =================
+    if (warp == 6) {
+        // ================= TMA producer (warp 6) =================
         // One 3-D box per (page, tensor): both 64-column halves of BH keys of
         // one kv-head, 256*BH bytes, landing as [half][key][128 B] with the
         // 128-byte swizzle the MMAs read.  Boxes of a tile are issued by
@@ -682,20 +802,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (ok)
                     mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
                                           KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
-                                              : 2u * nbox * BH * 256);
+                                              : (nvalid + 7) / 8 * 2048u + nbox * 4096u);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (lane < (KV8 ? 4 : 2) * nbox) {
-                const int bx = KV8 ? lane >> 2 : lane >> 1;
-                int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
-                if (page < 0 || page >= a.num_pages) {
-                    raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
-                    page = 0;
-                }
-                const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BH) % P;
-                uint8_t* st = sm + Smem::RAW + s * Smem::RAW_STAGE;
-                if constexpr (KV8) {
+            uint8_t* st = sm + Smem::RAW + s * Smem::RAW_STAGE;
+            if constexpr (KV8) {
+                if (lane < 4 * nbox) {
+                    const int bx = lane >> 2;
+                    int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
+                    if (page < 0 || page >= a.num_pages) {
+                        raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                        page = 0;
+                    }
+                    const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BH) % P;
                     // lane & 3: K box, V box (16 rows x 128 int8), k / v scales (16 fp16)
                     const int what = lane & 3;
                     if (what < 2)
@@ -706,10 +826,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         bulk_load(st + 2 * RAW8_KV + (what - 2) * TN * 2 + bx * BH * 2,
                                   (what == 2 ? a.k_scale : a.v_scale) + row, BH * 2,
                                   &bars[Smem::B_KVFULL + s]);
-                } else {
-                    const int tensor = lane & 1;
-                    tma_load_3d_hint(st + tensor * KV_BYTES + bx * BH * 256,
-                                     tensor ? (const void*)&vmap : (const void*)&kmap,
+                }
+            } else {
+                // K: 8-key boxes (lanes 0-7, 2 KB: both head-dim halves of 8
+                // full rows) landing as [half 0 | half 1], so 8-key group g of
+                // half h sits at g*2 KB + h*1 KB -- the uniform stride an N = 64
+                // Q K^T reads, with no relayout.  V: 16-key boxes (lanes 16-19,
+                // 4 KB) in the layout P V reads.
+                const bool isv = lane >= 16;
+                const int j = isv ? lane - 16 : lane;
+                if (isv ? j < nbox : j * 8 < nvalid) {
+                    const int bx = isv ? j : j >> 1;  // 16-key slice (one page)
+                    int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
+                    if (page < 0 || page >= a.num_pages) {
+                        raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                        page = 0;
+                    }
+                    const int row = (page * Hkv + cur.kvh) * P + (key0 + j * (isv ? 16 : 8)) % P;
+                    tma_load_3d_hint(st + (isv ? KV_BYTES + j * 4096 : j * 2048),
+                                     isv ? (const void*)&vmap : (const void*)&kmap,
                                      &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
                 }
             }
@@ -728,7 +863,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
     } else if (KV8 && warp >= 8) {
         // ================= INT8 widening (warps 8-11) =================
-        // Raw stage -> operand stage: K lands in the relayouted order the N = 64
+        // Raw stage -> operand stage: K lands in the order the N = 64
         // Q K^T reads (8-key groups 2 KB apart), V in the box order of P V
         // (16-key boxes 4 KB apart), both as fp16 with the 128-byte swizzle;
         // the per-key scales become fp32 rows (k pre-multiplied by
@@ -786,145 +921,77 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
-    } else if (!KV8 && warp == 8) {
-        // ================= K relayout (warp 8) =================
-        // A K box lands as [h0 rows 0-7 | h0 rows 8-15 | h1 rows 0-7 | h1 rows
-        // 8-15] (1 KB blocks, 128-byte swizzle).  Swapping the middle blocks
-        // gives [h0 0-7 | h1 0-7 | h0 8-15 | h1 8-15]: every 8-key group of the
-        // tile then sits 2 KB after the previous one.  A row's swizzle phase is
-        // its index mod 8, which the move keeps.
-        Cursor cur;
-        if (n_tiles > 0) cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
-        bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            const int s = it % NS;
-            const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
-            const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-            ok = warp_wait(&bars[Smem::B_KVFULL + s], (it / NS) & 1, abort_flag, a.dev_err);
-            if (!ok) break;
-            uint4* kst = reinterpret_cast<uint4*>(sm + Smem::STAGES + s * STAGE_BYTES);
-            for (int bx = 0; bx < nbox; ++bx) {
-                uint4* b1 = kst + bx * (BOX_ROWS * 256 / 16) + 1024 / 16;
-                uint4* b2 = b1 + 1024 / 16;
-                const uint4 x0 = b1[lane], x1 = b1[lane + 32];
-                const uint4 y0 = b2[lane], y1 = b2[lane + 32];
-                b1[lane] = y0;
-                b1[lane + 32] = y1;
-                b2[lane] = x0;
-                b2[lane + 32] = x1;
-            }
-            fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[Smem::B_KREADY + s]);
-            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
-        }
-    } else if (warp >= 4 && warp <= 6) {
-        // ================= tensor-core issue: warps 4-5 = Q K^T, warp 6 = P V =================
-        // A tcgen05.mma takes ~100 cycles to issue from one warp whatever its
-        // N, so the GEMMs of a tile are issued by three warps in parallel: Q K^T
-        // split by head-dim half into two partial score buffers (the softmax
-        // adds them), and P V.
-        //
-        // K arrives relayouted by warp 8 (INT8: widened by warps 8-11) with
-        // 8-key groups 2 KB apart, one uniform stride for an N = 64 MMA; V
-        // keeps the box layout and P V runs one K = 16 MMA per box.
-        const int role = warp - 4;  // 0, 1: Q K^T head-dim half; 2: P V
+    } else if (warp == 4) {
+        // ================= Q K^T issue (warp 4) =================
+        // K arrives (bf16: as 8-key TMA boxes; INT8: widened by warps 8-11)
+        // with 8-key groups 2 KB apart, one uniform stride for an N = 64 MMA.
+        // P V is issued by the softmax warps.
         if (n_tiles > 0) {
             Cursor cur;
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             int pc = -1;
             bool ok = true;
-            constexpr uint32_t kIdescQK = idesc_qk<KV8>(), kIdescPV = idesc_pv<KV8>();
+            constexpr uint32_t kIdescQK = idesc_qk<KV8>();
             // smem descriptors are built once; an operand's start address
             // lives in the low 14 bits (in 16-byte units), so stepping to
             // another k-slice, box or stage is one 64-bit add
             const uint64_t qdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::Q), 16, 1024);
             const uint64_t kdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::STAGES), 16, 2048);
-            const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::STAGES + KV_BYTES),
-                                                     BOX_ROWS * 128, 1024);
             for (int it = 0; it < n_tiles && ok; ++it) {
                 const bool first = (it == 0) || (cur.lt == 0);
                 if (first) ++pc;
-                const int s = it % NM, sb = it & 1;
-                const int nvalid = min(TN, s_ctx[cur.b] + k - cur.lt * TN);
-                const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-                if (role < 2) {
-                    const int h = role;  // head-dim half: columns 64h .. 64h+63
+                const int s = it % NM, sq = it % NSB;
+                {
                     if (first) {
                         ok = warp_wait(&bars[Smem::B_QFULL], pc & 1, abort_flag, a.dev_err);
                         if (ok && pc >= 1) {
-                            // the previous piece's MMAs still read this half of
-                            // TMEM Q: wait for them before overwriting it
-                            if (lane == 0) umma_commit(&bars[Smem::B_QCP + h]);
+                            // the previous piece's MMAs still read TMEM Q: wait
+                            // for them before overwriting it
+                            if (lane == 0) umma_commit(&bars[Smem::B_QCP]);
                             __syncwarp();
-                            ok = warp_wait(&bars[Smem::B_QCP + h], (pc - 1) & 1, abort_flag,
-                                           a.dev_err);
+                            ok = warp_wait(&bars[Smem::B_QCP], (pc - 1) & 1, abort_flag, a.dev_err);
                         }
                     }
                     if (KV8 && first && ok) {
-                        // this half of the piece's Q to fp16, in place (the
-                        // MMAs read fp16 operands when the cache is INT8)
-                        uint4* qh = reinterpret_cast<uint4*>(sm + Smem::Q + h * Q_HALF);
+                        // the piece's Q to fp16, in place (the MMAs read fp16
+                        // operands when the cache is INT8)
+                        uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
 #pragma unroll 4
-                        for (int e = lane; e < Q_HALF / 16; e += 32) qh[e] = bf16x8_to_f16(qh[e]);
+                        for (int e = lane; e < Q_BYTES / 16; e += 32) q4[e] = bf16x8_to_f16(q4[e]);
                         fence_proxy_async_smem();
                     }
-                    // K of tile it landed and was relayouted / widened
+                    // K of tile it landed (bf16) / was widened (INT8)
                     if (ok)
-                        ok = warp_wait(&bars[Smem::B_KREADY + s], (it / NM) & 1, abort_flag,
-                                       a.dev_err);
-                    // S buffer sb is free once the softmax has read tile it-2
-                    if (ok && it >= 2)
-                        ok = warp_wait(&bars[Smem::B_PFULL + sb], ((it - 2) >> 1) & 1, abort_flag,
-                                       a.dev_err);
+                        ok = warp_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_KVFULL + s],
+                                       (it / NM) & 1, abort_flag, a.dev_err);
+                    // S buffer sq is free once every softmax warp has loaded tile it - NSB
+                    if (ok && it >= NSB)
+                        ok = warp_wait(&bars[Smem::B_SFREE + sq], ((it / NSB) - 1) & 1,
+                                       abort_flag, a.dev_err);
                     if (!ok) break;
                     __syncwarp();
                     tc_fence_after();
                     if (lane == 0) {
                         if (first) {
-                            // this half of the piece's Q: smem (TMA, 128-byte
-                            // swizzle) -> TMEM; k-slice kk = 32-byte step kk%4
+                            // the piece's Q: smem (TMA, 128-byte swizzle) ->
+                            // TMEM; k-slice kk = half kk/4, 32-byte step kk%4
 #pragma unroll
-                            for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                            for (int kk = 0; kk < 8; ++kk)
                                 tmem_cp_128x256b(tmem + TM_Q + kk * 8,
-                                                 qdesc0 + h * (Q_HALF >> 4) + (kk & 3) * 2);
-                            // the staging buffer may take the next piece's Q once
-                            // both halves' copies are done
+                                                 qdesc0 + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                            // the staging buffer may take the next piece's Q
+                            // once the copies are done
                             umma_commit(&bars[Smem::B_QFREE]);
                         }
-                        // S_h = Q_h K_h^T: K half h of 8-key group g at g*2 KB + h*1 KB
-                        const uint64_t kd =
-                            kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4) + h * (1024 >> 4);
-                        const uint32_t dcol = tmem + (h ? TM_SB : TM_S) + sb * TN;
+                        // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
+                        const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                        const uint32_t dcol = tmem + TM_S + sq * TN;
 #pragma unroll
-                        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-                            umma_ts(dcol, tmem + TM_Q + kk * 8, kd + (kk & 3) * 2, kIdescQK,
-                                    (kk & 3) ? 1u : 0u);
-                        umma_commit(&bars[Smem::B_SFULL + sb]);
-                    }
-                    __syncwarp();
-                } else {
-                    // O += P V over the first nbox boxes of tile it (the rest are
-                    // past the sequence end and hold no probability mass)
-                    ok = warp_wait(&bars[Smem::B_PFULL + sb], (it >> 1) & 1, abort_flag, a.dev_err);
-                    // V landed (bf16) / was widened (INT8)
-                    if (ok)
-                        ok = warp_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_KVFULL + s],
-                                       (it / NM) & 1, abort_flag, a.dev_err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
-                        const uint64_t vd = vdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
-                        const uint32_t pcol = tmem + TM_P + sb * (TN / 2);
-#pragma unroll
-                        for (int bx = 0; bx < MAX_BOX; ++bx)
-                            if (bx < nbox)
-                                umma_ts(tmem + TM_O, pcol + bx * (BOX_ROWS / 2),
-                                        vd + ((bx * BOX_ROWS * 256) >> 4), kIdescPV,
-                                        (bx > 0 || !first) ? 1u : 0u);
-                        umma_commit(&bars[Smem::B_KVEMPTY + s]);
-                        umma_commit(&bars[Smem::B_ODONE + sb]);
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ts(dcol, tmem + TM_Q + kk * 8,
+                                    kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, kIdescQK,
+                                    kk ? 1u : 0u);
+                        umma_commit(&bars[Smem::B_SFULL + sq]);
                     }
                     __syncwarp();
                 }
@@ -932,12 +999,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             // every tensor-core op of this warp must finish before TMEM is released
             if (lane == 0) {
-                umma_commit(&bars[Smem::B_DRAIN + role]);
-                mbar_drain(&bars[Smem::B_DRAIN + role], 0);
+                umma_commit(&bars[Smem::B_DRAIN]);
+                mbar_drain(&bars[Smem::B_DRAIN], 0);
             }
             __syncwarp();
         }
-    } else {
+    } else if (warp < 4 || (!KV8 && warp >= 8)) {
         Cta x;
         x.a = &a;
         x.prm = &prm;
@@ -953,9 +1020,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         x.R = R;
         x.G = G;
         x.BH = BH;
-        if (REP == 4) softmax_role<4, KV8>(x);
-        else if (REP == 2) softmax_role<2, KV8>(x);
-        else softmax_role<1, KV8>(x);
+        // bf16 cache, one copy: warps 0-3 and 8-11 take alternate tiles;
+        // with copies the second set has no work
+        const bool second = warp >= 8;
+        if (REP == 4) {
+            if (!second) softmax_role<4, KV8, false>(x);
+        } else if (REP == 2) {
+            if (!second) softmax_role<2, KV8, false>(x);
+        } else if (KV8) {
+            softmax_role<1, true, false>(x);
+        } else {
+            softmax_role<1, false, true>(x);
+        }
     }
 
     tc_fence_before();
@@ -1138,7 +1214,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
     for (int t = 0; t < 2 && !kv8; ++t) {
         cuuint64_t dims[3] = {64, rows, 2};
         cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-        cuuint32_t box[3] = {64, (cuuint32_t)BH, 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)(t == 0 ? BH / 2 : BH), 2};  // K: 8-key boxes
         cuuint32_t es[3] = {1, 1, 1};
         if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
