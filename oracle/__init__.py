@@ -12,6 +12,9 @@ computes and which passage of the pages it follows:
   Compression".
 * ``accept_greedy`` -- first-disagreement acceptance plus bonus token (same
   blog, "Speculating to get sequence parallelism during decode").
+* ``accept_rejection`` -- lossless rejection-sampling acceptance (same blog,
+  "How does this drafter maintain the same distribution of the target?"),
+  with its draws from the counter-based generator SplitMix64.
 
 Arrays are numpy; 16-bit float types travel as their raw ``uint16`` bits.
 """
@@ -45,6 +48,16 @@ def _load():
         lib.oracle_attn_rows.restype = i32
         lib.oracle_accept_greedy.argtypes = [P, i32, P, i32, i32, ctypes.c_int64, P, P, P]
         lib.oracle_accept_greedy.restype = i32
+        u64 = ctypes.c_uint64
+        lib.oracle_accept_rejection.argtypes = [P, P, i32, P, i32, i32, ctypes.c_int64,
+                                                ctypes.c_double, u64, P, P, P, P, P]
+        lib.oracle_accept_rejection.restype = i32
+        lib.oracle_splitmix64.argtypes = [u64, u64]
+        lib.oracle_splitmix64.restype = u64
+        lib.oracle_accept_uniform.argtypes = [u64, i32, i32]
+        lib.oracle_accept_uniform.restype = ctypes.c_double
+        lib.oracle_gumbel.argtypes = [u64, i32, ctypes.c_int64]
+        lib.oracle_gumbel.restype = ctypes.c_double
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -124,6 +137,46 @@ def accept_greedy(logits, dtype, draft_tokens):
     return acc, nxt, am
 
 
+def accept_rejection(target_logits, draft_logits, dtype, draft_tokens, temperature, seed):
+    """target_logits [B, k+1, V]; draft_logits [B, k, V]; draft_tokens int32 [B, k].
+
+    Return (accepted_len[B] int32, next_token[B] int32, ratio[B, k],
+    unif[B, k], key_gap[B]): p(x)/q(x) and the acceptance uniform at every
+    position up to the first rejection (NaN after it), and the gap between
+    the two best Gumbel keys of the final draw.
+    """
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    assert draft_logits.shape == (B, k, V)
+    draft_tokens = np.ascontiguousarray(draft_tokens, np.int32)
+    assert draft_tokens.shape == (B, k)
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    ratio = np.zeros((B, k), np.float64)
+    unif = np.zeros((B, k), np.float64)
+    gap = np.zeros(B, np.float64)
+    rc = _load().oracle_accept_rejection(_ptr(target_logits), _ptr(draft_logits), DTYPES[dtype],
+                                         _ptr(draft_tokens), B, k, V, float(temperature),
+                                         int(seed) & (2**64 - 1), _ptr(acc), _ptr(nxt),
+                                         _ptr(ratio), _ptr(unif), _ptr(gap))
+    if rc:
+        raise ValueError("oracle_accept_rejection failed (%d)" % rc)
+    return acc, nxt, ratio, unif, gap
+
+
+def splitmix64(seed: int, n: int) -> int:
+    """The n-th (0-based) output of SplitMix64 seeded with `seed`."""
+    return int(_load().oracle_splitmix64(int(seed) & (2**64 - 1), int(n)))
+
+
+def accept_uniform(seed: int, b: int, i: int) -> float:
+    return float(_load().oracle_accept_uniform(int(seed) & (2**64 - 1), int(b), int(i)))
+
+
+def gumbel(seed: int, b: int, x: int) -> float:
+    return float(_load().oracle_gumbel(int(seed) & (2**64 - 1), int(b), int(x)))
+
+
 def bf16_bits_to_f64(bits: int) -> float:
     return _load().oracle_bf16_to_f64(int(bits))
 
@@ -132,5 +185,5 @@ def f16_bits_to_f64(bits: int) -> float:
     return _load().oracle_f16_to_f64(int(bits))
 
 
-__all__ = ["verify_attn", "attn_rows", "accept_greedy", "bf16_bits_to_f64", "f16_bits_to_f64",
-           "DTYPES"]
+__all__ = ["verify_attn", "attn_rows", "accept_greedy", "accept_rejection", "splitmix64",
+           "accept_uniform", "gumbel", "bf16_bits_to_f64", "f16_bits_to_f64", "DTYPES"]

@@ -241,3 +241,122 @@ int oracle_accept_greedy(const void *logits, int dtype, const int32_t *draft, in
     free(a);
     return 0;
 }
+
+/*
+ * 3. Rejection-sampling acceptance ("Decoding Speculative Decoding from First
+ *    Principles", section "How does this drafter maintain the same
+ *    distribution of the target?").  p is the target's next-token
+ *    distribution and q the drafter's, each softmax(logits / T).  At every
+ *    drafted position the draft x is kept with probability min(1, p(x)/q(x))
+ *    (always when p(x) >= q(x)); at the first rejection a token is drawn from
+ *    the residual max(p - q, 0), renormalised; when all k drafts are kept the
+ *    bonus token is drawn from p at position k.  The emitted tokens then
+ *    follow p exactly (the section's "Proving the same distribution").
+ *
+ *    Random draws.  Every draw comes from the counter-based generator
+ *    SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ *    generators", 2014): the n-th output for seed s is the SplitMix64 mix of
+ *    s + (n + 1) * 0x9E3779B97F4A7C15.  Draw n = ((2 b + kind) << 32) | j:
+ *      kind 0, j = position i: the acceptance uniform u in [0, 1) (24 bits);
+ *      kind 1, j = token x:    the Gumbel noise g = -ln(-ln u'), u' in (0, 1).
+ *    A draw from a distribution w over the vocabulary is the Gumbel-max
+ *    choice argmax_x ln w(x) + g(x) (lowest index on ties), which picks x
+ *    with probability w(x) / sum w.
+ *
+ *    target [B, k+1, V], draft_logits [B, k, V] (same dtype), draft [B, k].
+ *    Optional diagnostics: ratio / unif [B, k] receive p(x)/q(x) and u at
+ *    every position up to the first rejection (NaN after it); key_gap [B]
+ *    the gap between the best and second-best Gumbel keys of the draw.
+ */
+static uint64_t sm64_at(uint64_t seed, uint64_t n) {
+    uint64_t z = seed + (n + 1) * 0x9E3779B97F4A7C15ULL;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+/* The n-th SplitMix64 output (exported for the generator's known-answer pin). */
+uint64_t oracle_splitmix64(uint64_t seed, uint64_t n) { return sm64_at(seed, n); }
+
+static uint64_t draw_index(int b, int kind, int64_t j) {
+    return ((uint64_t)(2 * (uint64_t)b + (uint64_t)kind) << 32) | (uint64_t)j;
+}
+
+/* 24-bit uniform in [0, 1) and in (0, 1). */
+static double unif_co(uint64_t z) { return (double)(z >> 40) * 0x1p-24; }
+static double unif_oo(uint64_t z) { return (double)((z >> 41) * 2 + 1) * 0x1p-24; }
+
+double oracle_accept_uniform(uint64_t seed, int b, int i) {
+    return unif_co(sm64_at(seed, draw_index(b, 0, i)));
+}
+
+double oracle_gumbel(uint64_t seed, int b, int64_t x) {
+    return -log(-log(unif_oo(sm64_at(seed, draw_index(b, 1, x)))));
+}
+
+/* ln sum_x exp(row[x] / T) */
+static double row_lse(const void *logits, int dtype, int64_t off, int64_t V, double T) {
+    double m = -INFINITY;
+    for (int64_t x = 0; x < V; ++x) {
+        double l = load_f64(logits, dtype, off + x) / T;
+        if (l > m) m = l;
+    }
+    double s = 0.0;
+    for (int64_t x = 0; x < V; ++x) s += exp(load_f64(logits, dtype, off + x) / T - m);
+    return m + log(s);
+}
+
+int oracle_accept_rejection(const void *target, const void *draft_logits, int dtype,
+                            const int32_t *draft, int B, int num_draft, int64_t V,
+                            double temperature, uint64_t seed, int32_t *accepted_len,
+                            int32_t *next_token, double *ratio, double *unif, double *key_gap) {
+    if (B < 0 || num_draft < 1 || V < 1 || !(temperature > 0.0)) return -1;
+    const double T = temperature;
+    const int k = num_draft;
+    for (int b = 0; b < B; ++b) {
+        int n = k;
+        double lse_p = 0.0, lse_q = 0.0;
+        for (int i = 0; i < k; ++i) {
+            const int32_t x = draft[(int64_t)b * k + i];
+            if (x < 0 || x >= V) return -1;
+            const int64_t po = ((int64_t)b * (k + 1) + i) * V, qo = ((int64_t)b * k + i) * V;
+            lse_p = row_lse(target, dtype, po, V, T);
+            lse_q = row_lse(draft_logits, dtype, qo, V, T);
+            const double lp = load_f64(target, dtype, po + x) / T - lse_p;
+            const double lq = load_f64(draft_logits, dtype, qo + x) / T - lse_q;
+            const double r = exp(lp - lq);  /* p(x) / q(x) */
+            const double u = oracle_accept_uniform(seed, b, i);
+            if (ratio) ratio[(int64_t)b * k + i] = r;
+            if (unif) unif[(int64_t)b * k + i] = u;
+            if (!(u < r)) { n = i; break; }
+        }
+        if (ratio)
+            for (int i = n + 1; i < k; ++i) ratio[(int64_t)b * k + i] = NAN;
+        if (unif)
+            for (int i = n + 1; i < k; ++i) unif[(int64_t)b * k + i] = NAN;
+        /* Gumbel-max draw: from p at position k (bonus) or from the residual at n */
+        double best = -INFINITY, second = -INFINITY;
+        int32_t arg = -1;
+        const int64_t po = ((int64_t)b * (k + 1) + n) * V, qo = ((int64_t)b * k + n) * V;
+        for (int64_t x = 0; x < V; ++x) {
+            double lw;
+            if (n == k) {
+                lw = load_f64(target, dtype, po + x) / T;  /* ln p(x) up to a constant */
+            } else {
+                const double p = exp(load_f64(target, dtype, po + x) / T - lse_p);
+                const double q = exp(load_f64(draft_logits, dtype, qo + x) / T - lse_q);
+                const double w = p - q;
+                lw = w > 0.0 ? log(w) : -INFINITY;
+            }
+            if (lw == -INFINITY) continue;
+            const double key = lw + oracle_gumbel(seed, b, x);
+            if (key > best) { second = best; best = key; arg = (int32_t)x; }
+            else if (key > second) second = key;
+        }
+        if (arg < 0) return -3; /* an empty residual cannot follow a rejection */
+        accepted_len[b] = n;
+        next_token[b] = arg;
+        if (key_gap) key_gap[b] = best - second;
+    }
+    return 0;
+}
