@@ -188,6 +188,47 @@ SPEC_API int spec_accept_greedy_noalloc(const void *logits, int32_t logits_dtype
                                         int32_t num_draft, int64_t vocab, int32_t *accepted_len,
                                         int32_t *next_token, void *stream);
 
+/*
+ * Rejection-sampling acceptance ("Decoding Speculative Decoding from First
+ * Principles", section "How does this drafter maintain the same
+ * distribution of the target?").
+ *
+ * With p_i = softmax(target_logits[b, i, :] / temperature) and
+ * q_i = softmax(draft_logits[b, i, :] / temperature), draft x_i =
+ * draft_tokens[b, i] is kept while u_i < p_i(x_i) / q_i(x_i); at the first
+ * rejection n a token is drawn from max(p_n - q_n, 0) (renormalised); after
+ * k acceptances the bonus token is drawn from p_k.  The emitted tokens then
+ * follow the target distribution exactly.
+ *   accepted_len[b] = n (number of drafts kept), next_token[b] = the draw,
+ *   so each sequence gains n + 1 tokens and commits by ctx_b += n + 1.
+ *
+ * Draws come from the counter-based generator SplitMix64 keyed by `seed`:
+ * draw number ((2b + kind) << 32) | j is the SplitMix64 mix of
+ * seed + (draw + 1) * 0x9E3779B97F4A7C15; kind 0 gives u_j = top 24 bits /
+ * 2^24, kind 1 the Gumbel noise g_j = -ln(-ln u') (u' = (2 * top 23 bits +
+ * 1) / 2^24) of token j, and a draw from weights w is argmax_x ln w(x) +
+ * g_x (lowest index on ties).  The same seed gives the same tokens; use a
+ * fresh seed per step.  Arithmetic is fp32, so a test u_i within ~1e-6 of
+ * p/q, or two Gumbel keys within ~1e-6, may decide differently from an
+ * exact evaluation.
+ *
+ *   target_logits  [batch, num_draft + 1, vocab]  logits_dtype (F32|BF16), finite
+ *   draft_logits   [batch, num_draft, vocab]      same dtype, finite
+ *   draft_tokens   [batch, num_draft] int32 in [0, vocab) (others are
+ *                  rejected and flagged with SPEC_DEVERR_TOKEN)
+ *   temperature    > 0 and finite
+ *   accepted_len, next_token  [batch] int32, written
+ *
+ * Limits: 1 <= num_draft <= 64; 1 <= vocab < 2^31; both logits arrays
+ * 16-byte aligned.  Uses the library workspace (grown on demand, like the
+ * other calls).
+ */
+SPEC_API int spec_accept_rejection(const void *target_logits, const void *draft_logits,
+                                   int32_t logits_dtype, const int32_t *draft_tokens,
+                                   int32_t batch, int32_t num_draft, int64_t vocab,
+                                   float temperature, uint64_t seed, int32_t *accepted_len,
+                                   int32_t *next_token, void *stream);
+
 /* Read and clear the device error word of the current device (synchronises
  * the device).  0 = no fault seen; otherwise a bitwise OR of SPEC_DEVERR_*. */
 SPEC_API int spec_device_error(int32_t *flags);
@@ -195,7 +236,8 @@ SPEC_API int spec_device_error(int32_t *flags);
 enum {
     SPEC_DEVERR_PAGE = 1,    /* block_table entry outside [0, num_pages) (clamped) */
     SPEC_DEVERR_CTX = 2,     /* ctx_b + k beyond the block table (clamped) */
-    SPEC_DEVERR_TIMEOUT = 4  /* a bounded on-chip wait gave up; results invalid */
+    SPEC_DEVERR_TIMEOUT = 4, /* a bounded on-chip wait gave up; results invalid */
+    SPEC_DEVERR_TOKEN = 8    /* a draft token outside [0, vocab) (treated as rejected) */
 };
 
 /* Free the current device's workspace (synchronises the device). */

@@ -20,12 +20,12 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecveri
 SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_F16, SPEC_DTYPE_I8 = 0, 1, 2, 3
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_OPT_ATTN_PATH, SPEC_OPT_NUM_CTAS, SPEC_OPT_VALIDATE, SPEC_OPT_SIMT_CHUNK = 0, 1, 2, 3
-SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT = 1, 2, 4
+SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT, SPEC_DEVERR_TOKEN = 1, 2, 4, 8
 
 # every symbol the public header declares
 EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
-            "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_device_error",
-            "spec_release"]
+            "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_accept_rejection",
+            "spec_device_error", "spec_release"]
 SPEC_NOALLOC_MAX_PARTIALS, SPEC_NOALLOC_MAX_BATCH = 65536, 4096
 
 _TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
@@ -64,6 +64,9 @@ def _open(path: str):
     lib.spec_accept_greedy.restype = ctypes.c_int
     lib.spec_accept_greedy_noalloc.argtypes = [P, i32, P, i32, i32, i64, P, P, P]
     lib.spec_accept_greedy_noalloc.restype = ctypes.c_int
+    lib.spec_accept_rejection.argtypes = [P, P, i32, P, i32, i32, i64, ctypes.c_float,
+                                          ctypes.c_uint64, P, P, P]
+    lib.spec_accept_rejection.restype = ctypes.c_int
     lib.spec_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.spec_device_error.restype = ctypes.c_int
     lib.spec_release.restype = ctypes.c_int
@@ -147,6 +150,27 @@ def spec_accept_greedy_noalloc(logits, draft_tokens, num_draft: int, accepted_le
                                              _ptr(draft_tokens), B, num_draft, V,
                                              _ptr(accepted_len), _ptr(next_token),
                                              _stream(stream)))
+
+
+def spec_accept_rejection(target_logits, draft_logits, draft_tokens, num_draft: int,
+                          temperature: float, seed: int, accepted_len, next_token,
+                          stream=None) -> None:
+    """Rejection-sampling acceptance; writes ``accepted_len`` and ``next_token``.
+
+    target_logits [B, k+1, V], draft_logits [B, k, V] (same dtype), drafts
+    int32 [B, k]; draws from SplitMix64 keyed by ``seed``.
+    """
+    B, k1, V = target_logits.shape
+    if (k1 != num_draft + 1 or tuple(draft_logits.shape) != (B, num_draft, V)
+            or tuple(draft_tokens.shape) != (B, num_draft)):
+        raise ValueError("target_logits must be [B, k+1, V], draft_logits [B, k, V], drafts [B, k]")
+    if draft_logits.dtype != target_logits.dtype:
+        raise ValueError("target and draft logits must share a dtype")
+    _check(load().spec_accept_rejection(_ptr(target_logits), _ptr(draft_logits),
+                                        _TORCH_DT[target_logits.dtype], _ptr(draft_tokens), B,
+                                        num_draft, V, float(temperature),
+                                        int(seed) & (2**64 - 1), _ptr(accepted_len),
+                                        _ptr(next_token), _stream(stream)))
 
 
 def spec_device_error() -> int:

@@ -68,6 +68,15 @@ size_t accept_workspace_bytes(const AcceptArgs& a);
 cudaError_t launch_accept(const AcceptArgs& a, void* workspace, int32_t* tickets,
                           cudaStream_t stream);
 
+// ---- rejection-sampling acceptance (two launches; see accept_rejection.cu) ----
+size_t rejection_workspace_bytes(int B, int k, int64_t V);
+// `tickets` must hold B zeroed int32 (self-resetting across calls).
+cudaError_t launch_accept_rejection(const void* target, const void* draft, int32_t dtype,
+                                    const int32_t* draft_tokens, int B, int k, int64_t V,
+                                    float temperature, uint64_t seed, int32_t* accepted_len,
+                                    int32_t* next_token, void* workspace, int32_t* tickets,
+                                    int* dev_err, cudaStream_t stream);
+
 // Sets the thread-local error message of the C ABI; returns `code`.
 int set_error(int code, const char* msg);
 

@@ -2,6 +2,7 @@
 // workspace, path selection and launches on the caller's stream.  Every
 // entry point returns a status code; on an error nothing is enqueued and the
 // thread-local message says why.
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -277,6 +278,38 @@ int spec_accept_greedy(const void* logits, int32_t logits_dtype, const int32_t* 
     cudaError_t e = specv::launch_accept(a, static_cast<char*>(ws->base) + kHeader, tickets,
                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "accept_greedy launch");
+    return SPEC_OK;
+}
+
+int spec_accept_rejection(const void* target_logits, const void* draft_logits,
+                          int32_t logits_dtype, const int32_t* draft_tokens, int32_t batch,
+                          int32_t num_draft, int64_t vocab, float temperature, uint64_t seed,
+                          int32_t* accepted_len, int32_t* next_token, void* stream) {
+    g_err.clear();
+    if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
+    if (num_draft < 1 || num_draft > 64) return fail(SPEC_ERR_INVALID, "num_draft must be in [1, 64]");
+    if (vocab < 1 || vocab >= (1LL << 31)) return fail(SPEC_ERR_INVALID, "vocab must be in [1, 2^31)");
+    if (logits_dtype != SPEC_DTYPE_F32 && logits_dtype != SPEC_DTYPE_BF16)
+        return fail(SPEC_ERR_INVALID, "logits_dtype must be F32 or BF16");
+    if (!(temperature > 0.f) || !(temperature < INFINITY))
+        return fail(SPEC_ERR_INVALID, "temperature must be positive and finite");
+    if (batch == 0) return SPEC_OK;
+    if (batch > kMaxTickets) return fail(SPEC_ERR_UNSUPPORTED, "batch > %d", kMaxTickets);
+    if (!target_logits || !draft_logits || !draft_tokens || !accepted_len || !next_token)
+        return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    if (!aligned16(target_logits) || !aligned16(draft_logits))
+        return fail(SPEC_ERR_INVALID, "logits must be 16-byte aligned");
+    const int64_t units = (int64_t)batch * (2 * num_draft + 1) * ((vocab + 8191) / 8192);
+    if (units >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "logits too large");
+    Workspace* ws = nullptr;
+    int rc = get_workspace(specv::rejection_workspace_bytes(batch, num_draft, vocab), &ws);
+    if (rc) return rc;
+    int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws->base) + kTicketsOff);
+    cudaError_t e = specv::launch_accept_rejection(
+        target_logits, draft_logits, logits_dtype, draft_tokens, batch, num_draft, vocab,
+        temperature, seed, accepted_len, next_token, static_cast<char*>(ws->base) + kHeader,
+        tickets, static_cast<int*>(ws->base), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "accept_rejection launch");
     return SPEC_OK;
 }
 

@@ -290,3 +290,42 @@ def algorithmic_bytes(inp: VerifyInputs) -> dict:
     lg_elem = 4 if s.logits_dtype == "f32" else 2
     accept = B * (k + 1) * s.vocab * lg_elem + B * k * 4 + 2 * B * 4
     return {"attn": attn, "accept": accept, "total": attn + accept, "kv": kv}
+
+
+# ---------------------------------------------------------------- rejection-sampling inputs
+
+@dataclasses.dataclass
+class RejectionInputs:
+    """Seeded inputs of rejection-sampling acceptance (stored dtype bits as
+    in VerifyInputs: float32 arrays, or uint16 bf16 bits)."""
+    dtype: str
+    target_logits: np.ndarray  # [B, k+1, V]
+    draft_logits: np.ndarray   # [B, k, V]
+    draft_tokens: np.ndarray   # [B, k] int32, drawn from the drafter's distribution
+    temperature: float
+    seed: int                  # key of the verification draws
+
+
+def make_rejection_inputs(batch: int, num_draft: int, vocab: int, dtype: str = "bf16",
+                          seed: int = 0, sigma: float = math.sqrt(2.0), agreement: float = 0.8,
+                          temperature: float = 1.0) -> RejectionInputs:
+    """Target logits N(0, sigma^2); the drafter's logits are agreement * target
+    + sqrt(1 - agreement^2) * fresh noise (a drafter that mostly agrees); each
+    draft token is drawn from the drafter's softmax(logits / T) with numpy's
+    generator (input construction only)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x5EC]))
+    B, k, V = batch, num_draft, vocab
+    tl = rng.standard_normal((B, k + 1, V), dtype=np.float32) * np.float32(sigma)
+    noise = rng.standard_normal((B, k, V), dtype=np.float32) * np.float32(sigma)
+    a = np.float32(agreement)
+    dl = a * tl[:, :k] + np.float32(math.sqrt(max(0.0, 1.0 - agreement ** 2))) * noise
+    tl_s, dl_s = _round_to(tl, dtype), _round_to(dl.astype(np.float32), dtype)
+    # draft tokens ~ softmax(stored draft logits / T), by inverse CDF on float64
+    dq = _as_f32(dl_s, dtype).astype(np.float64) / temperature
+    dq -= dq.max(axis=-1, keepdims=True)
+    cdf = np.cumsum(np.exp(dq), axis=-1)
+    u = rng.random((B, k, 1)) * cdf[..., -1:]
+    drafts = np.minimum((cdf < u).sum(axis=-1), V - 1).astype(np.int32)
+    return RejectionInputs(dtype=dtype, target_logits=tl_s, draft_logits=dl_s,
+                           draft_tokens=np.ascontiguousarray(drafts), temperature=temperature,
+                           seed=int(rng.integers(0, 2**63)))

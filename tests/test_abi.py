@@ -96,6 +96,27 @@ def test_accept_rejects_bad_arguments(lib, bad, needle):
     assert needle in lib.spec_last_error().decode()
 
 
+@pytest.mark.parametrize("bad,needle", [
+    (dict(k=0), "num_draft"),
+    (dict(V=0), "vocab"),
+    (dict(dt=2), "logits_dtype"),
+    (dict(T=0.0), "temperature"),
+    (dict(T=float("nan")), "temperature"),
+    (dict(T=float("inf")), "temperature"),
+    (dict(dl=0), "null"),
+    (dict(tl=24), "aligned"),
+    (dict(dl=40), "aligned"),
+])
+def test_rejection_rejects_bad_arguments(lib, bad, needle):
+    a = dict(tl=16, dl=32, dt=1, draft=16, B=2, k=4, V=1000, T=1.0, acc=16, nxt=16)
+    a.update(bad)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    rc = lib.spec_accept_rejection(vp(a["tl"]), vp(a["dl"]), a["dt"], vp(a["draft"]), a["B"],
+                                   a["k"], a["V"], a["T"], 7, vp(a["acc"]), vp(a["nxt"]), None)
+    assert rc == -1
+    assert needle in lib.spec_last_error().decode()
+
+
 def test_options(lib):
     assert lib.spec_set_option(0, 4) == -1
     assert lib.spec_set_option(0, 3) == 0
