@@ -242,6 +242,21 @@ def run_gpu(args, inp, world, rank, local):
     units = s.batch * k
 
     base = binding.inputs_to_torch(inp, device)
+    rejection = args.accept == "rejection"
+    if rejection:
+        # lossless speculative sampling: seeded target and drafter logits of
+        # the workload's shape, drafts drawn from the drafter's distribution
+        from speculative_decoding_verification_attn_gb300.workload import make_rejection_inputs
+        rej = make_rejection_inputs(s.batch, k, s.vocab, s.logits_dtype, seed=inp.seed)
+        to_dev = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+                            if s.logits_dtype == "bf16" else torch.from_numpy(a)).to(device)
+        base["logits"] = to_dev(rej.target_logits)
+        base["draft_logits"] = to_dev(rej.draft_logits)
+        base["draft_tokens"] = torch.from_numpy(rej.draft_tokens).to(device)
+        nbytes = dict(nbytes)
+        extra = base["draft_logits"].numel() * base["draft_logits"].element_size()
+        nbytes["accept"] += extra
+        nbytes["total"] += extra
     # rotate over enough input copies that one step's inputs are out of L2
     # by the time they are used again
     n_sets = max(2, math.ceil(2.5 * L2_BYTES / nbytes["total"]))
@@ -249,9 +264,20 @@ def run_gpu(args, inp, world, rank, local):
     outs = [binding.alloc_outputs(inp, device) for _ in range(n_sets)]
     stream = torch.cuda.current_stream()
 
+    def accept(t, o, j):
+        if rejection:
+            binding.spec_accept_rejection(t["logits"], t["draft_logits"], t["draft_tokens"], k, 1.0,
+                                          rej.seed + j, o["accepted_len"], o["next_token"])
+        else:
+            binding.spec_accept_greedy(t["logits"], t["draft_tokens"], k, o["accepted_len"],
+                                       o["next_token"])
+
     def step(j):
         t, o = sets[j % n_sets], outs[j % n_sets]
-        binding.run_verify(t, o, k, scale)
+        binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                 t["ctx_lens"], k, scale, o["out"], o["lse"],
+                                 t.get("k_scale"), t.get("v_scale"))
+        accept(t, o, j)
 
     for j in range(max(args.warmup, 3)):
         step(j)
@@ -283,8 +309,7 @@ def run_gpu(args, inp, world, rank, local):
                                      t["ctx_lens"], k, scale, o["out"], o["lse"],
                                      t.get("k_scale"), t.get("v_scale"))
             ev[j][1].record(stream)
-            binding.spec_accept_greedy(t["logits"], t["draft_tokens"], k, o["accepted_len"],
-                                       o["next_token"])
+            accept(t, o, j)
             ev[j][2].record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -300,6 +325,11 @@ def run_gpu(args, inp, world, rank, local):
     # memory, results read back, every step
     host_names = ["q", "logits", "draft_tokens", "block_table", "ctx_lens"]
     host = binding.inputs_to_torch(inp, pin=True)
+    if rejection:
+        host_names.append("draft_logits")
+        host = dict(host)
+        for n in ("logits", "draft_logits", "draft_tokens"):
+            host[n] = base[n].cpu().pin_memory()
     h_in = {n: host[n] for n in host_names}
     h_out = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
              for n, v in outs[0].items()}
@@ -310,7 +340,7 @@ def run_gpu(args, inp, world, rank, local):
         t, o = sets[j % n_sets], outs[j % n_sets]
         for n in host_names:
             t[n].copy_(h_in[n], non_blocking=True)
-        binding.run_verify(t, o, k, scale)
+        step(j)
         for n, v in o.items():
             h_out[n].copy_(v, non_blocking=True)
 
@@ -339,16 +369,19 @@ def run_gpu(args, inp, world, rank, local):
                                   (n_sets, nbytes["total"] / 1e6)),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * launches_per_step(inp),
+        "gpu_launches": args.steps * (launches_per_step(inp) + (1 if rejection else 0)),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "spec_verify_attn (attention + split-KV combine)",
                      "peak_source": peak_kind, "attn_ms": attn_ms, "accept_ms": acc_ms,
                      "attn_bytes": nbytes["attn"], "step_bytes": nbytes["total"],
+                     "accept_GBps": nbytes["accept"] / (acc_ms / 1e3) / 1e9,
                      "step_frac": nbytes["total"] / (ms_per_step / 1e3) / 1e9 / peak},
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rejection:
+        line["config"]["accept"] = "rejection sampling (T = 1, SplitMix64 draws, fresh seed per step)"
+    if rank == 0 and not args.no_cpu_baseline and not rejection:
         t_cpu, desc = oracle_step_estimate(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": units / t_cpu, "unit": UNIT, "cores": 1,
                                 "kind": "oracle", "sample": desc}
@@ -379,6 +412,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--accept", choices=["greedy", "rejection"], default="greedy",
+                    help="acceptance rule of the step (greedy: the headline configuration)")
     args = ap.parse_args(argv)
 
     world, rank, local = dist_env()

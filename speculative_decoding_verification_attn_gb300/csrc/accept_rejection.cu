@@ -15,7 +15,7 @@
 // argmax_x ln w(x) + g(x), lowest index on ties.
 //
 // Two launches, both HBM-bound:
-//  1. rows: one CTA per (row, 8192-entry slice) of the k+1 target and k
+//  1. rows: one CTA per (row, 2048-entry slice) of the k+1 target and k
 //     draft rows of every sequence: online (max, sum of exp) of logits / T,
 //     and on the target's bonus row the Gumbel-max partial.  The CTA taking
 //     the last ticket of a sequence turns the partials into log-sum-exps,
@@ -27,6 +27,7 @@
 #include <limits.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -34,7 +35,8 @@ namespace specv {
 namespace {
 
 constexpr int kRThreads = 256;
-constexpr int kRSlice = 8192;  // vocabulary entries per CTA
+constexpr int kRSlice = 2048;  // vocabulary entries per CTA (many small CTAs balance the
+                               // Gumbel-heavy rows against the plain ones)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -52,10 +54,13 @@ __device__ __forceinline__ float unif_co(uint64_t z) { return (float)(z >> 40) *
 __device__ __forceinline__ float unif_oo(uint64_t z) {
     return (float)((z >> 41) * 2 + 1) * 0x1p-24f;
 }
+// -ln(-ln u): the inner logarithm is accurate (the largest keys come from u
+// near 1, where -ln u is small); the outer one is the fast hardware form,
+// whose absolute error (~1e-6 on keys of ~10) is far below key gaps that
+// decide a draw
 __device__ __forceinline__ float gumbel(uint64_t seed, int b, int64_t x) {
-    return -logf(-logf(unif_oo(sm64_at(seed, draw_index(b, 1, x)))));
+    return -__logf(-logf(unif_oo(sm64_at(seed, draw_index(b, 1, x)))));
 }
-
 // (key, index) beats (bk, bi): larger key, or equal key and lower index
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
@@ -86,27 +91,97 @@ struct RejArgs {
     int* dev_err;
 };
 
-// Visits the elements [e0, e1) of row x, each thread in increasing index
-// order: 16-byte loads when the row is aligned, scalar head/tail otherwise.
-template <typename T, typename F>
-__device__ __forceinline__ void for_slice(const T* x, int64_t e0, int64_t e1, F&& f) {
-    constexpr int VEC = 16 / sizeof(T);
-    const int tid = threadIdx.x;
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(x + e0);
-    int64_t head = (int64_t)(((16 - (addr & 15)) & 15) / sizeof(T));
-    if (head > e1 - e0) head = e1 - e0;
-    if (tid < head) f(e0 + tid, to_f(x[e0 + tid]));
-    const int64_t eb = e0 + head;
-    const int64_t nvec = (e1 - eb) / VEC;
-    const uint4* xv = reinterpret_cast<const uint4*>(x + eb);
-    for (int64_t vi = tid; vi < nvec; vi += kRThreads) {
-        const uint4 raw = __ldcs(xv + vi);
-        const T* el = reinterpret_cast<const T*>(&raw);
-#pragma unroll
-        for (int q = 0; q < VEC; ++q) f(eb + vi * VEC + q, to_f(el[q]));
+// A slice is C chunks of kRSlice entries; the host takes C = 4 for large
+// vocabularies (fewer, longer CTAs) and C = 1 otherwise (enough CTAs for the
+// Gumbel-heavy rows to spread).  Vector path: the slice starts on a 16-byte
+// boundary and holds whole 16-byte vectors; otherwise one entry at a time.
+template <typename T, int C>
+struct Slice {
+    static constexpr int VEC = 16 / sizeof(T);
+    static constexpr int PER = C * kRSlice / VEC / kRThreads;  // 16-byte loads per thread
+    static __device__ __forceinline__ bool vector_path(const T* x, int64_t e0, int64_t e1) {
+        return (reinterpret_cast<uintptr_t>(x + e0) & 15) == 0 && (e1 - e0) % VEC == 0;
     }
-    const int64_t et = eb + nvec * VEC;
-    if (et + tid < e1) f(et + tid, to_f(x[et + tid]));
+};
+
+// (max, sum of exp) of logits / T over a slice: every load first, then the
+// max, then the sum (no per-element branch)
+template <typename T, int C>
+__device__ __forceinline__ Lse slice_lse(const T* x, int64_t e0, int64_t e1, float inv_t) {
+    using S = Slice<T, C>;
+    const int tid = threadIdx.x;
+    if (S::vector_path(x, e0, e1)) {
+        const int nvec = (int)((e1 - e0) / S::VEC);
+        const uint4* xv = reinterpret_cast<const uint4*>(x + e0);
+        uint4 raw[S::PER];
+#pragma unroll
+        for (int u = 0; u < S::PER; ++u) {
+            const int vi = tid + u * kRThreads;
+            raw[u] = vi < nvec ? __ldcs(xv + vi) : make_uint4(0, 0, 0, 0);
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < S::PER; ++u) {
+            if (tid + u * kRThreads >= nvec) continue;
+            const T* el = reinterpret_cast<const T*>(&raw[u]);
+#pragma unroll
+            for (int q = 0; q < S::VEC; ++q) m = fmaxf(m, to_f(el[q]) * inv_t);
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < S::PER; ++u) {
+            if (tid + u * kRThreads >= nvec) continue;
+            const T* el = reinterpret_cast<const T*>(&raw[u]);
+#pragma unroll
+            for (int q = 0; q < S::VEC; ++q) sum += __expf(to_f(el[q]) * inv_t - m);
+        }
+        return {m, sum};
+    }
+    Lse acc = {-INFINITY, 0.f};
+    for (int64_t e = e0 + tid; e < e1; e += kRThreads) {
+        const float l = to_f(x[e]) * inv_t;
+        if (l > acc.m) {
+            acc.s = acc.s * __expf(acc.m - l) + 1.f;  // exp(-inf) = 0 on the first element
+            acc.m = l;
+        } else {
+            acc.s += __expf(l - acc.m);
+        }
+    }
+    return acc;
+}
+
+// Visits the entries [e0, e1) of row xp and the same entries of row xq (if
+// given), each thread in increasing index order: f(e, p, q).  For the
+// Gumbel-heavy passes: one 16-byte vector per step, the next one in flight
+// while the current one is processed (no unrolling across vectors).
+template <typename T, int C, typename F>
+__device__ __forceinline__ void walk_slice(const T* xp, const T* xq, int64_t e0, int64_t e1, F&& f) {
+    using S = Slice<T, C>;
+    const int tid = threadIdx.x;
+    if (S::vector_path(xp, e0, e1) && (!xq || S::vector_path(xq, e0, e1))) {
+        const int nvec = (int)((e1 - e0) / S::VEC);
+        const uint4* pv = reinterpret_cast<const uint4*>(xp + e0);
+        const uint4* qv = xq ? reinterpret_cast<const uint4*>(xq + e0) : nullptr;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        int vi = tid;
+        uint4 cp = vi < nvec ? __ldcs(pv + vi) : z;
+        uint4 cq = (qv && vi < nvec) ? __ldcs(qv + vi) : z;
+#pragma unroll 1
+        for (; vi < nvec; vi += kRThreads) {
+            const int vn = vi + kRThreads;
+            const uint4 np = vn < nvec ? __ldcs(pv + vn) : z;
+            const uint4 nq = (qv && vn < nvec) ? __ldcs(qv + vn) : z;
+            const T* ep = reinterpret_cast<const T*>(&cp);
+            const T* eq = reinterpret_cast<const T*>(&cq);
+#pragma unroll
+            for (int q = 0; q < S::VEC; ++q) f(e0 + (int64_t)vi * S::VEC + q, to_f(ep[q]), to_f(eq[q]));
+            cp = np;
+            cq = nq;
+        }
+        return;
+    }
+    for (int64_t e = e0 + tid; e < e1; e += kRThreads)
+        f(e, to_f(xp[e]), xq ? to_f(xq[e]) : 0.f);
 }
 
 // CTA-wide reductions; results valid in every thread
@@ -142,47 +217,48 @@ __device__ __forceinline__ KeyPair merge_key(KeyPair x, KeyPair y) {
     return better(y.a, y.b, x.a, x.b) ? y : x;
 }
 
-template <typename T>
+// grid (slices, 2k+1 rows, B): row r <= k is target row r, r > k draft row r-k-1
+template <typename T, int C>
 __global__ void __launch_bounds__(kRThreads)
-rej_rows_kernel(RejArgs a, int ns, float2* __restrict__ part_ms, float* __restrict__ part_gk,
+rej_rows_kernel(RejArgs a, float2* __restrict__ part_ms, float* __restrict__ part_gk,
                 int* __restrict__ part_gi, int4* __restrict__ state, int32_t* __restrict__ tickets) {
     __shared__ LsePair s_lse[kRThreads / 32];
     __shared__ KeyPair s_key[kRThreads / 32];
     __shared__ float s_row_lse[129];  // 2k + 1 <= 129 rows
     __shared__ int s_last, s_first_fail;
 
-    const int rows = 2 * a.k + 1;
-    const int64_t unit = blockIdx.x;
-    const int slice = (int)(unit % ns);
-    const int r = (int)((unit / ns) % rows);
-    const int b = (int)(unit / ns / rows);
+    const int ns = gridDim.x, rows = gridDim.y;
+    const int slice = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
     const bool is_target = r <= a.k, bonus = r == a.k;
     const T* x = is_target
                      ? static_cast<const T*>(a.target) + ((int64_t)b * (a.k + 1) + r) * a.V
                      : static_cast<const T*>(a.draft) + ((int64_t)b * a.k + (r - a.k - 1)) * a.V;
-    const int64_t e0 = (int64_t)slice * kRSlice, e1 = min(a.V, e0 + (int64_t)kRSlice);
+    const int64_t sl = (int64_t)C * kRSlice;
+    const int64_t e0 = (int64_t)slice * sl, e1 = min(a.V, e0 + sl);
 
     Lse acc = {-INFINITY, 0.f};
     float bk = -INFINITY;
     int bi = INT_MAX;
-    for_slice(x, e0, e1, [&](int64_t e, float v) {
-        const float l = v * a.inv_t;
-        if (l > acc.m) {
-            acc.s = acc.s * __expf(acc.m - l) + 1.f;  // exp(-inf) = 0 on the first element
-            acc.m = l;
-        } else {
-            acc.s += __expf(l - acc.m);
-        }
-        if (bonus) {
+    if (!bonus) {
+        acc = slice_lse<T, C>(x, e0, e1, a.inv_t);
+    } else {
+        walk_slice<T, C>(x, (const T*)nullptr, e0, e1, [&](int64_t e, float v, float) {
+            const float l = v * a.inv_t;
+            if (l > acc.m) {
+                acc.s = acc.s * __expf(acc.m - l) + 1.f;
+                acc.m = l;
+            } else {
+                acc.s += __expf(l - acc.m);
+            }
             const float key = l + gumbel(a.seed, b, e);
             if (better(key, (int)e, bk, bi)) { bk = key; bi = (int)e; }
-        }
-    });
+        });
+    }
     const LsePair tot = block_reduce(LsePair{acc.m, acc.s}, s_lse, merge_lse);
     KeyPair best = {bk, bi};
     if (bonus) best = block_reduce(best, s_key, merge_key);
     if (threadIdx.x == 0) {
-        part_ms[unit] = make_float2(tot.a, tot.b);
+        part_ms[((int64_t)b * rows + r) * ns + slice] = make_float2(tot.a, tot.b);
         if (bonus) {
             part_gk[(int64_t)b * ns + slice] = best.a;
             part_gi[(int64_t)b * ns + slice] = best.b;
@@ -194,7 +270,6 @@ rej_rows_kernel(RejArgs a, int ns, float2* __restrict__ part_ms, float* __restri
     }
     __syncthreads();
     if (!s_last) return;
-
     // ---- last CTA of sequence b: log-sum-exp of every row, then the tests
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int rr = warp; rr < rows; rr += kRThreads / 32) {
@@ -260,27 +335,28 @@ rej_rows_kernel(RejArgs a, int ns, float2* __restrict__ part_ms, float* __restri
     if (tid == 0) tickets[b] = 0;  // ready for the residual launch / the next call
 }
 
-template <typename T>
+// grid (slices, B)
+template <typename T, int C>
 __global__ void __launch_bounds__(kRThreads)
-rej_residual_kernel(RejArgs a, int ns, const int4* __restrict__ state, float* __restrict__ part_k,
+rej_residual_kernel(RejArgs a, const int4* __restrict__ state, float* __restrict__ part_k,
                     int* __restrict__ part_i, int32_t* __restrict__ tickets) {
     __shared__ KeyPair s_key[kRThreads / 32];
     __shared__ int s_last;
-    const int b = blockIdx.x / ns, slice = blockIdx.x % ns;
+    const int ns = gridDim.x;
+    const int slice = blockIdx.x, b = blockIdx.y;
     const int4 st = __ldcg(state + b);
     const int n = st.x;
     if (n >= a.k) return;  // every draft kept: nothing to draw here
     const float lse_p = __int_as_float(st.y), lse_q = __int_as_float(st.z);
     const T* xp = static_cast<const T*>(a.target) + ((int64_t)b * (a.k + 1) + n) * a.V;
     const T* xq = static_cast<const T*>(a.draft) + ((int64_t)b * a.k + n) * a.V;
-    const int64_t e0 = (int64_t)slice * kRSlice, e1 = min(a.V, e0 + (int64_t)kRSlice);
+    const int64_t sl = (int64_t)C * kRSlice;
+    const int64_t e0 = (int64_t)slice * sl, e1 = min(a.V, e0 + sl);
     float bk = -INFINITY;
     int bi = INT_MAX;
-    // the target row in order; the draft value of the same entry by a plain load
-    for_slice(xp, e0, e1, [&](int64_t e, float v) {
-        const float p = __expf(v * a.inv_t - lse_p);
-        const float q = __expf(to_f(xq[e]) * a.inv_t - lse_q);
-        const float w = p - q;
+    walk_slice<T, C>(xp, xq, e0, e1, [&](int64_t e, float v, float vq) {
+        // ln(p - q) + g where p > q
+        const float w = __expf(v * a.inv_t - lse_p) - __expf(vq * a.inv_t - lse_q);
         if (w > 0.f) {
             const float key = logf(w) + gumbel(a.seed, b, e);
             if (better(key, (int)e, bk, bi)) { bk = key; bi = (int)e; }
@@ -300,8 +376,8 @@ rej_residual_kernel(RejArgs a, int ns, const int4* __restrict__ state, float* __
     const int lane = threadIdx.x & 31;
     if (threadIdx.x < 32) {
         KeyPair v = {-INFINITY, INT_MAX};
-        for (int sl = lane; sl < ns; sl += 32)
-            v = merge_key(v, {__ldcg(part_k + (int64_t)b * ns + sl), __ldcg(part_i + (int64_t)b * ns + sl)});
+        for (int q = lane; q < ns; q += 32)
+            v = merge_key(v, {__ldcg(part_k + (int64_t)b * ns + q), __ldcg(part_i + (int64_t)b * ns + q)});
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             KeyPair w;
@@ -316,7 +392,14 @@ rej_residual_kernel(RejArgs a, int ns, const int4* __restrict__ state, float* __
     }
 }
 
-int rej_slices(int64_t V) { return (int)((V + kRSlice - 1) / kRSlice); }
+// chunks per slice: long CTAs for large vocabularies, short ones otherwise
+int rej_chunks(int64_t V) { return V >= 65536 ? 4 : 1; }
+int rej_slices(int64_t V) {
+    const int64_t sl = (int64_t)rej_chunks(V) * kRSlice;
+    return (int)((V + sl - 1) / sl);
+}
+
+
 
 }  // namespace
 
@@ -357,16 +440,22 @@ cudaError_t launch_accept_rejection(const void* target, const void* draft, int32
     w += (size_t)B * ns * sizeof(int);
     w = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(w) + 15) & ~uintptr_t(15));
     int4* state = reinterpret_cast<int4*>(w);
-    if (dtype == SPEC_DTYPE_F32) {
-        rej_rows_kernel<float><<<(unsigned)units, kRThreads, 0, stream>>>(a, ns, part_ms, part_k,
+    const int rows = 2 * k + 1;
+    auto go = [&](auto tag, auto ctag) {
+        using T = decltype(tag);
+        constexpr int C = decltype(ctag)::value;
+        rej_rows_kernel<T, C><<<dim3(ns, rows, B), kRThreads, 0, stream>>>(a, part_ms, part_k,
                                                                           part_i, state, tickets);
-        rej_residual_kernel<float><<<(unsigned)(B * ns), kRThreads, 0, stream>>>(a, ns, state, part_k,
-                                                                               part_i, tickets);
+        rej_residual_kernel<T, C><<<dim3(ns, B), kRThreads, 0, stream>>>(a, state, part_k, part_i,
+                                                                       tickets);
+    };
+    using C1 = std::integral_constant<int, 1>;
+    using C4 = std::integral_constant<int, 4>;
+    const bool big = rej_chunks(V) == 4;
+    if (dtype == SPEC_DTYPE_F32) {
+        if (big) go(float(), C4()); else go(float(), C1());
     } else {
-        rej_rows_kernel<__nv_bfloat16><<<(unsigned)units, kRThreads, 0, stream>>>(
-            a, ns, part_ms, part_k, part_i, state, tickets);
-        rej_residual_kernel<__nv_bfloat16><<<(unsigned)(B * ns), kRThreads, 0, stream>>>(
-            a, ns, state, part_k, part_i, tickets);
+        if (big) go(__nv_bfloat16(), C4()); else go(__nv_bfloat16(), C1());
     }
     return cudaGetLastError();
 }

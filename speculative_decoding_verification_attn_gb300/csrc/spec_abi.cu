@@ -299,7 +299,7 @@ int spec_accept_rejection(const void* target_logits, const void* draft_logits,
         return fail(SPEC_ERR_INVALID, "null tensor pointer");
     if (!aligned16(target_logits) || !aligned16(draft_logits))
         return fail(SPEC_ERR_INVALID, "logits must be 16-byte aligned");
-    const int64_t units = (int64_t)batch * (2 * num_draft + 1) * ((vocab + 8191) / 8192);
+    const int64_t units = (int64_t)batch * (2 * num_draft + 1) * ((vocab + 2047) / 2048);
     if (units >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "logits too large");
     Workspace* ws = nullptr;
     int rc = get_workspace(specv::rejection_workspace_bytes(batch, num_draft, vocab), &ws);
