@@ -12,6 +12,10 @@ computes and which passage of the pages it follows:
   Compression".
 * ``accept_greedy`` -- first-disagreement acceptance plus bonus token (same
   blog, "Speculating to get sequence parallelism during decode").
+* ``kv_append`` / ``quantize_rows`` / ``commit`` -- the drafts' K/V rows
+  written into the paged cache (INT8: CXL-SpecKV's "Algorithm 2 KV-Cache
+  Compression", per (token, kv-head) row) and HeteroReason's KVMU Accept
+  pointer move.
 * ``accept_rejection`` -- lossless rejection-sampling acceptance (same blog,
   "How does this drafter maintain the same distribution of the target?"),
   with its draws from the counter-based generator SplitMix64.
@@ -58,6 +62,13 @@ def _load():
         lib.oracle_accept_uniform.restype = ctypes.c_double
         lib.oracle_gumbel.argtypes = [u64, i32, ctypes.c_int64]
         lib.oracle_gumbel.restype = ctypes.c_double
+        lib.oracle_quantize_rows.argtypes = [P, i32, ctypes.c_int64, i32, P, P]
+        lib.oracle_quantize_rows.restype = i32
+        lib.oracle_kv_append.argtypes = [P, P, i32, P, P, P, P, i32, P, P, i32, i32, i32, i32,
+                                         i32, i32, i32]
+        lib.oracle_kv_append.restype = i32
+        lib.oracle_commit.argtypes = [P, P, i32, i32]
+        lib.oracle_commit.restype = i32
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -164,6 +175,45 @@ def accept_rejection(target_logits, draft_logits, dtype, draft_tokens, temperatu
     return acc, nxt, ratio, unif, gap
 
 
+def quantize_rows(x, dtype):
+    """Rows x [..., D] (f32 array or bf16 bits) -> (codes int8 [..., D], scale fp16 bits [...])."""
+    x = np.ascontiguousarray(x)
+    D = x.shape[-1]
+    n = x.size // D
+    codes = np.zeros(x.shape, np.int8)
+    scales = np.zeros(x.shape[:-1], np.uint16)
+    rc = _load().oracle_quantize_rows(_ptr(x), DTYPES[dtype], n, D, _ptr(codes), _ptr(scales))
+    if rc:
+        raise ValueError("oracle_quantize_rows failed (%d)" % rc)
+    return codes, scales
+
+
+def kv_append(k_new, v_new, src_dtype, k_cache, v_cache, k_scale, v_scale, cache_dtype,
+              block_table, ctx_lens):
+    """Return copies of (k_cache, v_cache, k_scale, v_scale) with the rows
+    k_new / v_new [B, n, Hkv, D] written at positions ctx_b .. ctx_b + n - 1."""
+    B, n, Hkv, D = k_new.shape
+    NP, Hkv2, P, D2 = k_cache.shape
+    assert (Hkv2, D2) == (Hkv, D) and v_new.shape == k_new.shape
+    kc, vc = k_cache.copy(), v_cache.copy()
+    ks = None if k_scale is None else k_scale.copy()
+    vs = None if v_scale is None else v_scale.copy()
+    rc = _load().oracle_kv_append(_ptr(np.ascontiguousarray(k_new)), _ptr(np.ascontiguousarray(v_new)),
+                                  DTYPES[src_dtype], _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                  DTYPES[cache_dtype], _ptr(block_table), _ptr(ctx_lens), B, n,
+                                  Hkv, D, P, NP, block_table.shape[1])
+    if rc:
+        raise ValueError("oracle_kv_append failed (%d)" % rc)
+    return kc, vc, ks, vs
+
+
+def commit(ctx_lens, accepted_len, extra=1):
+    out = np.ascontiguousarray(ctx_lens, np.int32).copy()
+    acc = np.ascontiguousarray(accepted_len, np.int32)
+    _load().oracle_commit(_ptr(out), _ptr(acc), len(out), int(extra))
+    return out
+
+
 def splitmix64(seed: int, n: int) -> int:
     """The n-th (0-based) output of SplitMix64 seeded with `seed`."""
     return int(_load().oracle_splitmix64(int(seed) & (2**64 - 1), int(n)))
@@ -185,5 +235,6 @@ def f16_bits_to_f64(bits: int) -> float:
     return _load().oracle_f16_to_f64(int(bits))
 
 
-__all__ = ["verify_attn", "attn_rows", "accept_greedy", "accept_rejection", "splitmix64",
+__all__ = ["verify_attn", "attn_rows", "accept_greedy", "accept_rejection", "quantize_rows",
+           "kv_append", "commit", "splitmix64",
            "accept_uniform", "gumbel", "bf16_bits_to_f64", "f16_bits_to_f64", "DTYPES"]

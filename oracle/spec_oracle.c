@@ -360,3 +360,128 @@ int oracle_accept_rejection(const void *target, const void *draft_logits, int dt
     }
     return 0;
 }
+
+/*
+ * 4. Writing the drafts' K/V rows into the paged cache, and the commit.
+ *
+ *    The drafted positions ctx_b .. ctx_b + n - 1 of sequence b get the new
+ *    rows k_new / v_new [B, n, Hkv, D] (f32 or bf16) at page
+ *    block_table[b][pos / P], slot pos % P.  An f32 or bf16 cache stores the
+ *    value (bf16 rounded to nearest even); an INT8 cache stores the
+ *    quantised row of CXL-SpecKV's "Algorithm 2 KV-Cache Compression" (steps
+ *    "Scaling" and "Quantization"), per (token, kv-head) row:
+ *      s = fp16(max_d |x_d| / 127), c_d = clamp(rint(x_d / s), -127, 127),
+ *      and c = 0 when s = 0.
+ *    The quantiser decides integers, so it takes the kernel's precision:
+ *    every step in fp32 (IEEE division, round half to even), the scale
+ *    rounded to binary16 by round-to-nearest-even.
+ *
+ *    The commit is the KVMU's Accept pointer move (HeteroReason, KV Cache
+ *    Management Unit): the validated length of sequence b grows by its
+ *    accepted drafts (plus `extra`, 1 when the emitted token's row is counted
+ *    too); rejected drafts are not advanced over, so the next step's append
+ *    overwrites them (the Rollback).
+ */
+
+/* float -> IEEE binary16 bits, round to nearest even; overflow -> inf. */
+static uint16_t f32_to_f16_bits(float f) {
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    const double v = fabs((double)f);
+    if (v != v) return sign | 0x7e00u;
+    if (v >= 65520.0) return sign | 0x7c00u;          /* beyond the largest finite half */
+    if (v < ldexp(1.0, -14)) {                        /* subnormal range: multiples of 2^-24 */
+        const double r = rint(v * ldexp(1.0, 24));     /* exact scaling, round half even */
+        return sign | (uint16_t)r;                     /* r == 1024 is the smallest normal */
+    }
+    int e2;
+    frexp(v, &e2);                                    /* v in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;
+    double r = rint(ldexp(v, 10 - E));                /* in [1024, 2048] */
+    if (r == 2048.0) { r = 1024.0; E += 1; }
+    if (E + 15 >= 31) return sign | 0x7c00u;
+    return sign | (uint16_t)(((E + 15) << 10) | ((int)r - 1024));
+}
+
+/* float -> bfloat16 bits, round to nearest even (finite inputs). */
+static uint16_t f32_to_bf16_bits(float f) {
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    return (uint16_t)((x + 0x7fffu + ((x >> 16) & 1u)) >> 16);
+}
+
+static void quantize_row(const void *src, int src_dtype, int64_t off, int D, int8_t *codes,
+                         uint16_t *scale_bits) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        const float v = fabsf((float)load_f64(src, src_dtype, off + d));
+        if (v > amax) amax = v;
+    }
+    const float sf = amax / 127.0f;
+    const uint16_t sb = f32_to_f16_bits(sf);
+    const float s = (float)f16_to_f64(sb);
+    for (int d = 0; d < D; ++d) {
+        float c = 0.0f;
+        if (s > 0.0f) {
+            const float q = (float)load_f64(src, src_dtype, off + d) / s;
+            c = rintf(q);
+            if (c > 127.0f) c = 127.0f;
+            if (c < -127.0f) c = -127.0f;
+        }
+        codes[d] = (int8_t)c;
+    }
+    *scale_bits = sb;
+}
+
+/* Rows [n, D] of src -> codes [n, D] int8 and scale bits [n] (fp16). */
+int oracle_quantize_rows(const void *src, int src_dtype, int64_t n, int D, int8_t *codes,
+                         uint16_t *scale_bits) {
+    if (n < 0 || D < 1) return -1;
+    for (int64_t r = 0; r < n; ++r)
+        quantize_row(src, src_dtype, r * D, D, codes + r * D, scale_bits + r);
+    return 0;
+}
+
+int oracle_kv_append(const void *k_new, const void *v_new, int src_dtype, void *k_cache,
+                     void *v_cache, uint16_t *k_scale, uint16_t *v_scale, int cache_dtype,
+                     const int32_t *block_table, const int32_t *ctx_lens, int B, int n_new,
+                     int Hkv, int D, int P, int num_pages, int max_pages) {
+    if (B < 0 || n_new < 1 || Hkv < 1 || D < 1 || P < 1) return -1;
+    if (src_dtype != ORC_F32 && src_dtype != ORC_BF16) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < n_new; ++t) {
+            const int64_t pos = (int64_t)ctx_lens[b] + t;
+            if (pos < 0 || pos / P >= max_pages) return -1;
+            const int32_t page = block_table[(int64_t)b * max_pages + pos / P];
+            if (page < 0 || page >= num_pages) return -1;
+            for (int g = 0; g < Hkv; ++g) {
+                const int64_t srow = (((int64_t)b * n_new + t) * Hkv + g) * D;
+                const int64_t crow = (((int64_t)page * Hkv + g) * P + pos % P);
+                for (int tensor = 0; tensor < 2; ++tensor) {
+                    const void *src = tensor ? v_new : k_new;
+                    void *cache = tensor ? v_cache : k_cache;
+                    if (cache_dtype == ORC_I8) {
+                        uint16_t *sc = tensor ? v_scale : k_scale;
+                        quantize_row(src, src_dtype, srow, D, (int8_t *)cache + crow * D, sc + crow);
+                    } else {
+                        for (int d = 0; d < D; ++d) {
+                            const float v = (float)load_f64(src, src_dtype, srow + d);
+                            if (cache_dtype == ORC_F32)
+                                ((float *)cache)[crow * D + d] = v;
+                            else if (cache_dtype == ORC_BF16)
+                                ((uint16_t *)cache)[crow * D + d] = f32_to_bf16_bits(v);
+                            else
+                                return -1;
+                        }
+                    }
+                }
+            }
+        }
+    return 0;
+}
+
+int oracle_commit(int32_t *ctx_lens, const int32_t *accepted_len, int B, int extra) {
+    for (int b = 0; b < B; ++b) ctx_lens[b] += accepted_len[b] + extra;
+    return 0;
+}
