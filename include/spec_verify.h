@@ -229,6 +229,42 @@ SPEC_API int spec_accept_rejection(const void *target_logits, const void *draft_
                                    float temperature, uint64_t seed, int32_t *accepted_len,
                                    int32_t *next_token, void *stream);
 
+/*
+ * Write the drafts' K/V rows into the paged cache (the step before
+ * verification: the target's projections of the k drafted tokens).
+ *
+ * Positions ctx_b .. ctx_b + num_new - 1 of sequence b receive rows
+ * k_new / v_new [batch, num_new, num_kv_heads, head_dim] (src_dtype F32 |
+ * BF16) at page block_table[b, pos / page_size], slot pos % page_size.
+ *   - F32 / BF16 cache: the value (bf16 rounded to nearest even);
+ *   - I8 cache: CXL-SpecKV's "Algorithm 2 KV-Cache Compression" per
+ *     (token, kv-head) row: s = fp16(max_d |x_d| / 127) into k_scale /
+ *     v_scale [num_pages, num_kv_heads, page_size], c_d = clamp(rint(x_d / s),
+ *     -127, 127) (c = 0 when s = 0), every step in fp32 (IEEE division,
+ *     round half to even), fp16 by round-to-nearest-even.
+ * Caches, scales and tables as in spec_verify_attn; ctx_lens is not changed
+ * (spec_commit moves it).  A position past the block table or a page id
+ * outside [0, num_pages) writes nothing and sets SPEC_DEVERR_CTX /
+ * SPEC_DEVERR_PAGE.  Limits: head_dim % 32 == 0 and <= 256; num_new >= 1.
+ */
+SPEC_API int spec_kv_append(const void *k_new, const void *v_new, int32_t src_dtype,
+                            void *k_cache, void *v_cache, void *k_scale, void *v_scale,
+                            int32_t cache_dtype, const int32_t *block_table,
+                            const int32_t *ctx_lens, int32_t batch, int32_t num_new,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                            int32_t num_pages, int32_t max_pages_per_seq, void *stream);
+
+/*
+ * Commit a verification step on the device: ctx_lens[b] += accepted_len[b]
+ * + extra (HeteroReason's KV Cache Management Unit, "Accept" mode: the
+ * validated pointer moves over the accepted drafts; pass extra = 1 to count
+ * the emitted correction / bonus token as well, once its row is appended).
+ * Rejected drafts are left behind and the next spec_kv_append overwrites
+ * them ("Rollback").  ctx_lens and accepted_len are device int32 [batch].
+ */
+SPEC_API int spec_commit(int32_t *ctx_lens, const int32_t *accepted_len, int32_t batch,
+                         int32_t extra, void *stream);
+
 /* Read and clear the device error word of the current device (synchronises
  * the device).  0 = no fault seen; otherwise a bitwise OR of SPEC_DEVERR_*. */
 SPEC_API int spec_device_error(int32_t *flags);

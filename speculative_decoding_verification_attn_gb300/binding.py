@@ -25,7 +25,7 @@ SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT, SPEC_DEVERR_TOKEN = 1, 2
 # every symbol the public header declares
 EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
             "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_accept_rejection",
-            "spec_device_error", "spec_release"]
+            "spec_kv_append", "spec_commit", "spec_device_error", "spec_release"]
 SPEC_NOALLOC_MAX_PARTIALS, SPEC_NOALLOC_MAX_BATCH = 65536, 4096
 
 _TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
@@ -67,6 +67,11 @@ def _open(path: str):
     lib.spec_accept_rejection.argtypes = [P, P, i32, P, i32, i32, i64, ctypes.c_float,
                                           ctypes.c_uint64, P, P, P]
     lib.spec_accept_rejection.restype = ctypes.c_int
+    lib.spec_kv_append.argtypes = [P, P, i32, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                   i32, P]
+    lib.spec_kv_append.restype = ctypes.c_int
+    lib.spec_commit.argtypes = [P, P, i32, i32, P]
+    lib.spec_commit.restype = ctypes.c_int
     lib.spec_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.spec_device_error.restype = ctypes.c_int
     lib.spec_release.restype = ctypes.c_int
@@ -171,6 +176,26 @@ def spec_accept_rejection(target_logits, draft_logits, draft_tokens, num_draft: 
                                         num_draft, V, float(temperature),
                                         int(seed) & (2**64 - 1), _ptr(accepted_len),
                                         _ptr(next_token), _stream(stream)))
+
+
+def spec_kv_append(k_new, v_new, k_cache, v_cache, block_table, ctx_lens, k_scale=None,
+                   v_scale=None, stream=None) -> None:
+    """Write k_new / v_new [B, n, Hkv, D] at positions ctx_b .. ctx_b + n - 1 of
+    the paged caches (INT8 caches are quantised into k_scale / v_scale)."""
+    B, n, Hkv, D = k_new.shape
+    NP, Hkv2, P, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new / v_new must be [B, n, Hkv, D] matching the cache")
+    _check(load().spec_kv_append(_ptr(k_new), _ptr(v_new), _TORCH_DT[k_new.dtype], _ptr(k_cache),
+                                 _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                 _TORCH_DT[k_cache.dtype], _ptr(block_table), _ptr(ctx_lens), B,
+                                 n, Hkv, D, P, NP, block_table.shape[1], _stream(stream)))
+
+
+def spec_commit(ctx_lens, accepted_len, extra: int = 1, stream=None) -> None:
+    """ctx_lens[b] += accepted_len[b] + extra, on the device."""
+    _check(load().spec_commit(_ptr(ctx_lens), _ptr(accepted_len), ctx_lens.shape[0], int(extra),
+                              _stream(stream)))
 
 
 def spec_device_error() -> int:

@@ -77,6 +77,15 @@ cudaError_t launch_accept_rejection(const void* target, const void* draft, int32
                                     int32_t* next_token, void* workspace, int32_t* tickets,
                                     int* dev_err, cudaStream_t stream);
 
+// ---- drafts' K/V append (INT8 quantisation) and the commit ----
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, int32_t src_dtype,
+                             void* k_cache, void* v_cache, uint16_t* k_scale, uint16_t* v_scale,
+                             int32_t cache_dtype, const int32_t* block_table,
+                             const int32_t* ctx_lens, int B, int n, int Hkv, int D, int P,
+                             int num_pages, int max_pages, int* dev_err, cudaStream_t stream);
+cudaError_t launch_commit(int32_t* ctx_lens, const int32_t* accepted_len, int B, int extra,
+                          cudaStream_t stream);
+
 // Sets the thread-local error message of the C ABI; returns `code`.
 int set_error(int code, const char* msg);
 

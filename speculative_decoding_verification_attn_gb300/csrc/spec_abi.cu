@@ -313,6 +313,56 @@ int spec_accept_rejection(const void* target_logits, const void* draft_logits,
     return SPEC_OK;
 }
 
+int spec_kv_append(const void* k_new, const void* v_new, int32_t src_dtype, void* k_cache,
+                   void* v_cache, void* k_scale, void* v_scale, int32_t cache_dtype,
+                   const int32_t* block_table, const int32_t* ctx_lens, int32_t batch,
+                   int32_t num_new, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                   int32_t num_pages, int32_t max_pages_per_seq, void* stream) {
+    g_err.clear();
+    if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
+    if (num_new < 1) return fail(SPEC_ERR_INVALID, "num_new must be >= 1");
+    if (num_kv_heads < 1) return fail(SPEC_ERR_INVALID, "num_kv_heads must be >= 1");
+    if (head_dim < 32 || head_dim > 256 || head_dim % 32)
+        return fail(SPEC_ERR_INVALID, "head_dim must be a multiple of 32 in [32, 256]");
+    if (page_size < 1) return fail(SPEC_ERR_INVALID, "page_size < 1");
+    if (num_pages < 1 || max_pages_per_seq < 1)
+        return fail(SPEC_ERR_INVALID, "num_pages and max_pages_per_seq must be >= 1");
+    if (src_dtype != SPEC_DTYPE_F32 && src_dtype != SPEC_DTYPE_BF16)
+        return fail(SPEC_ERR_INVALID, "src_dtype must be F32 or BF16");
+    if (cache_dtype != SPEC_DTYPE_F32 && cache_dtype != SPEC_DTYPE_BF16 &&
+        cache_dtype != SPEC_DTYPE_I8)
+        return fail(SPEC_ERR_INVALID, "cache_dtype must be F32, BF16 or I8");
+    if (batch == 0) return SPEC_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !ctx_lens)
+        return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    if (cache_dtype == SPEC_DTYPE_I8 && (!k_scale || !v_scale))
+        return fail(SPEC_ERR_INVALID, "an I8 cache needs k_scale and v_scale");
+    if ((int64_t)batch * num_new * num_kv_heads * 2 / 8 >= (1LL << 31))
+        return fail(SPEC_ERR_UNSUPPORTED, "too many rows");
+    Workspace* ws = nullptr;
+    int rc = get_workspace(0, &ws);
+    if (rc) return rc;
+    cudaError_t e = specv::launch_kv_append(
+        k_new, v_new, src_dtype, k_cache, v_cache, static_cast<uint16_t*>(k_scale),
+        static_cast<uint16_t*>(v_scale), cache_dtype, block_table, ctx_lens, batch, num_new,
+        num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
+        static_cast<int*>(ws->base), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return SPEC_OK;
+}
+
+int spec_commit(int32_t* ctx_lens, const int32_t* accepted_len, int32_t batch, int32_t extra,
+                void* stream) {
+    g_err.clear();
+    if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
+    if (batch == 0) return SPEC_OK;
+    if (!ctx_lens || !accepted_len) return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    cudaError_t e = specv::launch_commit(ctx_lens, accepted_len, batch, extra,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    return SPEC_OK;
+}
+
 int spec_device_error(int32_t* flags) {
     g_err.clear();
     if (!flags) return fail(SPEC_ERR_INVALID, "flags is NULL");

@@ -117,6 +117,26 @@ def test_rejection_rejects_bad_arguments(lib, bad, needle):
     assert needle in lib.spec_last_error().decode()
 
 
+@pytest.mark.parametrize("bad,needle", [
+    (dict(n=0), "num_new"),
+    (dict(D=48), "head_dim"),
+    (dict(src=3), "src_dtype"),
+    (dict(cdt=2), "cache_dtype"),
+    (dict(kc=0), "null"),
+    (dict(cdt=3), "I8"),
+])
+def test_kv_append_rejects_bad_arguments(lib, bad, needle):
+    a = dict(kn=16, vn=16, src=1, kc=16, vc=16, ks=None, vs=None, cdt=1, bt=16, ctx=16, B=2, n=4,
+             Hkv=2, D=128, P=16, NP=8, MP=4)
+    a.update(bad)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    rc = lib.spec_kv_append(vp(a["kn"]), vp(a["vn"]), a["src"], vp(a["kc"]), vp(a["vc"]),
+                            vp(a["ks"]), vp(a["vs"]), a["cdt"], vp(a["bt"]), vp(a["ctx"]), a["B"],
+                            a["n"], a["Hkv"], a["D"], a["P"], a["NP"], a["MP"], None)
+    assert rc == -1
+    assert needle in lib.spec_last_error().decode()
+
+
 def test_options(lib):
     assert lib.spec_set_option(0, 4) == -1
     assert lib.spec_set_option(0, 3) == 0
