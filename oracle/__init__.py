@@ -12,6 +12,8 @@ computes and which passage of the pages it follows:
   Compression".
 * ``accept_greedy`` -- first-disagreement acceptance plus bonus token (same
   blog, "Speculating to get sequence parallelism during decode").
+* ``verify_attn_tree`` / ``accept_tree`` -- the same over a tree of drafts
+  (same blog, "Advances in speculators": token trees verified in one pass).
 * ``kv_append`` / ``quantize_rows`` / ``commit`` -- the drafts' K/V rows
   written into the paged cache (INT8: CXL-SpecKV's "Algorithm 2 KV-Cache
   Compression", per (token, kv-head) row) and HeteroReason's KVMU Accept
@@ -69,6 +71,10 @@ def _load():
         lib.oracle_kv_append.restype = i32
         lib.oracle_commit.argtypes = [P, P, i32, i32]
         lib.oracle_commit.restype = i32
+        lib.oracle_verify_attn_tree.argtypes = attn_common + [P, P, P]
+        lib.oracle_verify_attn_tree.restype = i32
+        lib.oracle_accept_tree.argtypes = [P, i32, P, P, i32, i32, ctypes.c_int64, P, P, P]
+        lib.oracle_accept_tree.restype = i32
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -127,6 +133,39 @@ def attn_rows(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_ta
         raise ValueError("oracle_attn_rows failed (%d)" % rc)
     del keep
     return out, lse
+
+
+def verify_attn_tree(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_table,
+                     ctx_lens, scale, tree_mask):
+    """Attention where draft query i sees the context and the drafts set in
+    tree_mask[b, i] (uint64 [B, k]); returns (out, lse) float64."""
+    keep, args, (B, k, Hq, D) = _attn_common(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale,
+                                             v_scale, block_table, ctx_lens, scale)
+    tree_mask = np.ascontiguousarray(tree_mask, np.uint64)
+    assert tree_mask.shape == (B, k)
+    out = np.zeros((B, k, Hq, D), np.float64)
+    lse = np.zeros((B, k, Hq), np.float64)
+    rc = _load().oracle_verify_attn_tree(*args, _ptr(tree_mask), _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_verify_attn_tree failed (%d)" % rc)
+    return out, lse
+
+
+def accept_tree(logits, dtype, draft_tokens, parents):
+    """Greedy acceptance over a tree of drafts; returns (accepted_len, next_token, path [B, k])."""
+    B, k1, V = logits.shape
+    k = k1 - 1
+    draft_tokens = np.ascontiguousarray(draft_tokens, np.int32)
+    parents = np.ascontiguousarray(parents, np.int32)
+    assert draft_tokens.shape == (B, k) and parents.shape == (B, k)
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    path = np.zeros((B, k), np.int32)
+    rc = _load().oracle_accept_tree(_ptr(logits), DTYPES[dtype], _ptr(draft_tokens), _ptr(parents),
+                                    B, k, V, _ptr(acc), _ptr(nxt), _ptr(path))
+    if rc:
+        raise ValueError("oracle_accept_tree failed (%d)" % rc)
+    return acc, nxt, path
 
 
 def accept_greedy(logits, dtype, draft_tokens):
@@ -235,6 +274,7 @@ def f16_bits_to_f64(bits: int) -> float:
     return _load().oracle_f16_to_f64(int(bits))
 
 
-__all__ = ["verify_attn", "attn_rows", "accept_greedy", "accept_rejection", "quantize_rows",
+__all__ = ["verify_attn", "attn_rows", "verify_attn_tree", "accept_tree", "accept_greedy",
+           "accept_rejection", "quantize_rows",
            "kv_append", "commit", "splitmix64",
            "accept_uniform", "gumbel", "bf16_bits_to_f64", "f16_bits_to_f64", "DTYPES"]

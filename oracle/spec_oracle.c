@@ -98,6 +98,7 @@ typedef struct {
     const int32_t *block_table; const int32_t *ctx_lens;
     int B, num_draft, Hq, Hkv, D, P, num_pages, max_pages;
     double scale;
+    const uint64_t *tree_mask; /* [B, k] or NULL (causal chain) */
 } attn_args;
 
 /* Dequantised element d of cached row (sequence b, logical key j, kv-head g). */
@@ -119,24 +120,46 @@ static double cache_elem(const attn_args *a, const void *cache, const uint16_t *
  * out_row[D] receives sum_j softmax(s)_j * V_j and *lse_out the natural-log
  * log-sum-exp of s.  Returns 0, or -1 on an out-of-range page reference.
  */
+/*
+ * Keys visible to draft query i of sequence b: the whole cached context
+ * 0 .. ctx_b - 1, then draft position t (key ctx_b + t) when the query may
+ * see it -- t <= i for the causal chain, or bit t of tree_mask[b][i] for a
+ * tree of drafts (each node sees its ancestors and itself; SpecInfer-style
+ * tree verification, "Decoding Speculative Decoding from First Principles",
+ * section "Advances in speculators").
+ */
+static int64_t visible_keys(const attn_args *a, int b, int i, int64_t *keys) {
+    const int64_t ctx = a->ctx_lens[b];
+    int64_t n = 0;
+    for (int64_t j = 0; j < ctx; ++j) keys[n++] = j;
+    for (int t = 0; t < a->num_draft; ++t) {
+        const int vis = a->tree_mask ? (int)((a->tree_mask[(int64_t)b * a->num_draft + i] >> t) & 1u)
+                                     : t <= i;
+        if (vis) keys[n++] = ctx + t;
+    }
+    return n;
+}
+
 static int attn_row(const attn_args *a, int b, int i, int h, double *out_row, double *lse_out) {
     int G = a->Hq / a->Hkv;
     int g = h / G;                                  /* GQA: kv-head serving q-head h */
-    int64_t n_keys = (int64_t)a->ctx_lens[b] + i + 1; /* causal: keys 0 .. ctx_b + i */
     int bad = 0;
     const int64_t q_off = (((int64_t)b * a->num_draft + i) * a->Hq + h) * a->D;
-    double *s = (double *)malloc(sizeof(double) * (size_t)(n_keys > 0 ? n_keys : 1));
-    if (!s) return -2;
+    const int64_t cap = (int64_t)a->ctx_lens[b] + a->num_draft;
+    int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
+    if (!s || !keys) { free(s); free(keys); return -2; }
+    const int64_t n_keys = visible_keys(a, b, i, keys);
 
-    /* scores s_j = scale * <q, K_j> */
-    for (int64_t j = 0; j < n_keys; ++j) {
+    /* scores s_j = scale * <q, K_j> over the visible keys */
+    for (int64_t jj = 0; jj < n_keys; ++jj) {
         double dot = 0.0;
         for (int d = 0; d < a->D; ++d)
             dot += load_f64(a->q, a->q_dtype, q_off + d) *
-                   cache_elem(a, a->k_cache, a->k_scale, b, j, g, d, &bad);
-        s[j] = a->scale * dot;
+                   cache_elem(a, a->k_cache, a->k_scale, b, keys[jj], g, d, &bad);
+        s[jj] = a->scale * dot;
     }
-    if (bad) { free(s); return -1; }
+    if (bad) { free(s); free(keys); return -1; }
 
     /* two-pass softmax: max, then log-sum-exp */
     double m = -INFINITY;
@@ -150,9 +173,10 @@ static int attn_row(const attn_args *a, int b, int i, int h, double *out_row, do
     for (int64_t j = 0; j < n_keys; ++j) {
         double p = exp(s[j] - lse);
         for (int d = 0; d < a->D; ++d)
-            out_row[d] += p * cache_elem(a, a->v_cache, a->v_scale, b, j, g, d, &bad);
+            out_row[d] += p * cache_elem(a, a->v_cache, a->v_scale, b, keys[j], g, d, &bad);
     }
     free(s);
+    free(keys);
     *lse_out = lse;
     return bad ? -1 : 0;
 }
@@ -167,7 +191,7 @@ static int check_shape(const attn_args *a) {
 #define ATTN_ARGS_INIT                                                              \
     attn_args a = {q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,        \
                    block_table, ctx_lens, B, num_draft, Hq, Hkv, D, P, num_pages,   \
-                   max_pages, scale}
+                   max_pages, scale, NULL}
 
 /* Full attention: out [B, k, Hq, D] and lse [B, k, Hq], both float64. */
 int oracle_verify_attn(const void *q, int q_dtype, const void *k_cache, const void *v_cache,
@@ -483,5 +507,67 @@ int oracle_kv_append(const void *k_new, const void *v_new, int src_dtype, void *
 
 int oracle_commit(int32_t *ctx_lens, const int32_t *accepted_len, int B, int extra) {
     for (int b = 0; b < B; ++b) ctx_lens[b] += accepted_len[b] + extra;
+    return 0;
+}
+
+/* Tree attention: as oracle_verify_attn, query i of sequence b seeing the
+ * context and the drafts set in tree_mask[b][i] (see visible_keys). */
+int oracle_verify_attn_tree(const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                            int kv_dtype, const uint16_t *k_scale, const uint16_t *v_scale,
+                            const int32_t *block_table, const int32_t *ctx_lens, int B,
+                            int num_draft, int Hq, int Hkv, int D, int P, int num_pages,
+                            int max_pages, double scale, const uint64_t *tree_mask, double *out,
+                            double *lse) {
+    ATTN_ARGS_INIT;
+    a.tree_mask = tree_mask;
+    if (check_shape(&a) || num_draft > 64) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < num_draft; ++i)
+            for (int h = 0; h < Hq; ++h) {
+                const int64_t r = ((int64_t)b * num_draft + i) * Hq + h;
+                int rc = attn_row(&a, b, i, h, out + r * D, lse + r);
+                if (rc) return rc;
+            }
+    return 0;
+}
+
+/*
+ * 5. Greedy acceptance over a tree of drafts (SpecInfer / EAGLE-style token
+ *    trees, "Advances in speculators"): node i carries token draft[b][i]
+ *    and parent parent[b][i] in [-1, i) (-1: a child of the last committed
+ *    token).  logits row 0 is the target's prediction at the root, row i+1
+ *    its prediction after node i.  From the root, the walk keeps the child
+ *    whose token equals the target's argmax at the current node (the lowest
+ *    index if several do), and stops when none does; accepted_len is the
+ *    path length, next_token the argmax after the last kept node, path
+ *    [B, k] the kept nodes in order (-1 after the end).  A chain
+ *    (parent[i] = i - 1) is the greedy rule of section 2.
+ */
+int oracle_accept_tree(const void *logits, int dtype, const int32_t *draft, const int32_t *parent,
+                       int B, int num_draft, int64_t V, int32_t *accepted_len,
+                       int32_t *next_token, int32_t *path) {
+    if (B < 0 || num_draft < 1 || V < 1) return -1;
+    const int k = num_draft;
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < k; ++i) {
+            const int32_t p = parent[(int64_t)b * k + i];
+            if (p < -1 || p >= i) return -1;
+        }
+        int cur = -1, n = 0;
+        for (int i = 0; i < k; ++i) path[(int64_t)b * k + i] = -1;
+        for (;;) {
+            const int32_t a = row_argmax(logits, dtype, ((int64_t)b * (k + 1) + cur + 1) * V, V);
+            int next = -1;
+            for (int c = 0; c < k && next < 0; ++c)
+                if (parent[(int64_t)b * k + c] == cur && draft[(int64_t)b * k + c] == a) next = c;
+            if (next < 0) {
+                accepted_len[b] = n;
+                next_token[b] = a;
+                break;
+            }
+            path[(int64_t)b * k + n++] = next;
+            cur = next;
+        }
+    }
     return 0;
 }

@@ -329,3 +329,54 @@ def make_rejection_inputs(batch: int, num_draft: int, vocab: int, dtype: str = "
     return RejectionInputs(dtype=dtype, target_logits=tl_s, draft_logits=dl_s,
                            draft_tokens=np.ascontiguousarray(drafts), temperature=temperature,
                            seed=int(rng.integers(0, 2**63)))
+
+
+# ---------------------------------------------------------------- draft trees
+
+def tree_masks(parents: np.ndarray) -> np.ndarray:
+    """Ancestor masks of draft trees: bit t of mask[b, i] is set when node t is
+    node i or one of its ancestors.  parents [B, k] int32, parent < index,
+    -1 for children of the last committed token."""
+    B, k = parents.shape
+    masks = np.zeros((B, k), np.uint64)
+    for b in range(B):
+        for i in range(k):
+            p = int(parents[b, i])
+            assert -1 <= p < i
+            masks[b, i] = (masks[b, p] if p >= 0 else np.uint64(0)) | np.uint64(1 << i)
+    return masks
+
+
+def random_trees(batch: int, num_draft: int, seed: int = 0, width: float = 0.5) -> np.ndarray:
+    """Seeded draft trees: node i's parent is -1 or an earlier node, nearer
+    nodes likelier (width 0: a chain, larger: bushier)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x7EE]))
+    parents = np.zeros((batch, num_draft), np.int32)
+    for b in range(batch):
+        for i in range(num_draft):
+            if i == 0 or rng.random() >= width:
+                parents[b, i] = i - 1
+            else:
+                parents[b, i] = int(rng.integers(-1, i))
+    return parents
+
+
+def plant_tree_tokens(logits_f32: np.ndarray, parents: np.ndarray, match: float,
+                      seed: int = 0) -> np.ndarray:
+    """Draft tokens of a tree: node i copies the target's argmax at its parent
+    with probability `match`, else a different random token (input
+    construction; numpy.argmax on the stored logits)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x70C]))
+    B, k = parents.shape
+    V = logits_f32.shape[-1]
+    am = np.argmax(logits_f32, axis=-1)  # [B, k+1]
+    tokens = np.zeros((B, k), np.int32)
+    for b in range(B):
+        for i in range(k):
+            target = am[b, parents[b, i] + 1]
+            if rng.random() < match:
+                tokens[b, i] = target
+            else:
+                o = int(rng.integers(0, V - 1))
+                tokens[b, i] = o + (o >= target)
+    return tokens
