@@ -161,6 +161,46 @@ SPEC_API int spec_accept_greedy(const void *logits, int32_t logits_dtype, const 
                        int32_t *accepted_len, int32_t *next_token, void *stream);
 
 /*
+ * Verification attention over a tree of drafts (token trees verified in one
+ * pass: "Decoding Speculative Decoding from First Principles", section
+ * "Advances in speculators").  Same arguments and results as
+ * spec_verify_attn, except that draft query i of sequence b sees the whole
+ * cached context and the draft keys t (position ctx_b + t) whose bit t is
+ * set in tree_mask[b, i] (uint64 [batch, num_draft], device memory) -- for a
+ * tree, node i's ancestors and itself.  The causal chain is the mask with
+ * bits 0..i.  Runs on the same kernels as spec_verify_attn.
+ */
+SPEC_API int spec_verify_attn_tree(const void *q, const void *k_cache, const void *v_cache,
+                                   const void *k_scale, const void *v_scale,
+                                   const int32_t *block_table, const int32_t *ctx_lens,
+                                   const uint64_t *tree_mask, int32_t batch, int32_t num_draft,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t page_size, int32_t num_pages,
+                                   int32_t max_pages_per_seq, int32_t q_dtype, int32_t kv_dtype,
+                                   float scale, void *out, float *lse, void *stream);
+
+/*
+ * Greedy acceptance over a tree of drafts.  Node i of sequence b carries
+ * draft_tokens[b, i] and parents[b, i] in [-1, i) (-1: a child of the last
+ * committed token); logits row 0 is the target's prediction at the root and
+ * row i + 1 its prediction after node i ([batch, num_draft + 1, vocab]).
+ * From the root, the walk keeps the lowest-index child whose token equals
+ * the target's argmax at the current node (lowest vocabulary index on
+ * ties), and stops when no child does:
+ *   accepted_len[b] = number of kept nodes,
+ *   next_token[b]   = the target's argmax after the last kept node,
+ *   path[b, :]      = the kept nodes in order, -1 after them (path may be
+ *                     NULL).
+ * A chain (parents[b, i] = i - 1) gives spec_accept_greedy's results.  A
+ * parent outside [-1, i) makes its node unreachable and sets
+ * SPEC_DEVERR_TREE.  Limits as spec_accept_greedy.
+ */
+SPEC_API int spec_accept_tree(const void *logits, int32_t logits_dtype,
+                              const int32_t *draft_tokens, const int32_t *parents, int32_t batch,
+                              int32_t num_draft, int64_t vocab, int32_t *accepted_len,
+                              int32_t *next_token, int32_t *path, void *stream);
+
+/*
  * Greedy acceptance that allocates nothing.  (The pages have no counterpart:
  * this is an interface convenience of this library.)
  *
@@ -273,7 +313,8 @@ enum {
     SPEC_DEVERR_PAGE = 1,    /* block_table entry outside [0, num_pages) (clamped) */
     SPEC_DEVERR_CTX = 2,     /* ctx_b + k beyond the block table (clamped) */
     SPEC_DEVERR_TIMEOUT = 4, /* a bounded on-chip wait gave up; results invalid */
-    SPEC_DEVERR_TOKEN = 8    /* a draft token outside [0, vocab) (treated as rejected) */
+    SPEC_DEVERR_TOKEN = 8,   /* a draft token outside [0, vocab) (treated as rejected) */
+    SPEC_DEVERR_TREE = 16    /* a tree parent outside [-1, i) (the node is never taken) */
 };
 
 /* Free the current device's workspace (synchronises the device). */

@@ -21,11 +21,13 @@ SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_F16, SPEC_DTYPE_I8 = 0, 1, 2, 3
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_OPT_ATTN_PATH, SPEC_OPT_NUM_CTAS, SPEC_OPT_VALIDATE, SPEC_OPT_SIMT_CHUNK = 0, 1, 2, 3
 SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT, SPEC_DEVERR_TOKEN = 1, 2, 4, 8
+SPEC_DEVERR_TREE = 16
 
 # every symbol the public header declares
 EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
             "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_accept_rejection",
-            "spec_kv_append", "spec_commit", "spec_device_error", "spec_release"]
+            "spec_kv_append", "spec_commit", "spec_verify_attn_tree", "spec_accept_tree",
+            "spec_device_error", "spec_release"]
 SPEC_NOALLOC_MAX_PARTIALS, SPEC_NOALLOC_MAX_BATCH = 65536, 4096
 
 _TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
@@ -72,6 +74,11 @@ def _open(path: str):
     lib.spec_kv_append.restype = ctypes.c_int
     lib.spec_commit.argtypes = [P, P, i32, i32, P]
     lib.spec_commit.restype = ctypes.c_int
+    lib.spec_verify_attn_tree.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                          i32, i32, i32, ctypes.c_float, P, P, P]
+    lib.spec_verify_attn_tree.restype = ctypes.c_int
+    lib.spec_accept_tree.argtypes = [P, i32, P, P, i32, i32, i64, P, P, P, P]
+    lib.spec_accept_tree.restype = ctypes.c_int
     lib.spec_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.spec_device_error.restype = ctypes.c_int
     lib.spec_release.restype = ctypes.c_int
@@ -127,6 +134,36 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, ctx_lens, num_draft: int,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
         _ptr(ctx_lens), B, k, Hq, Hkv, D, P, NP, block_table.shape[1], _TORCH_DT[q.dtype],
         _TORCH_DT[k_cache.dtype], float(scale), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def spec_verify_attn_tree(q, k_cache, v_cache, block_table, ctx_lens, tree_mask, num_draft: int,
+                          scale: float, out, lse=None, k_scale=None, v_scale=None,
+                          stream=None) -> None:
+    """spec_verify_attn with draft visibility from ``tree_mask`` (64-bit [B, k],
+    bit t of row i: query i sees draft t; int64 or uint64 tensor)."""
+    B, k, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    if k != num_draft or D2 != D or tuple(tree_mask.shape) != (B, k):
+        raise ValueError("q must be [B, num_draft, Hq, D], tree_mask [B, num_draft]")
+    if tree_mask.element_size() != 8:
+        raise ValueError("tree_mask must hold 64-bit words")
+    _check(load().spec_verify_attn_tree(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        _ptr(ctx_lens), _ptr(tree_mask), B, k, Hq, Hkv, D, P, NP, block_table.shape[1],
+        _TORCH_DT[q.dtype], _TORCH_DT[k_cache.dtype], float(scale), _ptr(out), _ptr(lse),
+        _stream(stream)))
+
+
+def spec_accept_tree(logits, draft_tokens, parents, num_draft: int, accepted_len, next_token,
+                     path=None, stream=None) -> None:
+    """Greedy acceptance over a tree of drafts (parents int32 [B, k] in [-1, i))."""
+    B, k1, V = logits.shape
+    if (k1 != num_draft + 1 or tuple(draft_tokens.shape) != (B, num_draft)
+            or tuple(parents.shape) != (B, num_draft)):
+        raise ValueError("logits [B, k+1, V], drafts and parents [B, k]")
+    _check(load().spec_accept_tree(_ptr(logits), _TORCH_DT[logits.dtype], _ptr(draft_tokens),
+                                   _ptr(parents), B, num_draft, V, _ptr(accepted_len),
+                                   _ptr(next_token), _ptr(path), _stream(stream)))
 
 
 def spec_accept_greedy(logits, draft_tokens, num_draft: int, accepted_len, next_token,

@@ -112,6 +112,45 @@ __device__ __forceinline__ void prefix_match(const AcceptArgs& a, int b, int my_
     }
 }
 
+// Greedy acceptance over a tree of drafts (SpecInfer / EAGLE-style token
+// trees, "Decoding Speculative Decoding from First Principles", "Advances in
+// speculators"): node i carries draft_tokens[b, i] and parent[b, i] in
+// [-1, i); s_am[0] is the target's argmax at the root, s_am[i+1] after node
+// i.  From the root, keep the lowest-index child whose token is the argmax
+// at the current node; stop when none is.  Warp 0 only: each lane holds
+// nodes lane and lane + 32, a step is one ballot.  Only children with a
+// higher index than the current node are taken, so the walk ends within k
+// steps even with corrupt parents (which are also flagged).
+__device__ __forceinline__ void tree_walk(const AcceptArgs& a, int b, const int* s_am) {
+    const int lane = threadIdx.x & 31;
+    int par[2], tok[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        par[h] = c < a.k ? __ldg(a.parent + (int64_t)b * a.k + c) : -2;
+        tok[h] = c < a.k ? __ldg(a.draft + (int64_t)b * a.k + c) : -1;
+        if (c < a.k && (par[h] < -1 || par[h] >= c)) raise_device_error(a.dev_err, SPEC_DEVERR_TREE);
+    }
+    int cur = -1, n = 0;
+    for (int step = 0; step < a.k; ++step) {
+        const int am = s_am[cur + 1];
+        const unsigned b0 = __ballot_sync(0xffffffffu, par[0] == cur && lane > cur && tok[0] == am);
+        const unsigned b1 =
+            __ballot_sync(0xffffffffu, par[1] == cur && lane + 32 > cur && tok[1] == am);
+        const int next = b0 ? __ffs(b0) - 1 : b1 ? 32 + __ffs(b1) - 1 : -1;
+        if (next < 0) break;
+        if (a.path && lane == 0) a.path[(int64_t)b * a.k + n] = next;
+        ++n;
+        cur = next;
+    }
+    if (a.path)
+        for (int i = n + lane; i < a.k; i += 32) a.path[(int64_t)b * a.k + i] = -1;
+    if (lane == 0) {
+        a.accepted_len[b] = n;
+        a.next_token[b] = s_am[cur + 1];
+    }
+}
+
 // ---------------------------------------------------------------- cluster form
 
 template <typename T>
@@ -175,7 +214,11 @@ accept_cluster_kernel(AcceptArgs a, int parts, int64_t part_len) {
         s_am[tid] = idx;
     }
     __syncthreads();
-    prefix_match(a, b, my_draft, s_am, &s_first_miss);
+    if (a.parent) {
+        if (tid < 32) tree_walk(a, b, s_am);
+    } else {
+        prefix_match(a, b, my_draft, s_am, &s_first_miss);
+    }
 }
 
 // ---------------------------------------------------------------- ticket form
@@ -272,7 +315,11 @@ accept_greedy_kernel(AcceptArgs a, int n_slices, float* __restrict__ part_v,
     }
     if (tid == 0) s_first_miss = a.k;
     __syncthreads();
-    prefix_match(a, b, my_draft, s_am, &s_first_miss);
+    if (a.parent) {
+        if (tid < 32) tree_walk(a, b, s_am);
+    } else {
+        prefix_match(a, b, my_draft, s_am, &s_first_miss);
+    }
     if (tid == 0) tickets[b] = 0;  // ready for the next call
 }
 

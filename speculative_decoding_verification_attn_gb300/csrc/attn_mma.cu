@@ -192,6 +192,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         int irow[2];
         irow[0] = g < R ? g / G : k - 1;
         irow[1] = g + 8 < R ? (g + 8) / G : k - 1;
+        uint64_t mrow[2] = {0, 0};  // draft bits of the two rows, per piece
         const int kv0 = warp * BOX_ROWS;  // this warp's first key in every tile
         uint8_t* ring = sm + Smem::RING + warp * WSTAGE_BYTES;  // stage s at + s * NW * WSTAGE_BYTES
         uint64_t* full = &bars[Smem::B_KVFULL + warp];           // stage s at full[s * NW]
@@ -305,6 +306,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int s = it % NS;
             const int ctx = s_ctx[cur.b], L = ctx + k, key0 = cur.lt * TN;
             const int nvalid = min(TN, L - key0);
+            if (first) {
+                mrow[0] = draft_bits(a, cur.b, irow[0]);
+                mrow[1] = draft_bits(a, cur.b, irow[1]);
+            }
             // block-table entry of the box NS tiles ahead: read now, used after this tile
             const bool refill = it + NS < n_tiles && box_valid(ahead);
             int pg_next = -1;
@@ -398,16 +403,32 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 // masked scores (log2 units); -inf where the key is invisible
                 float v[2][4];
                 float mt[2] = {-INFINITY, -INFINITY};
+                if (key0 + kv0 + BOX_ROWS <= ctx) {
+                    // every key of this warp's slice is context: all visible
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int hr = e >> 1;  // 0: row g, 1: row g + 8
-                        const int kr = kv0 + nt * 8 + t4 * 2 + (e & 1);
-                        const bool vis = kr < nvalid && key0 + kr <= ctx + irow[hr];
-                        v[nt][e] = vis ? sc[nt][e] * sl2 : -INFINITY;
-                        mt[hr] = fmaxf(mt[hr], v[nt][e]);
-                    }
+                        for (int e = 0; e < 4; ++e) {
+                            v[nt][e] = sc[nt][e] * sl2;
+                            mt[e >> 1] = fmaxf(mt[e >> 1], v[nt][e]);
+                        }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int hr = e >> 1;  // 0: row g, 1: row g + 8
+                            const int kr = kv0 + nt * 8 + t4 * 2 + (e & 1);
+                            // the context, then the drafts of the row's bits
+                            // (causal chain: keys <= ctx + i)
+                            const int key = key0 + kr;
+                            const bool vis =
+                                kr < nvalid &&
+                                (key < ctx || ((mrow[hr] >> (key < ctx ? 0 : key - ctx)) & 1ull));
+                            v[nt][e] = vis ? sc[nt][e] * sl2 : -INFINITY;
+                            mt[hr] = fmaxf(mt[hr], v[nt][e]);
+                        }
+                }
                 float alpha[2];
                 bool moved = false;
 #pragma unroll

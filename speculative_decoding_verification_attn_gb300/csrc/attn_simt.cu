@@ -110,7 +110,9 @@ attn_simt_kernel(AttnArgs a, SimtPlan p, float* __restrict__ part_o, float* __re
             const int r = e / kKeyTile, jj = e % kKeyTile, j = jt + jj;
             const int i = (r0 + r) / G;
             float s = -INFINITY;
-            if (j < j1 && j <= sg.ctx + i) {  // causal: query i sees keys <= ctx + i
+            // query i sees the context and the drafts of its row's bits
+            // (causal chain: keys <= ctx + i)
+            if (j < j1 && (j < sg.ctx || ((draft_bits(a, b, i) >> (j - sg.ctx)) & 1ull))) {
                 float dot = 0.f;
                 for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[jj * (D + 1) + d], dot);
                 s = dot * a.scale;

@@ -233,6 +233,7 @@ __device__ void softmax_role(const Cta& x) {
     }
     float m_ref = -INFINITY, l = 0.f;
     bool has = false;  // this set has taken a tile of the current piece
+    uint64_t mrow = 0;  // draft bits of this thread's query row, per piece
     Cursor cur;
     if (x.n_tiles > 0) cur.init(x.t_begin, x.s_pre, x.s_ctx, a.B, a.Hkv, k);
     bool ok = true;
@@ -247,6 +248,7 @@ __device__ void softmax_role(const Cta& x) {
             m_ref = -INFINITY;
             l = 0.f;
             has = false;
+            mrow = draft_bits(a, cur.b, i_row);
         }
         if (mine) {
             if (ok)
@@ -262,8 +264,23 @@ __device__ void softmax_role(const Cta& x) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[Smem::B_SFREE + sq]);
             if (ok && warp_active) {
-                // keys of this row visible in this copy's slice: cc < cmax
-                const int cmax = max(0, min(min(nvalid, ctx + i_row - key0 + 1) - cbase, CW));
+                // visible columns of this slice as one bit word: the context
+                // keys at its front, then the drafts of the row's bits (causal
+                // chain: keys <= ctx + i), limited to the keys the tile holds
+                uint32_t vlo, vhi;
+                {
+                    const int kc0 = key0 + cbase, nv = nvalid - cbase, nctx = ctx - kc0;
+                    const uint64_t valid = nv >= 64 ? ~0ull : nv <= 0 ? 0ull : (1ull << nv) - 1;
+                    const uint64_t cbits =
+                        nctx >= 64 ? ~0ull : nctx <= 0 ? 0ull : (1ull << nctx) - 1;
+                    const uint64_t dbits = nctx >= 64   ? 0ull
+                                           : nctx >= 0  ? mrow << nctx
+                                           : nctx > -64 ? mrow >> -nctx
+                                                        : 0ull;
+                    const uint64_t vis = (cbits | dbits) & valid;
+                    vlo = (uint32_t)vis;
+                    vhi = (uint32_t)(vis >> 32);
+                }
                 // INT8: per-key fp32 scales of this operand stage (k row, then v row)
                 const float* sc_k = reinterpret_cast<const float*>(
                     x.sm + Smem::SCALES + (it % Smem::NM) * 2 * TN * 4) + cbase;
@@ -280,7 +297,8 @@ __device__ void softmax_role(const Cta& x) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int cc = 4 * c4 + e;
-                        v[cc] = cc < cmax ? __uint_as_float(sr[cc]) * f[e] : -INFINITY;
+                        const bool vis = ((cc < 32 ? vlo >> cc : vhi >> (cc - 32)) & 1u) != 0;
+                        v[cc] = vis ? __uint_as_float(sr[cc]) * f[e] : -INFINITY;
                         mx[e] = fmaxf(mx[e], v[cc]);
                     }
                 }

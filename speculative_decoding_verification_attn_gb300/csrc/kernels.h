@@ -25,7 +25,20 @@ struct AttnArgs {
     float* lse;
     int* dev_err;       // device error word
     int* seg_counters;  // [B*Hkv] zeroed arrival counters (fused split-KV merge)
+    // [B, k] draft-visibility bits (bit t of row i: query i sees draft t), or
+    // null for the causal chain (bits 0..i)
+    const uint64_t* tree_mask;
 };
+
+// Draft bits visible to query i of sequence b: the tree row, or the causal chain.
+__host__ __device__ inline uint64_t draft_bits(const AttnArgs& a, int b, int i) {
+#ifdef __CUDA_ARCH__
+    if (a.tree_mask) return __ldg(a.tree_mask + (int64_t)b * a.k + i);
+#else
+    if (a.tree_mask) return a.tree_mask[(int64_t)b * a.k + i];
+#endif
+    return i >= 63 ? ~0ull : ((1ull << (i + 1)) - 1);
+}
 
 // ---- SIMT kernel (CUDA cores; any supported dtype / shape) ----
 struct SimtPlan {
@@ -62,6 +75,11 @@ struct AcceptArgs {
     int64_t V;
     int32_t* accepted_len;
     int32_t* next_token;
+    // tree acceptance (null for the chain rule): parent [B, k] in [-1, i),
+    // accepted node path [B, k] (-1 padded; may be null), device error word
+    const int32_t* parent = nullptr;
+    int32_t* path = nullptr;
+    int* dev_err = nullptr;
 };
 size_t accept_workspace_bytes(const AcceptArgs& a);
 // `tickets` must hold B zeroed int32 (self-resetting across calls).

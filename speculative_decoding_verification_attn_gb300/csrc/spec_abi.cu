@@ -158,12 +158,17 @@ int spec_set_option(int32_t option, int64_t value) {
     }
 }
 
-int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, const void* k_scale,
+}  // extern "C"
+
+namespace {
+
+int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, const void* k_scale,
                      const void* v_scale, const int32_t* block_table, const int32_t* ctx_lens,
-                     int32_t batch, int32_t num_draft, int32_t num_q_heads, int32_t num_kv_heads,
-                     int32_t head_dim, int32_t page_size, int32_t num_pages,
-                     int32_t max_pages_per_seq, int32_t q_dtype, int32_t kv_dtype, float scale,
-                     void* out, float* lse, void* stream) {
+                     const uint64_t* tree_mask, int32_t batch, int32_t num_draft,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t page_size, int32_t num_pages, int32_t max_pages_per_seq,
+                     int32_t q_dtype, int32_t kv_dtype, float scale, void* out, float* lse,
+                     void* stream) {
     g_err.clear();
     if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
     if (num_draft < 1 || num_draft > 64) return fail(SPEC_ERR_INVALID, "num_draft must be in [1, 64]");
@@ -201,6 +206,7 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
     a.q_dtype = q_dtype; a.kv_dtype = kv_dtype; a.scale = scale;
     a.out = out; a.lse = lse;
     a.dev_err = nullptr; a.seg_counters = nullptr;
+    a.tree_mask = tree_mask;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // kernels: 1 SIMT, 2 tcgen05, 3 warp MMA; automatic = warp MMA for <= 16
@@ -252,9 +258,43 @@ int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, co
     return SPEC_OK;
 }
 
-int spec_accept_greedy(const void* logits, int32_t logits_dtype, const int32_t* draft_tokens,
-                       int32_t batch, int32_t num_draft, int64_t vocab, int32_t* accepted_len,
-                       int32_t* next_token, void* stream) {
+}  // namespace
+
+extern "C" {
+
+int spec_verify_attn(const void* q, const void* k_cache, const void* v_cache, const void* k_scale,
+                     const void* v_scale, const int32_t* block_table, const int32_t* ctx_lens,
+                     int32_t batch, int32_t num_draft, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t page_size, int32_t num_pages,
+                     int32_t max_pages_per_seq, int32_t q_dtype, int32_t kv_dtype, float scale,
+                     void* out, float* lse, void* stream) {
+    return verify_attn_impl(q, k_cache, v_cache, k_scale, v_scale, block_table, ctx_lens, nullptr,
+                            batch, num_draft, num_q_heads, num_kv_heads, head_dim, page_size,
+                            num_pages, max_pages_per_seq, q_dtype, kv_dtype, scale, out, lse,
+                            stream);
+}
+
+int spec_verify_attn_tree(const void* q, const void* k_cache, const void* v_cache,
+                          const void* k_scale, const void* v_scale, const int32_t* block_table,
+                          const int32_t* ctx_lens, const uint64_t* tree_mask, int32_t batch,
+                          int32_t num_draft, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t page_size, int32_t num_pages,
+                          int32_t max_pages_per_seq, int32_t q_dtype, int32_t kv_dtype,
+                          float scale, void* out, float* lse, void* stream) {
+    if (batch > 0 && !tree_mask) return fail(SPEC_ERR_INVALID, "tree_mask is NULL");
+    return verify_attn_impl(q, k_cache, v_cache, k_scale, v_scale, block_table, ctx_lens,
+                            tree_mask, batch, num_draft, num_q_heads, num_kv_heads, head_dim,
+                            page_size, num_pages, max_pages_per_seq, q_dtype, kv_dtype, scale,
+                            out, lse, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int accept_greedy_impl(const void* logits, int32_t logits_dtype, const int32_t* draft_tokens,
+                       const int32_t* parents, int32_t batch, int32_t num_draft, int64_t vocab,
+                       int32_t* accepted_len, int32_t* next_token, int32_t* path, void* stream) {
     g_err.clear();
     if (batch < 0) return fail(SPEC_ERR_INVALID, "batch < 0");
     if (num_draft < 1 || num_draft > 64) return fail(SPEC_ERR_INVALID, "num_draft must be in [1, 64]");
@@ -269,16 +309,37 @@ int spec_accept_greedy(const void* logits, int32_t logits_dtype, const int32_t* 
     specv::AcceptArgs a;
     a.logits = logits; a.dtype = logits_dtype; a.draft = draft_tokens; a.B = batch;
     a.k = num_draft; a.V = vocab; a.accepted_len = accepted_len; a.next_token = next_token;
+    a.parent = parents; a.path = path;
     const int64_t blocks = (int64_t)batch * (num_draft + 1) * ((vocab + 8191) / 8192);
     if (blocks >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "logits too large");
     Workspace* ws = nullptr;
     int rc = get_workspace(specv::accept_workspace_bytes(a), &ws);
     if (rc) return rc;
+    a.dev_err = static_cast<int*>(ws->base);
     int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws->base) + kTicketsOff);
     cudaError_t e = specv::launch_accept(a, static_cast<char*>(ws->base) + kHeader, tickets,
                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "accept_greedy launch");
     return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_accept_greedy(const void* logits, int32_t logits_dtype, const int32_t* draft_tokens,
+                       int32_t batch, int32_t num_draft, int64_t vocab, int32_t* accepted_len,
+                       int32_t* next_token, void* stream) {
+    return accept_greedy_impl(logits, logits_dtype, draft_tokens, nullptr, batch, num_draft, vocab,
+                              accepted_len, next_token, nullptr, stream);
+}
+
+int spec_accept_tree(const void* logits, int32_t logits_dtype, const int32_t* draft_tokens,
+                     const int32_t* parents, int32_t batch, int32_t num_draft, int64_t vocab,
+                     int32_t* accepted_len, int32_t* next_token, int32_t* path, void* stream) {
+    if (batch > 0 && !parents) return fail(SPEC_ERR_INVALID, "parents is NULL");
+    return accept_greedy_impl(logits, logits_dtype, draft_tokens, parents, batch, num_draft,
+                              vocab, accepted_len, next_token, path, stream);
 }
 
 int spec_accept_rejection(const void* target_logits, const void* draft_logits,
