@@ -46,7 +46,8 @@ namespace {
 
 constexpr int D = 128;
 constexpr int TN = 64;           // keys per tile
-constexpr int NS = 5;            // K/V pipeline stages
+constexpr int NK = 3;            // bf16 cache: K slots (freed when Q K^T has read them)
+constexpr int NV = 7;            // bf16 cache: V slots (freed when P V has read them)
 constexpr int ROWS = 128;        // MMA M: query rows (padded / replicated)
 constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
@@ -87,33 +88,45 @@ __host__ __device__ constexpr uint32_t idesc_pv() {  // B (V) MN-major
 }
 using Cursor = CursorT<TN>;
 
-// Shared-memory plan (offsets from the 1024-aligned base).  bf16 cache: TMA
-// boxes land directly in NS operand stages [K 16 KB | V 16 KB].  INT8 cache:
+// Shared-memory plan (offsets from the 1024-aligned base).  INT8 cache:
 // boxes land in NSR raw stages, converted tiles go to NCV operand stages,
 // with one fp32 row of per-key k / v scales per operand stage.
+//
+// bf16 cache: TMA boxes land where the MMAs read them, and K and V have rings
+// of their own -- a K slot is held only from
+// its load until Q K^T has read it, a V slot until P V has -- so that the
+// bytes in flight are not tied up behind the softmax.  K slot s at
+// STAGES + s*16 KB, V slot s at VRING + s*16 KB (TMA lands there, the MMAs
+// read it).
+// INT8 cache: raw stages [K | V | scales] and operand stages [K | V].
 template <bool KV8>
 struct SmemT {
-    static constexpr int NL = KV8 ? NSR : NS;  // stages TMA lands in
-    static constexpr int NM = KV8 ? NCV : NS;  // stages the MMAs read
+    static constexpr int NL = KV8 ? NSR : NK;  // stages the (K) producer fills
+    static constexpr int NM = KV8 ? NCV : NK;  // stages Q K^T reads
     static constexpr int Q = 0;                // one Q staging buffer
     static constexpr int STAGES = Q + Q_BYTES;
+    static constexpr int VRING = STAGES + (KV8 ? 0 : NK * KV_BYTES);  // bf16: V slots
     static constexpr int RAW = KV8 ? STAGES + NM * STAGE_BYTES : STAGES;
-    static constexpr int RAW_STAGE = KV8 ? RAW8_STAGE : STAGE_BYTES;
-    static constexpr int SCRATCH = RAW + NL * RAW_STAGE;
+    static constexpr int RAW_STAGE = KV8 ? RAW8_STAGE : KV_BYTES;
+    static constexpr int SCRATCH = KV8 ? RAW + NL * RAW_STAGE : VRING + NV * KV_BYTES;
     static constexpr int SCALES = SCRATCH + SCRATCH_BYTES;  // [NM][k, v][TN] float
     static constexpr int BARS = SCALES + (KV8 ? NM * 2 * TN * 4 : 0);
     // barriers (uint64 each): landed (TMA), operands ready (INT8 widening),
-    // operand stage free (P V done), raw stage free (INT8)
+    // operand stage free (INT8: P V done; bf16: Q K^T done), raw stage free
+    // (INT8), V landed / V slot free (bf16)
     static constexpr int B_KVFULL = 0, B_KREADY = NL, B_KVEMPTY = NL + NM,
                          B_RAWFREE = KV8 ? NL + 2 * NM : B_KVEMPTY,
-                         B_QFULL = (KV8 ? 2 * NL : NL) + 2 * NM, B_QFREE = B_QFULL + 1,
+                         B_VFULL = KV8 ? 0 : NL + 2 * NM, B_VEMPTY = B_VFULL + (KV8 ? 0 : NV),
+                         B_QFULL = KV8 ? 2 * NL + 2 * NM : NL + 2 * NM + 2 * NV,
+                         B_QFREE = B_QFULL + 1,
                          B_SFULL = B_QFULL + 2, B_SFREE = B_SFULL + NSB, B_ODONE = B_SFREE + NSB,
                          B_DRAIN = B_ODONE + 2, B_QCP = B_DRAIN + 3,
                          NUM_BARS = B_QCP + 1;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
     static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
     static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
-    static constexpr int CTX = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;  // [MAX_BATCH] int
+    static constexpr int PIDS_V = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;  // the V producer's
+    static constexpr int CTX = PIDS_V + (LOOKAHEAD + 1) * MAX_BOX * 4;  // [MAX_BATCH] int
     static constexpr int PRE = CTX + MAX_BATCH * 4;           // [MAX_BATCH+1] int
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
 };
@@ -122,9 +135,9 @@ constexpr size_t smem_bytes() { return SmemT<KV8>::END + 1024; }  // + alignment
 static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory budget (bf16)");
 static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory budget (INT8)");
 static_assert(SmemT<true>::RAW % 128 == 0 && RAW8_STAGE % 128 == 0, "TMA destination alignment");
-// warps: softmax and P V issue 0-3, Q K^T 4, TMA producer 6 (5 and 7 idle),
-// then a second set of softmax warps 8-11 (bf16) or the INT8 widening warps
-// 8-11
+// warps: softmax and P V issue 0-3, Q K^T 4, TMA producer 6 (bf16: K), V
+// producer 7 (bf16; idle with INT8), 5 idle, then a second set of softmax
+// warps 8-11 (bf16) or the INT8 widening warps 8-11
 template <bool KV8>
 __host__ __device__ constexpr int threads() { return 12 * 32; }
 
@@ -221,8 +234,8 @@ __device__ void softmax_role(const Cta& x) {
     float* s_stat_m = reinterpret_cast<float*>(x.sm + Smem::STAT);
     float* s_stat_l = s_stat_m + 4 * ROWS;
     uint64_t* bars = x.bars;
-    const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(x.sm + Smem::STAGES + KV_BYTES),
-                                             BOX_ROWS * 128, 1024);
+    const uint64_t vdesc0 = umma_sdesc_sw128(
+        smem_u32(x.sm + (KV8 ? Smem::STAGES + KV_BYTES : Smem::VRING)), BOX_ROWS * 128, 1024);
 
     if (REP > 1) {
         // both P buffers start at zero: a lane only ever rewrites its copy's slice
@@ -285,23 +298,38 @@ __device__ void softmax_role(const Cta& x) {
                 const float* sc_k = reinterpret_cast<const float*>(
                     x.sm + Smem::SCALES + (it % Smem::NM) * 2 * TN * 4) + cbase;
                 const float* sc_v = sc_k + TN;
-                // branch-free masking (masked scores become -inf, exp2 -> 0);
-                // four running maxima for ILP
+                // scores in log2 units, two columns per packed multiply
+                // (bf16: scale*log2(e); INT8: the key's folded scale)
                 float v[CW];
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c4 = 0; c4 < CW / 4; ++c4) {
                     float4 f4 = make_float4(sl2, sl2, sl2, sl2);
                     if constexpr (KV8) f4 = reinterpret_cast<const float4*>(sc_k)[c4];
-                    const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+                    const int c = 4 * c4;
+                    f2_split(f2_mul(f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                    f2(f4.x, f4.y)),
+                             v[c], v[c + 1]);
+                    f2_split(f2_mul(f2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
+                                    f2(f4.z, f4.w)),
+                             v[c + 2], v[c + 3]);
+                }
+                // masked scores become -inf (exp2 -> 0); a slice inside the
+                // context -- nearly every tile -- skips the pass
+                const bool full = CW == 64   ? (vlo & vhi) == ~0u
+                                  : CW == 32 ? vlo == ~0u
+                                             : (vlo | ~((1u << (CW & 31)) - 1u)) == ~0u;
+                if (!full) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int cc = 4 * c4 + e;
+                    for (int cc = 0; cc < CW; ++cc) {
                         const bool vis = ((cc < 32 ? vlo >> cc : vhi >> (cc - 32)) & 1u) != 0;
-                        v[cc] = vis ? __uint_as_float(sr[cc]) * f[e] : -INFINITY;
-                        mx[e] = fmaxf(mx[e], v[cc]);
+                        v[cc] = vis ? v[cc] : -INFINITY;
                     }
                 }
+                // four running maxima of three-input max for ILP
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c2 = 0; c2 < CW / 2; ++c2)
+                    mx[c2 & 3] = fmax3(mx[c2 & 3], v[2 * c2], v[2 * c2 + 1]);
                 const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 const float m_new = fmaxf(m_ref, mt);
                 float alpha = 1.f;
@@ -312,28 +340,37 @@ __device__ void softmax_role(const Cta& x) {
                     l *= alpha;
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // keeps -inf - m finite
+                const uint64_t neg_m = f2(-m_use, -m_use);
                 uint32_t pk[CW / 2];
-                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                uint64_t ps[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                 for (int c4 = 0; c4 < CW / 4; ++c4) {
                     float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
                     if constexpr (KV8) g4 = reinterpret_cast<const float4*>(sc_v)[c4];
-                    const float g[4] = {g4.x, g4.y, g4.z, g4.w};
-                    float pe[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        pe[e] = fast_exp2(v[4 * c4 + e] - m_use);
-                        ps[e] += pe[e];
-                    }
-                    if constexpr (KV8) {
-                        pk[2 * c4] = pack_f16x2(pe[0] * g[0], pe[1] * g[1]);
-                        pk[2 * c4 + 1] = pack_f16x2(pe[2] * g[2], pe[3] * g[3]);
-                    } else {
-                        pk[2 * c4] = pack_bf16x2(pe[0], pe[1]);
-                        pk[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 4 * c4 + 2 * h;
+                        float e0, e1;
+                        f2_split(f2_add(f2(v[c], v[c + 1]), neg_m), e0, e1);
+                        e0 = fast_exp2(e0);
+                        e1 = fast_exp2(e1);
+                        const uint64_t pe = f2(e0, e1);
+                        ps[h] = f2_add(ps[h], pe);
+                        if constexpr (KV8) {
+                            // P V takes p_j * s_v,j
+                            f2_split(f2_mul(pe, h ? f2(g4.z, g4.w) : f2(g4.x, g4.y)), e0, e1);
+                            pk[2 * c4 + h] = pack_f16x2(e0, e1);
+                        } else {
+                            pk[2 * c4 + h] = pack_bf16x2(e0, e1);
+                        }
                     }
                 }
-                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                {
+                    float a0, a1, b0, b1;
+                    f2_split(ps[0], a0, a1);
+                    f2_split(ps[1], b0, b1);
+                    l += (a0 + b0) + (a1 + b1);
+                }
                 // P buffer sb is free once P V(it-2) has finished (PP: this
                 // set's previous P V).  P V of tile j completes a phase of
                 // o_done[j & 1]; the next phase of that barrier needs this
@@ -371,10 +408,10 @@ __device__ void softmax_role(const Cta& x) {
             if (!KV8 && ok && nvalid % BH != 0 && ltid < 32) {
                 // keys past the sequence end inside its last page: zero their V
                 // rows so that 0 * (stale or canary) never reaches O
-                ok = warp_wait(&bars[Smem::B_KVFULL + it % NS], (it / NS) & 1, x.abort_flag,
-                               a.dev_err);  // bf16: landing stage == operand stage
+                ok = warp_wait(&bars[Smem::B_VFULL + it % NV], (it / NV) & 1, x.abort_flag,
+                               a.dev_err);
                 if (ok) {
-                    uint8_t* vst = x.sm + Smem::STAGES + (it % NS) * STAGE_BYTES + KV_BYTES;
+                    uint8_t* vst = x.sm + Smem::VRING + (it % NV) * KV_BYTES;
                     const int bx = nvalid / BH, r_end = BH;
                     for (int e = (nvalid % BH) * 16 + lane; e < r_end * 16; e += 32) {
                         const int rr = e / 16, h = (e / 8) & 1, ch = e % 8;
@@ -392,16 +429,17 @@ __device__ void softmax_role(const Cta& x) {
             named_bar_sync(6 + set, 128);
             if (ltid == 0) {
                 tc_fence_after();
-                const int s = it % Smem::NM;
-                // V landed (bf16) / was widened (INT8); the wait that led to S
-                // already implies it, this one makes the ordering explicit
+                // INT8: the operand stage of tile it, widened; bf16: V slot it % NV
+                const int s = KV8 ? it % Smem::NM : it % NV;
+                const int nuse = KV8 ? it / Smem::NM : it / NV;
                 if (ok)
-                    ok = mbar_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_KVFULL + s],
-                                   (it / Smem::NM) & 1, x.abort_flag, a.dev_err);
+                    ok = mbar_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_VFULL + s], nuse & 1,
+                                   x.abort_flag, a.dev_err);
                 if (ok) {
                     // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
                     const int nbox = (nvalid + BOX_ROWS - 1) / BOX_ROWS;
-                    const uint64_t vd = vdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                    const uint64_t vd =
+                        vdesc0 + ((uint32_t)(s * (KV8 ? STAGE_BYTES : KV_BYTES)) >> 4);
                     const uint32_t pcol = x.tmem + TM_P + sb * (TN / 2);
 #pragma unroll
                     for (int bx = 0; bx < MAX_BOX; ++bx)
@@ -409,7 +447,8 @@ __device__ void softmax_role(const Cta& x) {
                             umma_ts(x.tmem + o_mine, pcol + bx * (BOX_ROWS / 2),
                                     vd + ((bx * BOX_ROWS * 256) >> 4), idesc_pv<KV8>(),
                                     (bx > 0 || has) ? 1u : 0u);
-                    umma_commit(&bars[Smem::B_KVEMPTY + s]);
+                    // INT8: the operand stage is free; bf16: the V slot is
+                    umma_commit(&bars[KV8 ? Smem::B_KVEMPTY + s : Smem::B_VEMPTY + s]);
                     umma_commit(&bars[Smem::B_ODONE + sb]);
                 }
             }
@@ -679,6 +718,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&bars[Smem::B_KREADY + s], KV8 ? 4 : 1);
             mbar_init(&bars[Smem::B_KVEMPTY + s], 1);
         }
+        if (!KV8)
+            for (int s = 0; s < NV; ++s) {
+                mbar_init(&bars[Smem::B_VFULL + s], 1);
+                mbar_init(&bars[Smem::B_VEMPTY + s], 1);
+            }
         mbar_init(&bars[Smem::B_QFULL], 1);
         mbar_init(&bars[Smem::B_QFREE], 1);
         mbar_init(&bars[Smem::B_QCP], 1);
@@ -743,11 +787,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (warp == 6) {
         // ================= TMA producer (warp 6) =================
-        // One 3-D box per (page, tensor): both 64-column halves of BH keys of
-        // one kv-head, 256*BH bytes, landing as [half][key][128 B] with the
-        // 128-byte swizzle the MMAs read.  Boxes of a tile are issued by
-        // parallel lanes; block-table entries are prefetched LOOKAHEAD tiles
-        // ahead with cp.async.
+        // Q of each piece, and K (bf16 cache) or the raw K, V and scales
+        // (INT8 cache).  Boxes cover both 64-column halves of their keys of
+        // one kv-head, landing as [half][key][128 B] with the 128-byte
+        // swizzle the MMAs read.  Boxes of a tile are issued by parallel
+        // lanes; block-table entries are prefetched LOOKAHEAD tiles ahead
+        // with cp.async.
         Cursor cur, ahead;
         if (n_tiles > 0) {
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
@@ -812,15 +857,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
             const int nbox = (nvalid + BH - 1) / BH;
             if (lane == 0) {
-                // bf16: the stage is free once P V has read it; INT8: once the
-                // converter warps have widened it
+                // bf16: the K slot is free once Q K^T has read it; INT8: the
+                // raw stage once the converter warps have widened it
                 if (use >= 1)
                     ok = mbar_wait(&bars[Smem::B_RAWFREE + s], (use - 1) & 1, abort_flag,
                                    a.dev_err);
                 if (ok)
                     mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
                                           KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
-                                              : (nvalid + 7) / 8 * 2048u + nbox * 4096u);
+                                              : (nvalid + 7) / 8 * 2048u);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -846,24 +891,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                   &bars[Smem::B_KVFULL + s]);
                 }
             } else {
-                // K: 8-key boxes (lanes 0-7, 2 KB: both head-dim halves of 8
-                // full rows) landing as [half 0 | half 1], so 8-key group g of
-                // half h sits at g*2 KB + h*1 KB -- the uniform stride an N = 64
-                // Q K^T reads, with no relayout.  V: 16-key boxes (lanes 16-19,
-                // 4 KB) in the layout P V reads.
-                const bool isv = lane >= 16;
-                const int j = isv ? lane - 16 : lane;
-                if (isv ? j < nbox : j * 8 < nvalid) {
-                    const int bx = isv ? j : j >> 1;  // 16-key slice (one page)
-                    int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
+                // 8-key boxes (lane j, 2 KB: both head-dim halves of 8 full
+                // rows) landing as [half 0 | half 1], so 8-key group g of half
+                // h sits at g*2 KB + h*1 KB -- the uniform stride an N = 64
+                // Q K^T reads, with no relayout
+                if (lane * 8 < nvalid) {
+                    int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + (lane >> 1)];
                     if (page < 0 || page >= a.num_pages) {
                         raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
                         page = 0;
                     }
-                    const int row = (page * Hkv + cur.kvh) * P + (key0 + j * (isv ? 16 : 8)) % P;
-                    tma_load_3d_hint(st + (isv ? KV_BYTES + j * 4096 : j * 2048),
-                                     isv ? (const void*)&vmap : (const void*)&kmap,
-                                     &bars[Smem::B_KVFULL + s], 0, row, 0, pol);
+                    const int row = (page * Hkv + cur.kvh) * P + (key0 + lane * 8) % P;
+                    tma_load_3d_hint(st + lane * 2048, &kmap, &bars[Smem::B_KVFULL + s], 0, row,
+                                     0, pol);
                 }
             }
             n_issued = it + 1;
@@ -879,6 +919,75 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
             if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
         }
+    } else if (!KV8 && warp == 7) {
+        // ================= V producer (warp 7, bf16 cache) =================
+        // 16-key boxes (4 KB: both halves of one page slice), lane j taking
+        // box j, into NV slots laid out as P V reads them; a slot is freed
+        // by the P V that read it, so V may run well ahead of the softmax
+        // without holding K slots.  Block-table entries are prefetched as
+        // for K, into a ring of this warp's own.
+        int* vpid = reinterpret_cast<int*>(sm + Smem::PIDS_V);
+        Cursor cur, ahead;
+        if (n_tiles > 0) {
+            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            ahead = cur;
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        auto fetch_pids = [&](int slot, const Cursor& c) {
+            const int key0 = c.lt * TN;
+            const int nvalid = min(TN, s_ctx[c.b] + k - key0);
+            if (lane * BH < nvalid)
+                cp_async_4(&vpid[slot * MAX_BOX + lane],
+                           &a.block_table[(int64_t)c.b * a.max_pages + (key0 + lane * BH) / P]);
+        };
+        for (int la = 0; la < LOOKAHEAD; ++la) {
+            if (la < n_tiles) {
+                fetch_pids(la % (LOOKAHEAD + 1), ahead);
+                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+        }
+        int n_issued = 0;
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            if (it + LOOKAHEAD < n_tiles) {
+                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
+                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+            }
+            cp_async_commit();
+            cp_async_wait<LOOKAHEAD>();
+            __syncwarp();
+            const int s = it % NV, use = it / NV;
+            const int key0 = cur.lt * TN;
+            const int nbox = (min(TN, s_ctx[cur.b] + k - key0) + BH - 1) / BH;
+            if (lane == 0) {
+                if (use >= 1)
+                    ok = mbar_wait(&bars[Smem::B_VEMPTY + s], (use - 1) & 1, abort_flag,
+                                   a.dev_err);
+                if (ok) mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], nbox * 4096u);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane < nbox) {
+                int page = vpid[(it % (LOOKAHEAD + 1)) * MAX_BOX + lane];
+                if (page < 0 || page >= a.num_pages) {
+                    raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
+                    page = 0;
+                }
+                const int row = (page * Hkv + cur.kvh) * P + (key0 + lane * BH) % P;
+                tma_load_3d_hint(sm + Smem::VRING + s * KV_BYTES + lane * 4096, &vmap,
+                                 &bars[Smem::B_VFULL + s], 0, row, 0, pol);
+            }
+            n_issued = it + 1;
+            __syncwarp();
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+        }
+        cp_async_wait<0>();
+        if (!ok && lane == 0)
+            for (int s = 0; s < NV; ++s) {
+                const int uses = n_issued > s ? (n_issued - 1 - s) / NV + 1 : 0;
+                if (uses > 0) mbar_drain(&bars[Smem::B_VFULL + s], (uses - 1) & 1);
+            }
     } else if (KV8 && warp >= 8) {
         // ================= INT8 widening (warps 8-11) =================
         // Raw stage -> operand stage: K lands in the order the N = 64
@@ -1002,7 +1111,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                             umma_commit(&bars[Smem::B_QFREE]);
                         }
                         // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
-                        const uint64_t kd = kdesc0 + ((uint32_t)(s * STAGE_BYTES) >> 4);
+                        const uint64_t kd =
+                            kdesc0 + ((uint32_t)(s * (KV8 ? STAGE_BYTES : KV_BYTES)) >> 4);
                         const uint32_t dcol = tmem + TM_S + sq * TN;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
@@ -1010,6 +1120,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                     kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, kIdescQK,
                                     kk ? 1u : 0u);
                         umma_commit(&bars[Smem::B_SFULL + sq]);
+                        // bf16: the K slot is free as soon as Q K^T has read it
+                        if (!KV8) umma_commit(&bars[Smem::B_KVEMPTY + s]);
                     }
                     __syncwarp();
                 }
