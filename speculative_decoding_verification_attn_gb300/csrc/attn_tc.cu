@@ -47,13 +47,13 @@ namespace {
 constexpr int D = 128;
 constexpr int TN = 64;           // keys per tile
 constexpr int NK = 3;            // bf16 cache: K slots (freed when Q K^T has read them)
-constexpr int NV = 7;            // bf16 cache: V slots (freed when P V has read them)
+constexpr int NV = 6;            // bf16 cache: V slots (freed when P V has read them)
 constexpr int ROWS = 128;        // MMA M: query rows (padded / replicated)
 constexpr int Q_HALF = ROWS * 128;        // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;       // 32 KB
 constexpr int KV_BYTES = TN * D * 2;      // 16 KB per tensor per stage
 constexpr int STAGE_BYTES = 2 * KV_BYTES; // K then V
-constexpr int LOOKAHEAD = 6;              // tiles of block-table prefetch
+constexpr int LOOKAHEAD_TILES = 6;        // block-table prefetch distance (all producers)
 constexpr int BOX_ROWS = 16;              // keys per TMA box: 16 rows x 256 B = 4 KB
 constexpr int MAX_BOX = TN / BOX_ROWS;    // boxes per tile
 // TMEM columns: S buffers [0,128) (2 x 64 fp32); O [128,256) and, for the
@@ -123,10 +123,17 @@ struct SmemT {
                          B_DRAIN = B_ODONE + 2, B_QCP = B_DRAIN + 3,
                          NUM_BARS = B_QCP + 1;
     static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
-    static constexpr int STAT = MISC + 16;                     // [2][4][128] float (m, l)
-    static constexpr int PIDS = STAT + 2 * 4 * ROWS * 4;       // [LOOKAHEAD+1][MAX_BOX] int
-    static constexpr int PIDS_V = PIDS + (LOOKAHEAD + 1) * MAX_BOX * 4;  // the V producer's
-    static constexpr int CTX = PIDS_V + (LOOKAHEAD + 1) * MAX_BOX * 4;  // [MAX_BATCH] int
+    // (m, l) of [set x copy][row]: bf16 two sets x up to 4 copies, INT8 one set
+    static constexpr int NSTAT = KV8 ? 4 : 8;
+    static constexpr int STAT = MISC + 16;
+    // TMA producer warps (5, 6, ...): tile it is issued by warp 5 + it % NPROD.
+    // bf16: three, since one issuing thread caps the bytes a CTA keeps in
+    // flight; INT8: one (its raw boxes are small and the widening warps set
+    // the pace, and idle producers' polling takes issue slots from them)
+    static constexpr int NPROD = KV8 ? 1 : 3;
+    static constexpr int LOOKAHEAD = LOOKAHEAD_TILES / NPROD;  // own tiles ahead
+    static constexpr int PIDS = STAT + 2 * NSTAT * ROWS * 4;  // [NPROD][LOOKAHEAD+1][MAX_BOX] int
+    static constexpr int CTX = PIDS + NPROD * (LOOKAHEAD + 1) * MAX_BOX * 4;  // [MAX_BATCH] int
     static constexpr int PRE = CTX + MAX_BATCH * 4;           // [MAX_BATCH+1] int
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
 };
@@ -135,6 +142,12 @@ constexpr size_t smem_bytes() { return SmemT<KV8>::END + 1024; }  // + alignment
 static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory budget (bf16)");
 static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory budget (INT8)");
 static_assert(SmemT<true>::RAW % 128 == 0 && RAW8_STAGE % 128 == 0, "TMA destination alignment");
+// every ring slot is filled by one producer warp only, so that a warp's
+// parity waits on a slot are in the slot's phase order
+static_assert(NK % SmemT<false>::NPROD == 0 && NV % SmemT<false>::NPROD == 0 &&
+                  NSR % SmemT<true>::NPROD == 0,
+              "slot ownership");
+static_assert(SmemT<false>::NPROD <= 3 && SmemT<true>::NPROD <= 3, "producers are warps 5-7");
 // warps: softmax and P V issue 0-3, Q K^T 4, TMA producer 6 (bf16: K), V
 // producer 7 (bf16; idle with INT8), 5 idle, then a second set of softmax
 // warps 8-11 (bf16) or the INT8 widening warps 8-11
@@ -213,7 +226,6 @@ __device__ __forceinline__ void store_cols(uint32_t taddr, const uint32_t* v) {
 template <int REP, bool KV8, bool PP>
 __device__ void softmax_role(const Cta& x) {
     using Smem = SmemT<KV8>;
-    static_assert(!PP || REP == 1, "ping-pong only with one copy");
     constexpr int RQ = REP == 4 ? 32 : REP == 2 ? 64 : ROWS;
     constexpr int CW = TN / REP;  // key columns of a tile owned by one thread
     const AttnArgs& a = *x.a;
@@ -232,16 +244,17 @@ __device__ void softmax_role(const Cta& x) {
     const uint32_t lane_base = x.tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t o_mine = TM_O + set * D;         // this set's O columns
     float* s_stat_m = reinterpret_cast<float*>(x.sm + Smem::STAT);
-    float* s_stat_l = s_stat_m + 4 * ROWS;
+    float* s_stat_l = s_stat_m + Smem::NSTAT * ROWS;
     uint64_t* bars = x.bars;
     const uint64_t vdesc0 = umma_sdesc_sw128(
         smem_u32(x.sm + (KV8 ? Smem::STAGES + KV_BYTES : Smem::VRING)), BOX_ROWS * 128, 1024);
 
     if (REP > 1) {
-        // both P buffers start at zero: a lane only ever rewrites its copy's slice
+        // P buffers start at zero: a lane only ever rewrites its copy's slice
+        // (PP: each set its own buffer)
         const uint32_t zero[32] = {};
-        tmem_st32(lane_base + TM_P, zero);
-        tmem_st32(lane_base + TM_P + TN / 2, zero);
+        if (!PP || set == 0) tmem_st32(lane_base + TM_P, zero);
+        if (!PP || set == 1) tmem_st32(lane_base + TM_P + TN / 2, zero);
         tmem_wait_st();
     }
     float m_ref = -INFINITY, l = 0.f;
@@ -427,13 +440,15 @@ __device__ void softmax_role(const Cta& x) {
             // which the softmax warps would starve of issue slots
             tc_fence_before();
             named_bar_sync(6 + set, 128);
-            if (ltid == 0) {
+            if (ltid < 32) {
+                // the set's warp 0 issues, converged, one elected lane
+                __syncwarp();
                 tc_fence_after();
                 // INT8: the operand stage of tile it, widened; bf16: V slot it % NV
                 const int s = KV8 ? it % Smem::NM : it % NV;
                 const int nuse = KV8 ? it / Smem::NM : it / NV;
                 if (ok)
-                    ok = mbar_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_VFULL + s], nuse & 1,
+                    ok = warp_wait(&bars[KV8 ? Smem::B_KREADY + s : Smem::B_VFULL + s], nuse & 1,
                                    x.abort_flag, a.dev_err);
                 if (ok) {
                     // V box bx: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
@@ -441,18 +456,17 @@ __device__ void softmax_role(const Cta& x) {
                     const uint64_t vd =
                         vdesc0 + ((uint32_t)(s * (KV8 ? STAGE_BYTES : KV_BYTES)) >> 4);
                     const uint32_t pcol = x.tmem + TM_P + sb * (TN / 2);
+                    umma_ts_w(x.tmem + o_mine, pcol, vd, idesc_pv<KV8>(), has ? 1u : 0u);
 #pragma unroll
-                    for (int bx = 0; bx < MAX_BOX; ++bx)
+                    for (int bx = 1; bx < MAX_BOX; ++bx)
                         if (bx < nbox)
-                            umma_ts(x.tmem + o_mine, pcol + bx * (BOX_ROWS / 2),
-                                    vd + ((bx * BOX_ROWS * 256) >> 4), idesc_pv<KV8>(),
-                                    (bx > 0 || has) ? 1u : 0u);
+                            umma_ts_w(x.tmem + o_mine, pcol + bx * (BOX_ROWS / 2),
+                                      vd + ((bx * BOX_ROWS * 256) >> 4), idesc_pv<KV8>(), 1u);
                     // INT8: the operand stage is free; bf16: the V slot is
-                    umma_commit(&bars[KV8 ? Smem::B_KVEMPTY + s : Smem::B_VEMPTY + s]);
-                    umma_commit(&bars[Smem::B_ODONE + sb]);
+                    umma_commit_w(&bars[KV8 ? Smem::B_KVEMPTY + s : Smem::B_VEMPTY + s]);
+                    umma_commit_w(&bars[Smem::B_ODONE + sb]);
                 }
             }
-            if (ltid < 32) ok = __shfl_sync(0xffffffffu, ok, 0);
             has = true;
         }
 
@@ -560,24 +574,29 @@ __device__ void softmax_role(const Cta& x) {
                     }
                 }
             } else {
-                // merge the REP copies of every row: weights from (m, l), the
-                // weighted O rows summed in fp32 in the scratch buffer (rows
-                // swizzled by 16-byte chunk), one or two column passes
+                // merge the states of every row -- REP copies, times two sets
+                // with PP -- with weights from (m, l): the weighted O rows
+                // are summed in fp32 in the scratch buffer (rows swizzled by
+                // 16-byte chunk), one or two column passes
+                constexpr int NSET = PP ? 2 : 1;
+                constexpr int NTH = 128 * NSET;  // threads of the merge
+                const int st_mine = set * REP + c;
                 if (row_valid) {
-                    s_stat_m[c * ROWS + r] = m_ref;
-                    s_stat_l[c * ROWS + r] = l;
+                    // a set without a tile of this piece: m = -inf, l = 0
+                    s_stat_m[st_mine * ROWS + r] = m_ref;
+                    s_stat_l[st_mine * ROWS + r] = l;
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, NTH);
                 float w = 0.f, lse = -INFINITY;
                 if (row_valid) {
                     float mt = -INFINITY;
 #pragma unroll
-                    for (int cc = 0; cc < REP; ++cc) mt = fmaxf(mt, s_stat_m[cc * ROWS + r]);
+                    for (int sc = 0; sc < NSET * REP; ++sc) mt = fmaxf(mt, s_stat_m[sc * ROWS + r]);
                     float Lsum = 0.f;
 #pragma unroll
-                    for (int cc = 0; cc < REP; ++cc) {
-                        const float mc = s_stat_m[cc * ROWS + r];
-                        if (mc != -INFINITY) Lsum += s_stat_l[cc * ROWS + r] * fast_exp2(mc - mt);
+                    for (int sc = 0; sc < NSET * REP; ++sc) {
+                        const float mc = s_stat_m[sc * ROWS + r];
+                        if (mc != -INFINITY) Lsum += s_stat_l[sc * ROWS + r] * fast_exp2(mc - mt);
                     }
                     w = (Lsum > 0.f && m_ref != -INFINITY) ? fast_exp2(m_ref - mt) / Lsum : 0.f;
                     lse = Lsum > 0.f ? (mt + log2f(Lsum)) * kLn2 : -INFINITY;
@@ -589,12 +608,12 @@ __device__ void softmax_role(const Cta& x) {
 #pragma unroll
                 for (int pass = 0; pass < D / CPP; ++pass) {
 #pragma unroll 1
-                    for (int cc = 0; cc < REP; ++cc) {
-                        if (ok && warp_active && c == cc) {
+                    for (int sc = 0; sc < NSET * REP; ++sc) {
+                        if (ok && warp_active && st_mine == sc) {
 #pragma unroll
                             for (int c4 = 0; c4 < CPP / 32; ++c4) {
                                 uint32_t ov[32];
-                                tmem_ld32(lane_base + TM_O + pass * CPP + c4 * 32, ov);
+                                tmem_ld32(lane_base + o_mine + pass * CPP + c4 * 32, ov);
                                 tmem_wait_ld();
                                 if (!row_valid) continue;
 #pragma unroll
@@ -602,11 +621,15 @@ __device__ void softmax_role(const Cta& x) {
                                     const int chunk = c4 * 8 + v;
                                     float4* dst = reinterpret_cast<float4*>(
                                         scratch + r * CPP + ((chunk ^ (r & (NCH - 1))) * 4));
-                                    float4 o = make_float4(__uint_as_float(ov[4 * v + 0]) * w,
-                                                           __uint_as_float(ov[4 * v + 1]) * w,
-                                                           __uint_as_float(ov[4 * v + 2]) * w,
-                                                           __uint_as_float(ov[4 * v + 3]) * w);
-                                    if (cc > 0) {
+                                    // weight 0: a state without keys (its O is
+                                    // stale or never written) adds nothing
+                                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                                    if (w > 0.f)
+                                        o = make_float4(__uint_as_float(ov[4 * v + 0]) * w,
+                                                        __uint_as_float(ov[4 * v + 1]) * w,
+                                                        __uint_as_float(ov[4 * v + 2]) * w,
+                                                        __uint_as_float(ov[4 * v + 3]) * w);
+                                    if (sc > 0) {
                                         const float4 prev = *dst;
                                         o.x += prev.x;
                                         o.y += prev.y;
@@ -617,10 +640,10 @@ __device__ void softmax_role(const Cta& x) {
                                 }
                             }
                         }
-                        named_bar_sync(1, 128);
+                        named_bar_sync(1, NTH);
                     }
                     if (ok) {
-                        for (int idx = tid; idx < R * NCH; idx += 128) {
+                        for (int idx = ltid + set * 128; idx < R * NCH; idx += NTH) {
                             const int rr = idx / NCH, chunk = idx % NCH;
                             const float4 o = *reinterpret_cast<const float4*>(
                                 scratch + rr * CPP + ((chunk ^ (rr & (NCH - 1))) * 4));
@@ -637,9 +660,9 @@ __device__ void softmax_role(const Cta& x) {
                             }
                         }
                     }
-                    named_bar_sync(1, 128);  // scratch reused by the next pass / piece
+                    named_bar_sync(1, NTH);  // scratch reused by the next pass / piece
                 }
-                if (ok && row_valid && c == 0) {
+                if (ok && row_valid && st_mine == 0) {
                     if (complete) {
                         if (a.lse) a.lse[out_row(r)] = lse;
                     } else {
@@ -651,9 +674,10 @@ __device__ void softmax_role(const Cta& x) {
         if (it + 1 < x.n_tiles) cur.next(x.s_ctx, a.Hkv, k);
     }
     // every P V issued from here must finish before TMEM is released
-    if (ltid == 0 && x.n_tiles > 0) {
-        umma_commit(&bars[Smem::B_DRAIN + 1 + set]);
-        mbar_drain(&bars[Smem::B_DRAIN + 1 + set], 0);
+    if (ltid < 32 && x.n_tiles > 0) {
+        __syncwarp();
+        umma_commit_w(&bars[Smem::B_DRAIN + 1 + set]);
+        if (lane == 0) mbar_drain(&bars[Smem::B_DRAIN + 1 + set], 0);
     }
     __syncwarp();
 }
@@ -785,209 +809,154 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
 
-    if (warp == 6) {
-        // ================= TMA producer (warp 6) =================
-        // Q of each piece, and K (bf16 cache) or the raw K, V and scales
-        // (INT8 cache).  Boxes cover both 64-column halves of their keys of
-        // one kv-head, landing as [half][key][128 B] with the 128-byte
-        // swizzle the MMAs read.  Boxes of a tile are issued by parallel
-        // lanes; block-table entries are prefetched LOOKAHEAD tiles ahead
-        // with cp.async.
+    if (warp >= 5 && warp < 5 + Smem::NPROD) {
+        // ================= TMA producers (warps 5 .. 4 + NPROD) =================
+        // Tile it is issued by warp 5 + it % NPROD: one issuing thread caps
+        // what a CTA can have in flight, several keep HBM busy.  A warp owns
+        // its ring slots (slot counts are multiples of NPROD).  Boxes cover
+        // both 64-column halves of their keys of one kv-head, landing as
+        // [half][key][128 B] with the 128-byte swizzle the MMAs read; the
+        // boxes of a tile are issued by parallel lanes, block-table entries
+        // prefetched LOOKAHEAD own tiles ahead with cp.async.
+        const int pw = warp - 5;
+        int* pids = pid_ring + pw * (Smem::LOOKAHEAD + 1) * MAX_BOX;
+        const int n_own = n_tiles > pw ? (n_tiles - 1 - pw) / Smem::NPROD + 1 : 0;
         Cursor cur, ahead;
-        if (n_tiles > 0) {
-            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+        if (n_own > 0) {
+            cur.init(t_begin + pw, s_pre, s_ctx, B, Hkv, k);
             ahead = cur;
         }
+        // from tile `from` to this warp's next one
+        auto advance = [&](Cursor& c, int from) {
+            for (int j = 1; j <= Smem::NPROD; ++j)
+                if (from + j < n_tiles) c.next(s_ctx, Hkv, k);
+        };
         const uint64_t pol = l2_policy_evict_first();
-        if (lane == 0) {
-            prefetch_tmap(&qmap);
+        if (lane == 0 && pw == 0) {
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
         }
         auto fetch_pids = [&](int slot, const Cursor& c) {
             const int key0 = c.lt * TN;
             const int nvalid = min(TN, s_ctx[c.b] + k - key0);
-            const int nbox = (nvalid + BH - 1) / BH;
-            if (lane < nbox) {
-                const int lp = (key0 + lane * BH) / P;
-                cp_async_4(&pid_ring[slot * MAX_BOX + lane],
-                           &a.block_table[(int64_t)c.b * a.max_pages + lp]);
-            }
+            if (lane * BH < nvalid)
+                cp_async_4(&pids[slot * MAX_BOX + lane],
+                           &a.block_table[(int64_t)c.b * a.max_pages + (key0 + lane * BH) / P]);
         };
-        for (int la = 0; la < LOOKAHEAD; ++la) {
-            if (la < n_tiles) {
-                fetch_pids(la % (LOOKAHEAD + 1), ahead);
-                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+        for (int la = 0; la < Smem::LOOKAHEAD; ++la) {
+            if (la < n_own) {
+                fetch_pids(la % (Smem::LOOKAHEAD + 1), ahead);
+                advance(ahead, pw + la * Smem::NPROD);
             }
             cp_async_commit();
         }
-        int pc = -1;
-        int n_issued = 0;
-        int issued_q = 0;
+        int nk_issued = 0, nv_issued = 0;  // own tiles whose K (raw stage) / V went out
         bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            if (it + LOOKAHEAD < n_tiles) {
-                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
-                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
+        for (int q = 0; q < n_own && ok; ++q) {
+            const int it = pw + q * Smem::NPROD;
+            if (q + Smem::LOOKAHEAD < n_own) {
+                fetch_pids((q + Smem::LOOKAHEAD) % (Smem::LOOKAHEAD + 1), ahead);
+                advance(ahead, pw + (q + Smem::LOOKAHEAD) * Smem::NPROD);
             }
             cp_async_commit();
-            cp_async_wait<LOOKAHEAD>();  // entries of tile `it`
+            cp_async_wait<Smem::LOOKAHEAD>();  // entries of tile `it`
             __syncwarp();
-            const bool first = (it == 0) || (cur.lt == 0);
-            if (first) {
-                // Q of the next piece once the previous one has been copied to TMEM
-                ++pc;
-                if (lane == 0) {
-                    if (pc >= 1)
-                        ok = mbar_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag, a.dev_err);
-                    if (ok) {
-                        mbar_arrive_expect_tx(&bars[Smem::B_QFULL], REP * 2 * R * 128);
-                        for (int c = 0; c < REP; ++c)
-                            for (int h = 0; h < 2; ++h)
-                                tma_load_3d(sm + Smem::Q + h * Q_HALF + c * RQ * 128, &qmap,
-                                            &bars[Smem::B_QFULL], h * 64, cur.kvh * G, cur.b * k);
-                        issued_q = pc + 1;
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-            const int s = it % NL, use = it / NL;
+            const int* pid = pids + (q % (Smem::LOOKAHEAD + 1)) * MAX_BOX;
             const int key0 = cur.lt * TN;
             const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
             const int nbox = (nvalid + BH - 1) / BH;
-            if (lane == 0) {
-                // bf16: the K slot is free once Q K^T has read it; INT8: the
-                // raw stage once the converter warps have widened it
-                if (use >= 1)
-                    ok = mbar_wait(&bars[Smem::B_RAWFREE + s], (use - 1) & 1, abort_flag,
-                                   a.dev_err);
-                if (ok)
-                    mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
-                                          KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
-                                              : (nvalid + 7) / 8 * 2048u);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            uint8_t* st = sm + Smem::RAW + s * Smem::RAW_STAGE;
-            if constexpr (KV8) {
-                if (lane < 4 * nbox) {
-                    const int bx = lane >> 2;
-                    int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + bx];
-                    if (page < 0 || page >= a.num_pages) {
-                        raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
-                        page = 0;
-                    }
-                    const int row = (page * Hkv + cur.kvh) * P + (key0 + bx * BH) % P;
-                    // lane & 3: K box, V box (16 rows x 128 int8), k / v scales (16 fp16)
-                    const int what = lane & 3;
-                    if (what < 2)
-                        tma_load_2d(st + what * RAW8_KV + bx * BH * D,
-                                    what ? (const void*)&vmap : (const void*)&kmap,
-                                    &bars[Smem::B_KVFULL + s], 0, row, pol);
-                    else
-                        bulk_load(st + 2 * RAW8_KV + (what - 2) * TN * 2 + bx * BH * 2,
-                                  (what == 2 ? a.k_scale : a.v_scale) + row, BH * 2,
-                                  &bars[Smem::B_KVFULL + s]);
-                }
-            } else {
-                // 8-key boxes (lane j, 2 KB: both head-dim halves of 8 full
-                // rows) landing as [half 0 | half 1], so 8-key group g of half
-                // h sits at g*2 KB + h*1 KB -- the uniform stride an N = 64
-                // Q K^T reads, with no relayout
-                if (lane * 8 < nvalid) {
-                    int page = pid_ring[(it % (LOOKAHEAD + 1)) * MAX_BOX + (lane >> 1)];
-                    if (page < 0 || page >= a.num_pages) {
-                        raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
-                        page = 0;
-                    }
-                    const int row = (page * Hkv + cur.kvh) * P + (key0 + lane * 8) % P;
-                    tma_load_3d_hint(st + lane * 2048, &kmap, &bars[Smem::B_KVFULL + s], 0, row,
-                                     0, pol);
-                }
-            }
-            n_issued = it + 1;
-            __syncwarp();
-            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
-        }
-        cp_async_wait<0>();
-        if (!ok && lane == 0) {
-            // drain: wait (bounded) for the copies this CTA issued
-            for (int s = 0; s < NL; ++s) {
-                const int uses = n_issued > s ? (n_issued - 1 - s) / NL + 1 : 0;
-                if (uses > 0) mbar_drain(&bars[Smem::B_KVFULL + s], (uses - 1) & 1);
-            }
-            if (issued_q > 0) mbar_drain(&bars[Smem::B_QFULL], (issued_q - 1) & 1);
-        }
-    } else if (!KV8 && warp == 7) {
-        // ================= V producer (warp 7, bf16 cache) =================
-        // 16-key boxes (4 KB: both halves of one page slice), lane j taking
-        // box j, into NV slots laid out as P V reads them; a slot is freed
-        // by the P V that read it, so V may run well ahead of the softmax
-        // without holding K slots.  Block-table entries are prefetched as
-        // for K, into a ring of this warp's own.
-        int* vpid = reinterpret_cast<int*>(sm + Smem::PIDS_V);
-        Cursor cur, ahead;
-        if (n_tiles > 0) {
-            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
-            ahead = cur;
-        }
-        const uint64_t pol = l2_policy_evict_first();
-        auto fetch_pids = [&](int slot, const Cursor& c) {
-            const int key0 = c.lt * TN;
-            const int nvalid = min(TN, s_ctx[c.b] + k - key0);
-            if (lane * BH < nvalid)
-                cp_async_4(&vpid[slot * MAX_BOX + lane],
-                           &a.block_table[(int64_t)c.b * a.max_pages + (key0 + lane * BH) / P]);
-        };
-        for (int la = 0; la < LOOKAHEAD; ++la) {
-            if (la < n_tiles) {
-                fetch_pids(la % (LOOKAHEAD + 1), ahead);
-                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
-            }
-            cp_async_commit();
-        }
-        int n_issued = 0;
-        bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            if (it + LOOKAHEAD < n_tiles) {
-                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
-                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
-            }
-            cp_async_commit();
-            cp_async_wait<LOOKAHEAD>();
-            __syncwarp();
-            const int s = it % NV, use = it / NV;
-            const int key0 = cur.lt * TN;
-            const int nbox = (min(TN, s_ctx[cur.b] + k - key0) + BH - 1) / BH;
-            if (lane == 0) {
-                if (use >= 1)
-                    ok = mbar_wait(&bars[Smem::B_VEMPTY + s], (use - 1) & 1, abort_flag,
-                                   a.dev_err);
-                if (ok) mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], nbox * 4096u);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane < nbox) {
-                int page = vpid[(it % (LOOKAHEAD + 1)) * MAX_BOX + lane];
+            auto page_of = [&](int bx) {
+                int page = pid[bx];
                 if (page < 0 || page >= a.num_pages) {
                     raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
                     page = 0;
                 }
-                const int row = (page * Hkv + cur.kvh) * P + (key0 + lane * BH) % P;
-                tma_load_3d_hint(sm + Smem::VRING + s * KV_BYTES + lane * 4096, &vmap,
-                                 &bars[Smem::B_VFULL + s], 0, row, 0, pol);
+                return page;
+            };
+            {
+                // K (bf16) / raw stage (INT8): free once Q K^T read it / the
+                // converter warps widened it
+                const int s = it % NL, use = it / NL;
+                if (lane == 0) {
+                    if (use >= 1)
+                        ok = mbar_wait(&bars[Smem::B_RAWFREE + s], (use - 1) & 1, abort_flag,
+                                       a.dev_err);
+                    if (ok)
+                        mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
+                                              KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
+                                                  : (nvalid + 7) / 8 * 2048u);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                uint8_t* st = sm + Smem::RAW + s * Smem::RAW_STAGE;
+                if constexpr (KV8) {
+                    if (lane < 4 * nbox) {
+                        const int bx = lane >> 2;
+                        const int row = (page_of(bx) * Hkv + cur.kvh) * P + (key0 + bx * BH) % P;
+                        // lane & 3: K box, V box (16 rows x 128 int8), k / v scales (16 fp16)
+                        const int what = lane & 3;
+                        if (what < 2)
+                            tma_load_2d(st + what * RAW8_KV + bx * BH * D,
+                                        what ? (const void*)&vmap : (const void*)&kmap,
+                                        &bars[Smem::B_KVFULL + s], 0, row, pol);
+                        else
+                            bulk_load(st + 2 * RAW8_KV + (what - 2) * TN * 2 + bx * BH * 2,
+                                      (what == 2 ? a.k_scale : a.v_scale) + row, BH * 2,
+                                      &bars[Smem::B_KVFULL + s]);
+                    }
+                } else {
+                    // 8-key boxes (lane j, 2 KB: both head-dim halves of 8 full
+                    // rows) landing as [half 0 | half 1], so 8-key group g of
+                    // half h sits at g*2 KB + h*1 KB -- the uniform stride an
+                    // N = 64 Q K^T reads, with no relayout
+                    if (lane * 8 < nvalid) {
+                        const int row = (page_of(lane >> 1) * Hkv + cur.kvh) * P +
+                                        (key0 + lane * 8) % P;
+                        tma_load_3d_hint(st + lane * 2048, &kmap, &bars[Smem::B_KVFULL + s], 0,
+                                         row, 0, pol);
+                    }
+                }
+                nk_issued = q + 1;
             }
-            n_issued = it + 1;
+            if constexpr (!KV8) {
+                // V: 16-key boxes (4 KB) in the layout P V reads, into slot
+                // it % NV, free once P V of tile it - NV has read it
+                const int s = it % NV, use = it / NV;
+                if (lane == 0) {
+                    if (use >= 1)
+                        ok = mbar_wait(&bars[Smem::B_VEMPTY + s], (use - 1) & 1, abort_flag,
+                                       a.dev_err);
+                    if (ok) mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], nbox * 4096u);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane < nbox) {
+                    const int row = (page_of(lane) * Hkv + cur.kvh) * P + (key0 + lane * BH) % P;
+                    tma_load_3d_hint(sm + Smem::VRING + s * KV_BYTES + lane * 4096, &vmap,
+                                     &bars[Smem::B_VFULL + s], 0, row, 0, pol);
+                }
+                nv_issued = q + 1;
+            }
             __syncwarp();
-            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
+            advance(cur, it);
         }
         cp_async_wait<0>();
-        if (!ok && lane == 0)
-            for (int s = 0; s < NV; ++s) {
-                const int uses = n_issued > s ? (n_issued - 1 - s) / NV + 1 : 0;
-                if (uses > 0) mbar_drain(&bars[Smem::B_VFULL + s], (uses - 1) & 1);
+        if (!ok && lane == 0) {
+            // drain: wait (bounded) for the latest copy into each slot this
+            // warp filled (a slot's earlier phases completed before it was refilled)
+            for (int q = max(0, nk_issued - 2); q < nk_issued; ++q) {
+                const int it = pw + q * Smem::NPROD;
+                const int last = pw + (nk_issued - 1) * Smem::NPROD;
+                if (q == nk_issued - 1 || it % NL != last % NL)
+                    mbar_drain(&bars[Smem::B_KVFULL + it % NL], (it / NL) & 1);
             }
+            for (int q = max(0, nv_issued - 2); q < nv_issued; ++q) {
+                const int it = pw + q * Smem::NPROD;
+                const int last = pw + (nv_issued - 1) * Smem::NPROD;
+                if (q == nv_issued - 1 || it % NV != last % NV)
+                    mbar_drain(&bars[Smem::B_VFULL + it % NV], (it / NV) & 1);
+            }
+        }
     } else if (KV8 && warp >= 8) {
         // ================= INT8 widening (warps 8-11) =================
         // Raw stage -> operand stage: K lands in the order the N = 64
@@ -1052,12 +1021,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ================= Q K^T issue (warp 4) =================
         // K arrives (bf16: as 8-key TMA boxes; INT8: widened by warps 8-11)
         // with 8-key groups 2 KB apart, one uniform stride for an N = 64 MMA.
-        // P V is issued by the softmax warps.
+        // P V is issued by the softmax warps.  This warp also loads Q: a
+        // piece's Q goes to the staging buffer as soon as the previous
+        // piece's Q has been copied out of it into TMEM.
         if (n_tiles > 0) {
             Cursor cur;
             cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             int pc = -1;
+            int q_issued = 0;  // pieces whose Q load has gone out
             bool ok = true;
+            auto issue_q = [&](const Cursor& c) {  // lane 0
+                mbar_arrive_expect_tx(&bars[Smem::B_QFULL], REP * 2 * R * 128);
+                for (int cp = 0; cp < REP; ++cp)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sm + Smem::Q + h * Q_HALF + cp * RQ * 128, &qmap,
+                                    &bars[Smem::B_QFULL], h * 64, c.kvh * G, c.b * k);
+            };
+            if (lane == 0) {
+                prefetch_tmap(&qmap);
+                issue_q(cur);
+            }
+            q_issued = 1;
             constexpr uint32_t kIdescQK = idesc_qk<KV8>();
             // smem descriptors are built once; an operand's start address
             // lives in the low 14 bits (in 16-byte units), so stepping to
@@ -1069,13 +1053,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 if (first) ++pc;
                 const int s = it % NM, sq = it % NSB;
                 {
+                    if (first && q_issued == pc) {
+                        // the previous piece had a single tile: its copy to
+                        // TMEM was not yet seen done when its MMAs went out
+                        if (lane == 0) {
+                            ok = mbar_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag,
+                                           a.dev_err);
+                            if (ok) issue_q(cur);
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        q_issued = pc + 1;
+                        if (!ok) break;
+                    }
                     if (first) {
                         ok = warp_wait(&bars[Smem::B_QFULL], pc & 1, abort_flag, a.dev_err);
                         if (ok && pc >= 1) {
                             // the previous piece's MMAs still read TMEM Q: wait
                             // for them before overwriting it
-                            if (lane == 0) umma_commit(&bars[Smem::B_QCP]);
                             __syncwarp();
+                            umma_commit_w(&bars[Smem::B_QCP]);
                             ok = warp_wait(&bars[Smem::B_QCP], (pc - 1) & 1, abort_flag, a.dev_err);
                         }
                     }
@@ -1098,40 +1094,58 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     if (!ok) break;
                     __syncwarp();
                     tc_fence_after();
-                    if (lane == 0) {
-                        if (first) {
-                            // the piece's Q: smem (TMA, 128-byte swizzle) ->
-                            // TMEM; k-slice kk = half kk/4, 32-byte step kk%4
+                    // issued by the whole warp, one elected lane (operands are
+                    // warp-uniform)
+                    if (first) {
+                        // the piece's Q: smem (TMA, 128-byte swizzle) -> TMEM;
+                        // k-slice kk = half kk/4, 32-byte step kk%4
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                tmem_cp_128x256b(tmem + TM_Q + kk * 8,
-                                                 qdesc0 + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
-                            // the staging buffer may take the next piece's Q
-                            // once the copies are done
-                            umma_commit(&bars[Smem::B_QFREE]);
-                        }
+                        for (int kk = 0; kk < 8; ++kk)
+                            tmem_cp_128x256b_w(tmem + TM_Q + kk * 8,
+                                               qdesc0 + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2);
+                        // the staging buffer may take the next piece's Q once
+                        // the copies are done
+                        umma_commit_w(&bars[Smem::B_QFREE]);
+                    }
+                    {
                         // S = Q K^T: K half h of 8-key group g at g*2 KB + h*1 KB
                         const uint64_t kd =
                             kdesc0 + ((uint32_t)(s * (KV8 ? STAGE_BYTES : KV_BYTES)) >> 4);
                         const uint32_t dcol = tmem + TM_S + sq * TN;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(dcol, tmem + TM_Q + kk * 8,
-                                    kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, kIdescQK,
-                                    kk ? 1u : 0u);
-                        umma_commit(&bars[Smem::B_SFULL + sq]);
+                            umma_ts_w(dcol, tmem + TM_Q + kk * 8,
+                                      kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, kIdescQK,
+                                      kk ? 1u : 0u);
+                        umma_commit_w(&bars[Smem::B_SFULL + sq]);
                         // bf16: the K slot is free as soon as Q K^T has read it
-                        if (!KV8) umma_commit(&bars[Smem::B_KVEMPTY + s]);
+                        if (!KV8) umma_commit_w(&bars[Smem::B_KVEMPTY + s]);
+                    }
+                    // the next piece's Q, once this piece's copy to TMEM is done
+                    // (not waited for: a later tile of the piece tries again)
+                    const int next_it = it + (cur.nb - cur.lt);
+                    if (q_issued == pc + 1 && next_it < n_tiles) {
+                        bool go = false;
+                        if (lane == 0 && mbar_try_wait(&bars[Smem::B_QFREE], pc & 1)) {
+                            Cursor nx = cur;
+                            nx.lt = nx.nb - 1;
+                            nx.next(s_ctx, Hkv, k);
+                            issue_q(nx);
+                            go = true;
+                        }
+                        if (__shfl_sync(0xffffffffu, go, 0)) q_issued = pc + 2;
                     }
                     __syncwarp();
                 }
                 if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
             }
+            // an abort leaves no Q copy in flight (Q loads complete in order,
+            // each issued after the previous one was waited for)
+            if (!ok && lane == 0) mbar_drain(&bars[Smem::B_QFULL], (q_issued - 1) & 1);
             // every tensor-core op of this warp must finish before TMEM is released
-            if (lane == 0) {
-                umma_commit(&bars[Smem::B_DRAIN]);
-                mbar_drain(&bars[Smem::B_DRAIN], 0);
-            }
+            __syncwarp();
+            umma_commit_w(&bars[Smem::B_DRAIN]);
+            if (lane == 0) mbar_drain(&bars[Smem::B_DRAIN], 0);
             __syncwarp();
         }
     } else if (warp < 4 || (!KV8 && warp >= 8)) {
@@ -1154,9 +1168,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // with copies the second set has no work
         const bool second = warp >= 8;
         if (REP == 4) {
-            if (!second) softmax_role<4, KV8, false>(x);
+            if (KV8) {
+                if (!second) softmax_role<4, true, false>(x);
+            } else {
+                softmax_role<4, false, true>(x);
+            }
         } else if (REP == 2) {
-            if (!second) softmax_role<2, KV8, false>(x);
+            if (KV8) {
+                if (!second) softmax_role<2, true, false>(x);
+            } else {
+                softmax_role<2, false, true>(x);
+            }
         } else if (KV8) {
             softmax_role<1, true, false>(x);
         } else {
