@@ -71,8 +71,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // INT8 cache: raw boxes (16 keys x 128 int8 = 2 KB per tensor) and their
 // fp16 scales land in NSR stages; four converter warps widen each tile into
 // one of NCV fp16 operand stages.
-constexpr int NSR = 6;
-constexpr int NCV = 2;
+constexpr int NSR = 4;
+constexpr int NCV = 3;
 constexpr int RAW8_KV = TN * D;                       // 8 KB of int8 per tensor per tile
 constexpr int RAW8_STAGE = 2 * RAW8_KV + 2 * TN * 2;  // K, V, then k / v scales (fp16)
 
@@ -159,6 +159,8 @@ struct TcParams {
     AttnArgs a;
     float* part_o;    // [2*C][ROWS][D]
     float* part_lse;  // [2*C][ROWS]
+    int4* seg_rec;    // [C][2]: per CTA boundary, the segment of its first tile
+    int* seg_pre;     // [B+1]: tiles of sequences before b (per kv-head)
 };
 
 // Row replication: RQ rows per copy (R rounded up to 32), REP copies.
@@ -808,6 +810,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int64_t t_begin = (int64_t)blockIdx.x * T / C;
     const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
     const int n_tiles = (int)(t_end - t_begin);
+    if (tid == 0) {
+        // the segment holding tile t_begin (b, kv-head, its tile index lt,
+        // its length) and T, for the combine; lt = -1: no tile there
+        int4 r0 = make_int4(0, 0, -1, 0);
+        if (t_begin < T) {
+            Cursor c0;
+            c0.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            r0 = make_int4(c0.b, c0.kvh, c0.lt, c0.nb);
+        }
+        prm.seg_rec[2 * blockIdx.x] = r0;
+        prm.seg_rec[2 * blockIdx.x + 1] = make_int4((int)(T & 0xffffffff), (int)(T >> 32), 0, 0);
+    }
+    if (blockIdx.x == 0)
+        for (int b = tid; b <= B; b += threads<KV8>()) prm.seg_pre[b] = s_pre[b];
 
     if (warp >= 5 && warp < 5 + Smem::NPROD) {
         // ================= TMA producers (warps 5 .. 4 + NPROD) =================
@@ -983,14 +999,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const uint8_t* raw = sm + Smem::RAW + s * Smem::RAW_STAGE;
             uint8_t* kc = sm + Smem::STAGES + m * STAGE_BYTES;
             uint8_t* vc = kc + KV_BYTES;
-            for (int id = ct; id < nbox * BOX_ROWS * 8; id += 128) {
+            // all of a thread's raw chunks are loaded before any is widened,
+            // so that the shared-memory loads overlap
+            constexpr int PER = TN * 8 / 128;  // 16-byte chunks per thread and tensor
+            const int nch = nbox * BOX_ROWS * 8;
+            uint4 rks[PER], rvs[PER];
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int id = ct + 128 * u;
+                if (id < nch) {
+                    rks[u] = *reinterpret_cast<const uint4*>(raw + id * 16);
+                    rvs[u] = *reinterpret_cast<const uint4*>(raw + RAW8_KV + id * 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int id = ct + 128 * u;
+                if (id >= nch) continue;
                 // 16-byte chunk c16 (head-dim 16*c16 .. +15) of key j
                 const int j = id >> 3, c16 = id & 7, h = c16 >> 2, sw = j & 7;
-                const uint4 rk = *reinterpret_cast<const uint4*>(raw + id * 16);
-                const uint4 rv = *reinterpret_cast<const uint4*>(raw + RAW8_KV + id * 16);
                 uint4 k0, k1, v0, v1;
-                i8x16_to_f16(rk, k0, k1);
-                i8x16_to_f16(rv, v0, v1);
+                i8x16_to_f16(rks[u], k0, k1);
+                i8x16_to_f16(rvs[u], v0, v1);
                 // fp16 chunks cc, cc+1 of half h; lanes of half 1 store their
                 // odd chunk first so that 8 consecutive lanes hit 8 bank groups
                 const int cc = (c16 & 3) * 2;
@@ -1193,48 +1223,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 }
 
 // Merge the partials of every segment cut by a CTA-range boundary.
-// grid (B*Hkv, ceil(R/8)), 8 warps, one query row per warp.
+// grid (B*Hkv segments or C-1 boundaries, ceil(R/8)), 8 warps, one query row
+// per warp.
+template <bool BY_SEG>
 __global__ void __launch_bounds__(256)
 combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
-                  const float* __restrict__ part_lse) {
-    __shared__ int s_red[8];
-    const int seg = blockIdx.x, kvh = seg % a.Hkv, b = seg / a.Hkv;
+                  const float* __restrict__ part_lse, const int4* __restrict__ seg_rec,
+                  const int* __restrict__ seg_pre) {
+    // BY_SEG: block x handles segment x (sequence x / Hkv, kv-head x % Hkv);
+    // else the boundary between CTAs x and x + 1 -- the segment holding CTA
+    // x+1's first tile, when that is not the segment's first tile and this
+    // is the first boundary inside it.  The launch takes the form with fewer
+    // blocks.
     const int G = a.Hq / a.Hkv, R = a.k * G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t cap = (int64_t)a.max_pages * a.P - a.k;
-    auto tiles_of = [&](int bb) {
-        int c = a.ctx_lens[bb];
-        if (c < 0 || (int64_t)c > cap) c = c < 0 ? 0 : (int)(cap < 0 ? 0 : cap);
-        return (c + a.k + TN - 1) / TN;
-    };
-    // tiles before sequence b, and in total
-    int before = 0, total = 0;
-    for (int bb = threadIdx.x; bb < a.B; bb += blockDim.x) {
-        const int n = tiles_of(bb);
-        total += n;
-        if (bb < b) before += n;
+    const int64_t C = num_ctas;
+    int b, kvh, nb;
+    int64_t T, s0;
+    if constexpr (BY_SEG) {
+        b = blockIdx.x / a.Hkv;
+        kvh = blockIdx.x % a.Hkv;
+        const int p0 = __ldg(seg_pre + b);
+        nb = __ldg(seg_pre + b + 1) - p0;
+        T = (int64_t)__ldg(seg_pre + a.B) * a.Hkv;
+        s0 = (int64_t)p0 * a.Hkv + (int64_t)kvh * nb;
+    } else {
+        const int x = blockIdx.x + 1;
+        const int4 r0 = __ldg(seg_rec + 2 * x), r1 = __ldg(seg_rec + 2 * x + 1);
+        if (r0.z <= 0) return;  // the boundary is a segment start (or past the end)
+        b = r0.x;
+        kvh = r0.y;
+        nb = r0.w;
+        T = (int64_t)(uint32_t)r1.x | ((int64_t)r1.y << 32);
+        s0 = (int64_t)x * T / C - r0.z;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        before += __shfl_xor_sync(0xffffffffu, before, o);
-        total += __shfl_xor_sync(0xffffffffu, total, o);
-    }
-    if (lane == 0) s_red[warp] = before;
-    __syncthreads();
-    int pre_b = 0;
-    for (int w = 0; w < 8; ++w) pre_b += s_red[w];
-    __syncthreads();
-    if (lane == 0) s_red[warp] = total;
-    __syncthreads();
-    int tot = 0;
-    for (int w = 0; w < 8; ++w) tot += s_red[w];
-
-    const int64_t T = (int64_t)tot * a.Hkv, C = num_ctas;
-    const int nb = tiles_of(b);
-    const int64_t s0 = (int64_t)pre_b * a.Hkv + (int64_t)kvh * nb, s1 = s0 + nb;
+    const int64_t s1 = s0 + nb;
     auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
     const int c_first = cta_of(s0), c_last = cta_of(s1 - 1);
-    if (c_first == c_last) return;  // written directly by its CTA
+    if (BY_SEG ? c_first == c_last : c_first + 1 != (int)blockIdx.x + 1)
+        return;  // written directly by its CTA / handled at an earlier boundary
     const int row = blockIdx.y * 8 + warp;
     if (row >= R) return;
 
@@ -1242,41 +1269,84 @@ combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
     // nothing and is skipped
     auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
     auto slot_of = [&](int c) { return 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1); };
-    // log-sum-exp of the pieces' lse: one piece per lane, all loads in flight
-    float m = -INFINITY;
-    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
-        const int c = c0 + lane;
-        const bool use = c <= c_last && !empty(c);
-        const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
-        m = fmaxf(m, lw);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float tsum = 0.f;
-    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
-        const int c = c0 + lane;
-        const bool use = c <= c_last && !empty(c);
-        const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
-        if (lw != -INFINITY) tsum += expf(lw - m);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
-    const float lse_tot = m + logf(tsum);
-    // weighted O rows: lane -> 4 columns; the loads of consecutive pieces are
-    // independent, so the unrolled loop keeps several in flight
+    constexpr uint32_t kAll = 0xffffffffu;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int c = c_first; c <= c_last; ++c) {
-        const bool use = !empty(c);
-        const int slot = slot_of(c);
-        const float lw = use ? __ldg(part_lse + (int64_t)slot * ROWS + row) : -INFINITY;
-        const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)slot * ROWS + row) * D);
-        const float4 v = use ? __ldg(src + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float w = lw == -INFINITY ? 0.f : expf(lw - lse_tot);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    float lse_tot;
+    auto add = [&](float w, float4 v) {
+        // a piece of weight 0 (an empty CTA range) wrote nothing: its value is
+        // dropped, not multiplied
+        if (w > 0.f) {
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+    };
+    const int npc = c_last - c_first + 1;
+    if (npc <= 32) {
+        // one piece per lane: its lse and the first 8 pieces' O rows (lane ->
+        // 4 columns) are loaded together, before any of them is needed
+        const int c = c_first + lane;
+        const bool use = lane < npc && !empty(c);
+        const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
+        const int64_t off = use ? ((int64_t)slot_of(c) * ROWS + row) * D : 0;
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t oj = __shfl_sync(kAll, off, j);
+            v[j] = j < npc ? __ldg(reinterpret_cast<const float4*>(part_o + oj) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float m = lw;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kAll, m, o));
+        float t = lw == -INFINITY ? 0.f : expf(lw - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kAll, t, o);
+        lse_tot = m + logf(t);
+        const float wl = lw == -INFINITY ? 0.f : expf(lw - lse_tot);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) add(__shfl_sync(kAll, wl, j), v[j]);
+#pragma unroll 8
+        for (int j = 8; j < npc; ++j) {
+            const float w = __shfl_sync(kAll, wl, j);
+            const int64_t oj = __shfl_sync(kAll, off, j);
+            add(w, __ldg(reinterpret_cast<const float4*>(part_o + oj) + lane));
+        }
+    } else {
+        // more pieces than lanes: lse max, sum, then the weighted rows
+        float m = -INFINITY;
+        for (int c0 = c_first; c0 <= c_last; c0 += 32) {
+            const int c = c0 + lane;
+            const bool use = c <= c_last && !empty(c);
+            m = fmaxf(m, use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kAll, m, o));
+        float tsum = 0.f;
+        for (int c0 = c_first; c0 <= c_last; c0 += 32) {
+            const int c = c0 + lane;
+            const bool use = c <= c_last && !empty(c);
+            const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
+            if (lw != -INFINITY) tsum += expf(lw - m);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(kAll, tsum, o);
+        lse_tot = m + logf(tsum);
+        for (int c0 = c_first; c0 <= c_last; c0 += 32) {
+            const int c = c0 + lane;
+            const bool use = c <= c_last && !empty(c);
+            const float lw = use ? __ldg(part_lse + (int64_t)slot_of(c) * ROWS + row) : -INFINITY;
+            const float wl = lw == -INFINITY ? 0.f : expf(lw - lse_tot);
+            const int64_t off = use ? ((int64_t)slot_of(c) * ROWS + row) * D : 0;
+            const int n = min(32, c_last - c0 + 1);
+#pragma unroll 8
+            for (int j = 0; j < n; ++j) {
+                const float w = __shfl_sync(kAll, wl, j);
+                const int64_t oj = __shfl_sync(kAll, off, j);
+                add(w, __ldg(reinterpret_cast<const float4*>(part_o + oj) + lane));
+            }
+        }
     }
     const int i = row / G, h = kvh * G + row % G;
     const int64_t orow = ((int64_t)b * a.k + i) * a.Hq + h;
@@ -1325,7 +1395,8 @@ bool tc_supported(const AttnArgs& a) {
 }
 
 size_t tc_workspace_bytes(const AttnArgs&, int num_ctas) {
-    return (size_t)2 * num_ctas * ROWS * (D + 1) * sizeof(float) + 256;
+    return (size_t)2 * num_ctas * ROWS * (D + 1) * sizeof(float) + (size_t)num_ctas * 32 +
+           (size_t)(MAX_BATCH + 1) * 4 + 256;
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream) {
@@ -1379,6 +1450,8 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
     prm.a = a;
     prm.part_o = static_cast<float*>(workspace);
     prm.part_lse = prm.part_o + (size_t)2 * num_ctas * ROWS * D;
+    prm.seg_rec = reinterpret_cast<int4*>(prm.part_lse + (size_t)2 * num_ctas * ROWS);
+    prm.seg_pre = reinterpret_cast<int*>(prm.seg_rec + 2 * (size_t)num_ctas);
     cudaError_t e;
     if (kv8) {
         e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1396,14 +1469,25 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, stream);
+    return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, prm.seg_rec,
+                                   prm.seg_pre, stream);
 }
 
 cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float* part_o,
-                                    const float* part_lse, cudaStream_t stream) {
+                                    const float* part_lse, const int4* seg_rec,
+                                    const int* seg_pre, cudaStream_t stream) {
+    if (num_ctas < 2) return cudaSuccess;  // one CTA splits nothing
     const int R = a.k * (a.Hq / a.Hkv);
-    dim3 cgrid(a.B * a.Hkv, (R + 7) / 8);
-    combine_tc_kernel<<<cgrid, 256, 0, stream>>>(a, num_ctas, part_o, part_lse);
+    const int64_t segs = (int64_t)a.B * a.Hkv;
+    if (segs <= num_ctas - 1) {
+        dim3 cgrid((unsigned)segs, (R + 7) / 8);
+        combine_tc_kernel<true>
+            <<<cgrid, 256, 0, stream>>>(a, num_ctas, part_o, part_lse, seg_rec, seg_pre);
+    } else {
+        dim3 cgrid(num_ctas - 1, (R + 7) / 8);
+        combine_tc_kernel<false>
+            <<<cgrid, 256, 0, stream>>>(a, num_ctas, part_o, part_lse, seg_rec, seg_pre);
+    }
     return cudaGetLastError();
 }
 

@@ -57,10 +57,13 @@ bool tc_supported(const AttnArgs& a);
 size_t tc_workspace_bytes(const AttnArgs& a, int num_ctas);
 cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream);
 
-// Merge of the split-KV partials written by either stream-K kernel (64-key
-// tiles over `num_ctas` persistent CTAs; partial slots [2*C][128][D]).
+// Merge of the split-KV partials written by the tensor-core kernel (64-key
+// tiles over `num_ctas` persistent CTAs; partial slots [2*C][128][D]; per CTA
+// boundary the segment record {b, kv-head, tile-in-segment, tiles} and T;
+// per sequence the tile prefix).
 cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float* part_o,
-                                    const float* part_lse, cudaStream_t stream);
+                                    const float* part_lse, const int4* seg_rec,
+                                    const int* seg_pre, cudaStream_t stream);
 
 // ---- warp-MMA kernel for k*G <= 16 query rows (mma.sync m16n8k16, TMA pages) ----
 bool mma_supported(const AttnArgs& a);
