@@ -60,13 +60,19 @@ def test_tensor_core_small(oracle_mod, kw):
     check_attn_full(oracle_mod, inp, str(kw))
 
 
+# query rows per kv-head 24 (four copies), 48 (two copies), 84 (one copy):
+# each with both softmax sets, the merge of their states and of the copies,
+# and the combine in its by-boundary (few CTAs) and by-segment forms
+@pytest.mark.parametrize("heads", [(16, 4, 6), (16, 2, 6), (28, 4, 12)],
+                         ids=["24rows", "48rows", "84rows"])
 @pytest.mark.parametrize("ctas", [1, 2, 5, 37, 152, 400])
-def test_tensor_core_stream_k_splits(oracle_mod, ctas):
-    inp = make_inputs(small_spec(batch=4, num_q_heads=16, num_kv_heads=4, num_draft=6,
+def test_tensor_core_stream_k_splits(oracle_mod, ctas, heads):
+    hq, hkv, k = heads
+    inp = make_inputs(small_spec(batch=4, num_q_heads=hq, num_kv_heads=hkv, num_draft=k,
                                  ctx=(0, 900)), seed=22)
     binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
     binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
-    check_attn_full(oracle_mod, inp, "ctas=%d" % ctas)
+    check_attn_full(oracle_mod, inp, "ctas=%d heads=%s" % (ctas, heads))
 
 
 SMALL_I8 = [
