@@ -21,6 +21,9 @@ computes and which passage of the pages it follows:
 * ``accept_rejection`` -- lossless rejection-sampling acceptance (same blog,
   "How does this drafter maintain the same distribution of the target?"),
   with its draws from the counter-based generator SplitMix64.
+* ``codec_encode`` / ``codec_decode`` -- the delta + run-length coding of a
+  page's INT8 codes (CXL-SpecKV, observation (5) and "Algorithm 2 KV-Cache
+  Compression"), in the byte format the C source defines.
 
 Arrays are numpy; 16-bit float types travel as their raw ``uint16`` bits.
 """
@@ -75,6 +78,10 @@ def _load():
         lib.oracle_verify_attn_tree.restype = i32
         lib.oracle_accept_tree.argtypes = [P, i32, P, P, i32, i32, ctypes.c_int64, P, P, P]
         lib.oracle_accept_tree.restype = i32
+        lib.oracle_codec_encode.argtypes = [P, ctypes.c_int64, i32, i32, P, P]
+        lib.oracle_codec_encode.restype = i32
+        lib.oracle_codec_decode.argtypes = [P, P, ctypes.c_int64, i32, i32, P]
+        lib.oracle_codec_decode.restype = i32
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -278,3 +285,25 @@ __all__ = ["verify_attn", "attn_rows", "verify_attn_tree", "accept_tree", "accep
            "accept_rejection", "quantize_rows",
            "kv_append", "commit", "splitmix64",
            "accept_uniform", "gumbel", "bf16_bits_to_f64", "f16_bits_to_f64", "DTYPES"]
+
+
+def codec_encode(codes):
+    """codes int8 [nblk, P, D] -> (pairs uint8 [nblk, 2*P*D], npairs int32 [nblk])."""
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    nblk, P, D = codes.shape
+    pairs = np.zeros((nblk, 2 * P * D), np.uint8)
+    npairs = np.zeros(nblk, np.int32)
+    if _load().oracle_codec_encode(_ptr(codes), nblk, P, D, _ptr(pairs), _ptr(npairs)) != 0:
+        raise MemoryError("oracle_codec_encode")
+    return pairs, npairs
+
+
+def codec_decode(pairs, npairs, P, D):
+    """Inverse of codec_encode; ValueError on a malformed block."""
+    pairs = np.ascontiguousarray(pairs, dtype=np.uint8)
+    npairs = np.ascontiguousarray(npairs, dtype=np.int32)
+    nblk = npairs.shape[0]
+    codes = np.zeros((nblk, P, D), np.int8)
+    if _load().oracle_codec_decode(_ptr(pairs), _ptr(npairs), nblk, P, D, _ptr(codes)) != 0:
+        raise ValueError("malformed codec block")
+    return codes
