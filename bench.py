@@ -389,6 +389,67 @@ def run_gpu(args, inp, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_codec(args, inp):
+    """The delta + run-length page codec on the workload's INT8 cache: every
+    (page, kv-head) block of K and V encoded and decoded, each timed with CUDA
+    events over --steps launches; the round trip is checked first.  Reports
+    the decode rate (INT8 bytes produced per second) with the decode's bytes
+    moved against the HBM roofline, the encode rate, and the coded size
+    relative to the INT8 pages -- the bytes a decode-in-load attention would
+    read instead of the INT8 pages."""
+    import torch
+    from speculative_decoding_verification_attn_gb300 import binding
+    s = inp.spec
+    if s.kv_dtype != "i8":
+        raise SystemExit("--codec needs an INT8-cache workload (e.g. int8kv_70b_layer)")
+    binding.load()
+    P, D = s.page_size, s.head_dim
+    codes = torch.cat([torch.from_numpy(np.ascontiguousarray(c).reshape(-1, P, D))
+                       for c in (inp.k_cache, inp.v_cache)]).cuda()
+    nblk, n = codes.shape[0], P * D
+    pairs = torch.empty((nblk, 2 * n), dtype=torch.uint8, device="cuda")
+    npairs = torch.empty(nblk, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(codes)
+    binding.spec_codec_encode(codes, pairs, npairs)
+    binding.spec_codec_decode(pairs, npairs, out)
+    torch.cuda.synchronize()
+    if not torch.equal(out, codes) or binding.spec_device_error() != 0:
+        raise SystemExit("codec round trip failed")
+    coded = int(npairs.sum().item()) * 2 + 4 * nblk
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps / 1e3
+
+    enc_s = timed(lambda: binding.spec_codec_encode(codes, pairs, npairs))
+    dec_s = timed(lambda: binding.spec_codec_decode(pairs, npairs, out))
+    peak, peak_kind = measured_peaks()
+    moved = coded + nblk * n
+    line = {"metric": "INT8 page decode rate", "value": nblk * n / dec_s / 1e9, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "u8", "data": "synthetic (the workload generator's INT8 cache)",
+            "config": {"workload": s.name + " K and V caches", "blocks": nblk, "page_size": P,
+                       "head_dim": D, "int8_bytes": nblk * n,
+                       "l2": "coded pages %d MB, decoded %d MB per launch" % (coded >> 20,
+                                                                             (nblk * n) >> 20)},
+            "coded_over_int8": coded / (nblk * n),
+            "encode_ms": enc_s * 1e3, "decode_ms": dec_s * 1e3,
+            "encode_GBps": nblk * n / enc_s / 1e9,
+            "roofline": {"bound": "hbm", "achieved": moved / dec_s / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac": moved / dec_s / 1e9 / peak,
+                         "traffic": None, "kernel": "codec_decode_kernel",
+                         "peak_source": peak_kind}}
+    print(json.dumps(line), flush=True)
+
+
 def launches_per_step(inp) -> int:
     """Kernels one step launches: the warp-MMA attention kernel (bf16, head_dim
     128, <= 16 query rows per kv-head, page size 16..256) merges its split-KV
@@ -414,6 +475,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--accept", choices=["greedy", "rejection"], default="greedy",
                     help="acceptance rule of the step (greedy: the headline configuration)")
+    ap.add_argument("--codec", action="store_true",
+                    help="time the delta + run-length page codec on the workload's INT8 cache "
+                         "instead of the step")
     args = ap.parse_args(argv)
 
     world, rank, local = dist_env()
@@ -427,6 +491,10 @@ def main(argv=None):
     import __graft_entry__
     __graft_entry__.build()
     inp = make_inputs(args.workload, args.seed, canary=False)
+    if args.codec:
+        if rank == 0:
+            run_codec(args, inp)
+        return
     run_gpu(args, inp, world, rank, local)
     if world > 1:
         import torch.distributed as dist

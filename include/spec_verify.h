@@ -201,6 +201,34 @@ SPEC_API int spec_accept_tree(const void *logits, int32_t logits_dtype,
                               int32_t *next_token, int32_t *path, void *stream);
 
 /*
+ * Delta + run-length coding of INT8 KV pages (CXL-SpecKV: key observation
+ * (5), delta coding delta_i = x_i - x_(i-1) of neighbouring elements of a
+ * head vector, and "Algorithm 2 KV-Cache Compression", whose output is
+ * (s, D_RLE(c))).  Lossless; the fp16 scales are not coded.
+ *
+ *   codes      [num_blocks, page_size, head_dim] int8: one block per
+ *              (page, kv-head), i.e. an INT8 cache [num_pages, Hkv, P, D]
+ *              with num_blocks = num_pages * Hkv
+ *   pairs      [num_blocks, 2 * page_size * head_dim] uint8: block i's
+ *              (length, value) byte pairs from byte 2*P*D*i (room for the
+ *              worst case, every run of length one); 16-byte aligned
+ *   num_pairs  [num_blocks] int32: pairs of each block
+ *
+ * Format: in each row of a block, e[0] = c[0] and e[d] = c[d] - c[d-1]
+ * modulo 256; the block's row-major stream e becomes maximal runs of equal
+ * bytes, each the pair (length 1..255, value), a longer run continuing in the
+ * next pair.  Encode writes pairs and num_pairs; decode writes codes.  A
+ * malformed block (pair count outside [0, P*D], a zero length, lengths not
+ * summing to P*D) decodes as zeros and sets SPEC_DEVERR_CODEC.
+ * Limits: head_dim a multiple of 32 in [32, 256]; 1 <= page_size and
+ * page_size * head_dim <= 16384; num_blocks >= 0.
+ */
+SPEC_API int spec_codec_encode(const void *codes, int64_t num_blocks, int32_t page_size,
+                               int32_t head_dim, void *pairs, int32_t *num_pairs, void *stream);
+SPEC_API int spec_codec_decode(const void *pairs, const int32_t *num_pairs, int64_t num_blocks,
+                               int32_t page_size, int32_t head_dim, void *codes, void *stream);
+
+/*
  * Greedy acceptance that allocates nothing.  (The pages have no counterpart:
  * this is an interface convenience of this library.)
  *
@@ -314,7 +342,8 @@ enum {
     SPEC_DEVERR_CTX = 2,     /* ctx_b + k beyond the block table (clamped) */
     SPEC_DEVERR_TIMEOUT = 4, /* a bounded on-chip wait gave up; results invalid */
     SPEC_DEVERR_TOKEN = 8,   /* a draft token outside [0, vocab) (treated as rejected) */
-    SPEC_DEVERR_TREE = 16    /* a tree parent outside [-1, i) (the node is never taken) */
+    SPEC_DEVERR_TREE = 16,   /* a tree parent outside [-1, i) (the node is never taken) */
+    SPEC_DEVERR_CODEC = 32   /* a malformed coded block (decoded as zeros) */
 };
 
 /* Free the current device's workspace (synchronises the device). */

@@ -22,12 +22,13 @@ SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_OPT_ATTN_PATH, SPEC_OPT_NUM_CTAS, SPEC_OPT_VALIDATE, SPEC_OPT_SIMT_CHUNK = 0, 1, 2, 3
 SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT, SPEC_DEVERR_TOKEN = 1, 2, 4, 8
 SPEC_DEVERR_TREE = 16
+SPEC_DEVERR_CODEC = 32
 
 # every symbol the public header declares
 EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
             "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_accept_rejection",
             "spec_kv_append", "spec_commit", "spec_verify_attn_tree", "spec_accept_tree",
-            "spec_device_error", "spec_release"]
+            "spec_codec_encode", "spec_codec_decode", "spec_device_error", "spec_release"]
 SPEC_NOALLOC_MAX_PARTIALS, SPEC_NOALLOC_MAX_BATCH = 65536, 4096
 
 _TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
@@ -74,6 +75,10 @@ def _open(path: str):
     lib.spec_kv_append.restype = ctypes.c_int
     lib.spec_commit.argtypes = [P, P, i32, i32, P]
     lib.spec_commit.restype = ctypes.c_int
+    lib.spec_codec_encode.argtypes = [P, ctypes.c_int64, i32, i32, P, P, P]
+    lib.spec_codec_encode.restype = ctypes.c_int
+    lib.spec_codec_decode.argtypes = [P, P, ctypes.c_int64, i32, i32, P, P]
+    lib.spec_codec_decode.restype = ctypes.c_int
     lib.spec_verify_attn_tree.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                           i32, i32, i32, ctypes.c_float, P, P, P]
     lib.spec_verify_attn_tree.restype = ctypes.c_int
@@ -227,6 +232,20 @@ def spec_kv_append(k_new, v_new, k_cache, v_cache, block_table, ctx_lens, k_scal
                                  _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                  _TORCH_DT[k_cache.dtype], _ptr(block_table), _ptr(ctx_lens), B,
                                  n, Hkv, D, P, NP, block_table.shape[1], _stream(stream)))
+
+
+def spec_codec_encode(codes, pairs, num_pairs, stream=None) -> None:
+    """codes int8 [num_blocks, P, D] -> pairs uint8 [num_blocks, 2*P*D], num_pairs int32."""
+    nblk, P, D = codes.shape
+    _check(load().spec_codec_encode(_ptr(codes), nblk, P, D, _ptr(pairs), _ptr(num_pairs),
+                                    _stream(stream)))
+
+
+def spec_codec_decode(pairs, num_pairs, codes, stream=None) -> None:
+    """pairs uint8 [num_blocks, 2*P*D], num_pairs int32 -> codes int8 [num_blocks, P, D]."""
+    nblk, P, D = codes.shape
+    _check(load().spec_codec_decode(_ptr(pairs), _ptr(num_pairs), nblk, P, D, _ptr(codes),
+                                    _stream(stream)))
 
 
 def spec_commit(ctx_lens, accepted_len, extra: int = 1, stream=None) -> None:

@@ -104,6 +104,13 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, int32_t src_d
                              int32_t cache_dtype, const int32_t* block_table,
                              const int32_t* ctx_lens, int B, int n, int Hkv, int D, int P,
                              int num_pages, int max_pages, int* dev_err, cudaStream_t stream);
+// ---- delta + run-length page codec (codec.cu) ----
+size_t codec_decode_smem(int P, int D);
+cudaError_t launch_codec_encode(const void* codes, int64_t nblk, int P, int D, void* pairs,
+                                int32_t* npairs, cudaStream_t stream);
+cudaError_t launch_codec_decode(const void* pairs, const int32_t* npairs, int64_t nblk, int P,
+                                int D, void* codes, int* dev_err, cudaStream_t stream);
+
 cudaError_t launch_commit(int32_t* ctx_lens, const int32_t* accepted_len, int B, int extra,
                           cudaStream_t stream);
 

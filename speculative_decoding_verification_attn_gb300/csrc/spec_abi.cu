@@ -412,6 +412,48 @@ int spec_kv_append(const void* k_new, const void* v_new, int32_t src_dtype, void
     return SPEC_OK;
 }
 
+static int codec_args(int64_t num_blocks, int32_t page_size, int32_t head_dim) {
+    if (num_blocks < 0) return fail(SPEC_ERR_INVALID, "num_blocks < 0");
+    if (head_dim < 32 || head_dim > 256 || head_dim % 32)
+        return fail(SPEC_ERR_INVALID, "head_dim must be a multiple of 32 in [32, 256]");
+    if (page_size < 1 || (int64_t)page_size * head_dim > 16384)
+        return fail(SPEC_ERR_INVALID, "page_size must be >= 1 with page_size * head_dim <= 16384");
+    if (num_blocks / 8 >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "too many blocks");
+    return SPEC_OK;
+}
+
+int spec_codec_encode(const void* codes, int64_t num_blocks, int32_t page_size, int32_t head_dim,
+                      void* pairs, int32_t* num_pairs, void* stream) {
+    g_err.clear();
+    int rc = codec_args(num_blocks, page_size, head_dim);
+    if (rc) return rc;
+    if (num_blocks == 0) return SPEC_OK;
+    if (!codes || !pairs || !num_pairs) return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    cudaError_t e = specv::launch_codec_encode(codes, num_blocks, page_size, head_dim, pairs,
+                                               num_pairs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "codec_encode launch");
+    return SPEC_OK;
+}
+
+int spec_codec_decode(const void* pairs, const int32_t* num_pairs, int64_t num_blocks,
+                      int32_t page_size, int32_t head_dim, void* codes, void* stream) {
+    g_err.clear();
+    int rc = codec_args(num_blocks, page_size, head_dim);
+    if (rc) return rc;
+    if (num_blocks == 0) return SPEC_OK;
+    if (!codes || !pairs || !num_pairs) return fail(SPEC_ERR_INVALID, "null tensor pointer");
+    if ((reinterpret_cast<uintptr_t>(pairs) & 15) || (reinterpret_cast<uintptr_t>(codes) & 15))
+        return fail(SPEC_ERR_INVALID, "pairs and codes must be 16-byte aligned");
+    Workspace* ws = nullptr;
+    rc = get_workspace(0, &ws);
+    if (rc) return rc;
+    cudaError_t e = specv::launch_codec_decode(pairs, num_pairs, num_blocks, page_size, head_dim,
+                                               codes, static_cast<int*>(ws->base),
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "codec_decode launch");
+    return SPEC_OK;
+}
+
 int spec_commit(int32_t* ctx_lens, const int32_t* accepted_len, int32_t batch, int32_t extra,
                 void* stream) {
     g_err.clear();

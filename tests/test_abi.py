@@ -137,6 +137,33 @@ def test_kv_append_rejects_bad_arguments(lib, bad, needle):
     assert needle in lib.spec_last_error().decode()
 
 
+@pytest.mark.parametrize("bad,needle", [
+    (dict(nblk=-1), "num_blocks"),
+    (dict(D=48), "head_dim"),
+    (dict(D=288), "head_dim"),
+    (dict(P=0), "page_size"),
+    (dict(P=129), "page_size"),
+    (dict(codes=0), "null"),
+    (dict(np_=0), "null"),
+])
+def test_codec_rejects_bad_arguments(lib, bad, needle):
+    a = dict(codes=64, pairs=64, np_=64, nblk=4, P=16, D=128)
+    a.update(bad)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    for rc in (lib.spec_codec_encode(vp(a["codes"]), a["nblk"], a["P"], a["D"], vp(a["pairs"]),
+                                     vp(a["np_"]), None),
+               lib.spec_codec_decode(vp(a["pairs"]), vp(a["np_"]), a["nblk"], a["P"], a["D"],
+                                     vp(a["codes"]), None)):
+        assert rc == -1
+        assert needle in lib.spec_last_error().decode()
+
+
+def test_codec_decode_rejects_unaligned(lib):
+    rc = lib.spec_codec_decode(ctypes.c_void_p(66), ctypes.c_void_p(64), 4, 16, 128,
+                               ctypes.c_void_p(64), None)
+    assert rc == -1 and "aligned" in lib.spec_last_error().decode()
+
+
 def test_options(lib):
     assert lib.spec_set_option(0, 4) == -1
     assert lib.spec_set_option(0, 3) == 0
