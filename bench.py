@@ -80,11 +80,17 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# sources whose change makes the committed attention / acceptance counters stale:
+# the kernels of the step and the device helpers they include (the ABI's other
+# entry points and their kernels do not run in the step)
+STEP_SOURCES = ("attn_tc.cu", "attn_mma.cu", "attn_simt.cu", "accept.cu", "common.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_attn_gb300",
-                                           "csrc", "*"))):
-        with open(f, "rb") as fh:
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_attn_gb300", "csrc")
+    for name in STEP_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
