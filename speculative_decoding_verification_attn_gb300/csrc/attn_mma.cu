@@ -389,17 +389,24 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     fence_proxy_async_smem();  // before the next TMA write of this stage
                     __syncwarp();
                 }
-                // S = Q K^T over this warp's 16 keys: n-tile 0 = keys 0-7, 1 = keys 8-15
+                // S = Q K^T over this warp's 16 keys: n-tile 0 = keys 0-7, 1 = keys 8-15;
+                // even and odd k-steps accumulate separately (four dependent
+                // MMA chains of four instead of two of eight), summed after
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     uint32_t b00, b01, b10, b11;
                     const int key = (lane & 7) + (lane >> 4) * 8;
                     const int chunk = kk * 2 + ((lane >> 3) & 1);
                     ldsm_x4(kb + sw_off(key, chunk, BOX_BYTES / 2), b00, b01, b10, b11);
-                    mma16816(sc[0], qf[kk], b00, b01);
-                    mma16816(sc[1], qf[kk], b10, b11);
+                    mma16816((kk & 1) ? sd[0] : sc[0], qf[kk], b00, b01);
+                    mma16816((kk & 1) ? sd[1] : sc[1], qf[kk], b10, b11);
                 }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
                 // masked scores (log2 units); -inf where the key is invisible
                 float v[2][4];
                 float mt[2] = {-INFINITY, -INFINITY};
