@@ -17,9 +17,10 @@
 // pair start writes its value and the previous pair's length (its distance
 // from the previous start), the last length is written after the block.
 //
-// Decode: one warp per block.  32 pairs per step: the lengths' exclusive
-// warp scan gives each run's offset, and each lane writes its run into the
-// block's staging buffer in shared memory; then each row's deltas are summed
+// Decode: one warp per block.  128 pairs per step, four per lane (one
+// 8-byte load): the exclusive warp scan of the lanes' length sums gives each
+// run's offset, and each lane writes its runs into the block's staging
+// buffer in shared memory; then each row's deltas are summed
 // modulo 256 (a warp scan over D/32-byte lane slices) and the codes stored
 // with coalesced 4-byte writes.  A malformed block (pair count outside
 // [0, P*D], a zero length, lengths not summing to P*D) is written as zeros and
@@ -103,25 +104,45 @@ codec_decode_kernel(const uint8_t* __restrict__ pairs, const int32_t* __restrict
     const int np = __ldg(npairs + blk);
     bool bad = np < 0 || np > n;
     int pos = 0;  // bytes expanded so far
-    for (int j0 = 0; j0 < (bad ? 0 : np); j0 += 32) {
-        const int j = j0 + lane;
-        uint32_t len = 0, val = 0;
-        if (j < np) {
-            const uint16_t pr = *reinterpret_cast<const uint16_t*>(in + 2 * j);
-            len = pr & 255u;
-            val = pr >> 8;
+    // four pairs per lane and step (one 8-byte load), 128 pairs per step
+    for (int j0 = 0; j0 < (bad ? 0 : np); j0 += 128) {
+        const int j = j0 + lane * 4;
+        uint32_t len[4] = {0, 0, 0, 0}, val[4] = {0, 0, 0, 0};
+        if (j + 4 <= np) {
+            const uint2 w = *reinterpret_cast<const uint2*>(in + 2 * j);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t pr = (q < 2 ? w.x : w.y) >> (16 * (q & 1));
+                len[q] = pr & 255u;
+                val[q] = (pr >> 8) & 255u;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j + q < np) {
+                    len[q] = in[2 * (j + q)];
+                    val[q] = in[2 * (j + q) + 1];
+                }
         }
-        if (__any_sync(0xffffffffu, j < np && len == 0)) bad = true;
-        // exclusive scan of the lengths: this run's offset in the block
-        int incl = (int)len;
+        bool zero = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) zero |= j + q < np && len[q] == 0;
+        if (__any_sync(0xffffffffu, zero)) bad = true;
+        const int tot = (int)(len[0] + len[1] + len[2] + len[3]);
+        // exclusive scan of the lanes' totals: this lane's first run offset
+        int incl = tot;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += v;
         }
-        const int start = pos + incl - (int)len;
-        for (int t = 0; t < (int)len; ++t)
-            if (start + t < n) stage[start + t] = (uint8_t)val;
+        int start = pos + incl - tot;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            for (int t = 0; t < (int)len[q]; ++t)
+                if (start + t < n) stage[start + t] = (uint8_t)val[q];
+            start += (int)len[q];
+        }
         pos += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (pos != n) bad = true;
