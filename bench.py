@@ -200,7 +200,8 @@ def run_reference(args, inp, world, rank):
         return
     s = inp.spec
     units = s.batch * s.num_draft
-    per_step_budget = 1.0
+    # about two minutes of oracle time for the whole run, at most 1 s a step
+    per_step_budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_step_estimate(inp, per_step_budget, seed=1000)
     times, desc = [], ""
