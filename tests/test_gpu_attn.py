@@ -50,6 +50,7 @@ SMALL_BF16 = [
     dict(page_size=256, ctx=(250, 700), batch=2),
     dict(batch=1, num_q_heads=8, num_kv_heads=1, ctx=[3000]),              # one long segment
     dict(num_q_heads=7, num_kv_heads=7, num_draft=5, ctx=(0, 130)),
+    dict(batch=1024, num_q_heads=4, num_kv_heads=2, num_draft=2, ctx=(0, 40)),  # most sequences
 ]
 
 
@@ -264,3 +265,19 @@ def test_warp_mma_matches_tcgen05():
     b_out, b_lse = gpu_attn(inp, t)
     assert np.abs(a_out - b_out).max() < 2e-2
     assert np.abs(a_lse - b_lse).max() < 2e-3
+
+
+def test_batch_beyond_tensor_core_limit(oracle_mod):
+    # 1025 sequences: the tcgen05 kernel refuses a forced call; the automatic
+    # choice still runs (another kernel) and matches the oracle
+    inp = make_inputs(small_spec(batch=1025, num_q_heads=4, num_kv_heads=1, num_draft=8,
+                                 ctx=(0, 20)), seed=23)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    t = binding.inputs_to_torch(inp)
+    o = binding.alloc_outputs(inp)
+    with pytest.raises(binding.SpecError):
+        binding.run_verify(t, o, inp.spec.num_draft, inp.scale)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 0)
+    out, lse = gpu_attn(inp, t)
+    ref_out, ref_lse = oracle_attn(oracle_mod, inp)
+    assert_attn_close(out, lse, ref_out, ref_lse, tol_for(inp), "batch 1025")
