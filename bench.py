@@ -87,11 +87,15 @@ STEP_SOURCES = ("attn_tc.cu", "attn_mma.cu", "attn_simt.cu", "accept.cu", "commo
 
 
 def kernel_source_hash() -> str:
+    """Hash of the step's kernel sources with comments and blank lines removed
+    (a comment edit does not change the kernels the counters describe)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_attn_gb300", "csrc")
     for name in STEP_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, name)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

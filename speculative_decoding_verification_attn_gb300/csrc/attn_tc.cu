@@ -1,5 +1,5 @@
 // Verification attention on the 5th-generation tensor cores (tcgen05 + TMEM),
-// bf16 queries over a bf16 paged KV cache, head_dim 128.
+// bf16 queries over a bf16 or INT8 paged KV cache, head_dim 128.
 //
 // What it computes: multi-query causal attention of each sequence's k draft
 // queries over its paged cache ("Decoding Speculative Decoding from First
@@ -23,10 +23,10 @@
 //    segment cut by a range boundary leaves (O/l, lse) partials that the
 //    combine kernel merges with log-sum-exp weights (split-KV).
 //  * Warp roles: 0-3 softmax / rescale / epilogue / P V issue (one (copy,
-//    query row) per thread), 4 Q K^T issue, 5 and 7 idle, 6 TMA producer
-//    (page-table driven), 8-11 a second set of softmax warps taking every
-//    other tile with an O of its own (bf16 cache, one copy) or the INT8
-//    widening warps.
+//    query row) per thread); 4 Q K^T issue and Q loads; TMA producers 5-7
+//    (bf16 cache: tile it by warp 5 + it % 3) or 5 (INT8 cache); 8-11 a
+//    second set of softmax warps taking every other tile with an O of its
+//    own (bf16 cache) or the INT8 widening warps.
 //  * S = Q K^T lands in one of two TMEM buffers (freed as soon as the
 //    softmax has loaded it), the softmax warps write bf16 P to TMEM, and
 //    O += P V takes P from there.  The running
@@ -148,9 +148,9 @@ static_assert(NK % SmemT<false>::NPROD == 0 && NV % SmemT<false>::NPROD == 0 &&
                   NSR % SmemT<true>::NPROD == 0,
               "slot ownership");
 static_assert(SmemT<false>::NPROD <= 3 && SmemT<true>::NPROD <= 3, "producers are warps 5-7");
-// warps: softmax and P V issue 0-3, Q K^T 4, TMA producer 6 (bf16: K), V
-// producer 7 (bf16; idle with INT8), 5 idle, then a second set of softmax
-// warps 8-11 (bf16) or the INT8 widening warps 8-11
+// warps: softmax and P V issue 0-3, Q K^T and Q loads 4, TMA producers 5-7
+// (INT8: 5; 6-7 idle), then a second set of softmax warps 8-11 (bf16) or the
+// INT8 widening warps 8-11
 template <bool KV8>
 __host__ __device__ constexpr int threads() { return 12 * 32; }
 
