@@ -1,8 +1,9 @@
 """Benchmark of the verification hot path (attention + greedy acceptance).
 
 One step = spec_verify_attn + spec_accept_greedy over one batch of a named
-synthetic workload (default: the 7B-target bf16 shape -- batch 8, 32 q/kv
-heads, head_dim 128, context 2048, k = 8, page size 16, vocab 32000).
+synthetic workload (default: the largest one, the ragged GQA 8B-target bf16
+shape -- batch 32, 32 q / 8 kv heads, head_dim 128, contexts uniform in
+[1024, 8192], k = 4, page size 16, vocab 128256).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the float64 CPU oracle, same metric
@@ -12,7 +13,11 @@ step / device step time, inputs resident in HBM); `e2e` is the same metric
 through the public API with the per-step inputs copied from pinned host
 memory and the results read back inside the timed region; `roofline` relates
 the attention call's algorithmic bytes to its measured time and to the
-measured HBM copy bandwidth.  With N > 1 (torchrun) every rank runs its own
+measured HBM copy bandwidth; `accepted_tok_s` is the goodput (tokens the
+step gains, sum of accepted_len + 1, per second); `timing` adds the same
+steps timed by one event pair and the median of 200 individually timed
+steps; `cpu_baseline` is the float64 oracle on all host cores (and on one).
+With N > 1 (torchrun) every rank runs its own
 replica on its own GPU (the path has no cross-GPU exchange); the slowest
 rank's time counts and `value` sums all ranks' tokens.
 """
@@ -37,7 +42,7 @@ sys.path.insert(0, ROOT)
 from speculative_decoding_verification_attn_gb300.workload import (  # noqa: E402
     WORKLOADS, algorithmic_bytes, make_inputs)
 
-DEFAULT_WORKLOAD = "mha7b_bf16"
+DEFAULT_WORKLOAD = "gqa8b_ragged_bf16"
 METRIC = "verified draft tokens/sec"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2**20
@@ -167,9 +172,71 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_step_estimate(inp, target_s: float, seed: int = 0):
-    """Time the float64 oracle on a bounded sample of one step and scale it to
-    the whole step.  Returns (seconds per full step, description)."""
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _oracle_rows_threaded(oracle, inp, rows, threads):
+    """The oracle's attention rows over chunks on `threads` host threads (the
+    oracle is a C library called through ctypes, which releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    s = inp.spec
+    args = (inp.q, s.q_dtype, inp.k_cache, inp.v_cache, s.kv_dtype, inp.k_scale, inp.v_scale,
+            inp.block_table, inp.ctx_lens, inp.scale)
+    if threads <= 1:
+        oracle.attn_rows(*args, rows)
+        return
+    chunks = [np.ascontiguousarray(c) for c in np.array_split(rows, min(len(rows), 8 * threads))
+              if len(c)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda c: oracle.attn_rows(*args, c), chunks))
+
+
+def _oracle_accept_threaded(oracle, inp, threads):
+    from concurrent.futures import ThreadPoolExecutor
+    s = inp.spec
+    if threads <= 1 or s.batch < 2:
+        oracle.accept_greedy(inp.logits, s.logits_dtype, inp.draft_tokens)
+        return
+    parts = [(b0, b1) for b0, b1 in zip(*[np.linspace(0, s.batch, min(s.batch, threads) + 1,
+                                                       dtype=int)[j:] for j in (0, 1)])
+             if b1 > b0]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda r: oracle.accept_greedy(np.ascontiguousarray(inp.logits[r[0]:r[1]]),
+                                                   s.logits_dtype,
+                                                   np.ascontiguousarray(inp.draft_tokens[r[0]:r[1]])),
+                    parts))
+
+
+def oracle_step_time(inp, threads: int, budget_s: float, seed: int = 0):
+    """Time the float64 oracle on one step of the workload, on `threads` host
+    threads: every attention row when that fits `budget_s`, else a random
+    sample of the rows scaled to the whole step; plus the acceptance over all
+    sequences.  Returns (seconds per full step, description, scale factor)."""
     import oracle
     s = inp.spec
     B, k, Hq = s.batch, s.num_draft, s.num_q_heads
@@ -177,41 +244,62 @@ def oracle_step_estimate(inp, target_s: float, seed: int = 0):
     rng = np.random.default_rng(seed)
     all_rows = np.stack(np.meshgrid(np.arange(B), np.arange(k), np.arange(Hq), indexing="ij"),
                         -1).reshape(-1, 3).astype(np.int32)
-    # calibrate on a few rows, then fill the time budget
-    probe = all_rows[rng.choice(rows_total, size=min(8, rows_total), replace=False)]
+    # calibrate on a few rows per thread, then fill the time budget
+    probe = all_rows[rng.choice(rows_total, size=min(4 * threads, rows_total), replace=False)]
     t0 = time.perf_counter()
-    oracle.attn_rows(inp.q, s.q_dtype, inp.k_cache, inp.v_cache, s.kv_dtype, inp.k_scale,
-                     inp.v_scale, inp.block_table, inp.ctx_lens, inp.scale, probe)
+    _oracle_rows_threaded(oracle, inp, probe, threads)
     per_row = max((time.perf_counter() - t0) / len(probe), 1e-7)
-    n = int(min(rows_total, max(len(probe), target_s * 0.8 / per_row)))
-    rows = all_rows[rng.choice(rows_total, size=n, replace=False)]
+    n = int(min(rows_total, max(len(probe), budget_s * 0.8 / per_row)))
+    rows = all_rows if n == rows_total else all_rows[np.sort(rng.choice(rows_total, size=n,
+                                                                        replace=False))]
     t0 = time.perf_counter()
-    oracle.attn_rows(inp.q, s.q_dtype, inp.k_cache, inp.v_cache, s.kv_dtype, inp.k_scale,
-                     inp.v_scale, inp.block_table, inp.ctx_lens, inp.scale, rows)
+    _oracle_rows_threaded(oracle, inp, rows, threads)
     t_attn = (time.perf_counter() - t0) * rows_total / n
     t0 = time.perf_counter()
-    oracle.accept_greedy(inp.logits, s.logits_dtype, inp.draft_tokens)
+    _oracle_accept_threaded(oracle, inp, threads)
     t_acc = time.perf_counter() - t0
-    desc = ("%d of %d attention rows (b, i, h) timed and scaled by %.1fx, plus acceptance "
-            "over all %d sequences; single-threaded C float64 oracle" %
-            (n, rows_total, rows_total / n, B))
-    return t_attn + t_acc, desc
+    who = "%d thread%s (C float64 oracle)" % (threads, "" if threads == 1 else "s")
+    if n == rows_total:
+        desc = "the whole step: all %d attention rows (b, i, h) and the acceptance of all %d " \
+               "sequences, on %s" % (rows_total, B, who)
+    else:
+        desc = ("%d of %d attention rows (b, i, h) timed and scaled by %.2fx, plus the "
+                "acceptance of all %d sequences, on %s" % (n, rows_total, rows_total / n, B, who))
+    return t_attn + t_acc, desc, rows_total / n
+
+
+def cpu_baseline(inp, budget_s: float):
+    """The oracle as it stands on the host cores: all cores (the reported
+    value) and one core, each on a bounded sample of one step."""
+    s = inp.spec
+    units = s.batch * s.num_draft
+    threads = host_threads()
+    t_all, desc_all, _ = oracle_step_time(inp, threads, budget_s, seed=0)
+    t_one, desc_one, _ = oracle_step_time(inp, 1, budget_s, seed=1)
+    return {"value": units / t_all, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": desc_all, "cpu": cpu_model(), "cpu_count": os.cpu_count(),
+            "single_core": {"value": units / t_one, "unit": UNIT, "cores": 1,
+                            "sample": desc_one}}
 
 
 def run_reference(args, inp, world, rank):
-    """--impl reference: the oracle as it stands on the host cores."""
+    """--impl reference: the oracle as it stands on the host cores (all of
+    them), whole steps when the run fits a few minutes, else a bounded sample
+    of each step scaled to the whole step (the factor is in the line)."""
     if rank != 0:
         return
     s = inp.spec
     units = s.batch * s.num_draft
-    # about two minutes of oracle time for the whole run, at most 1 s a step
-    per_step_budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    threads = host_threads()
+    # about two and a half minutes of oracle time for the whole run
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
     for _ in range(args.warmup):
-        oracle_step_estimate(inp, per_step_budget, seed=1000)
-    times, desc = [], ""
+        oracle_step_time(inp, threads, per_step_budget, seed=1000)
+    times, desc, factors = [], "", []
     for st in range(args.steps):
-        t, desc = oracle_step_estimate(inp, per_step_budget, seed=st)
+        t, desc, f = oracle_step_time(inp, threads, per_step_budget, seed=st)
         times.append(t)
+        factors.append(f)
     t_step = float(np.mean(times))
     value = units / t_step
     line = {
@@ -219,8 +307,10 @@ def run_reference(args, inp, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(inp, "host memory (CPU oracle)"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "each step: " + desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "each step: " + desc, "cpu": cpu_model(),
+                         "cpu_count": os.cpu_count()},
+        "extrapolation": float(np.mean(factors)),
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -331,6 +421,49 @@ def run_gpu(args, inp, world, rank, local):
     acc_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
     value, slowest_step_s = aggregate(units, total_ms / 1e3 / args.steps, world, device)
     ms_per_step = slowest_step_s * 1e3
+    # goodput: tokens the step gains, sum over sequences of accepted_len + 1
+    # (every input set holds the same values, so any set's results serve)
+    gained = int((outs[0]["accepted_len"].long() + 1).sum().item())
+    accepted_tok_s = gained * world / slowest_step_s
+
+    # the same K steps timed by one event pair alone (no events between the
+    # calls), and REPS steps each timed on its own for the median
+    def held(n):
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(min(2e8, 1e5 * n)))
+
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    held(args.steps)
+    p0.record(stream)
+    for j in range(args.steps):
+        step(j)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    pair_ms = p0.elapsed_time(p1) / args.steps
+    reps = max(200, args.steps)
+    rev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    torch.cuda.synchronize()
+    held(reps)
+    for j in range(reps):
+        t, o = sets[j % n_sets], outs[j % n_sets]
+        rev[j][0].record(stream)
+        binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                 t["ctx_lens"], k, scale, o["out"], o["lse"],
+                                 t.get("k_scale"), t.get("v_scale"))
+        rev[j][1].record(stream)
+        accept(t, o, j)
+        rev[j][2].record(stream)
+    torch.cuda.synchronize()
+    rep_step = np.array([e[0].elapsed_time(e[2]) for e in rev])
+    rep_attn = np.array([e[0].elapsed_time(e[1]) for e in rev])
+    rep_acc = np.array([e[1].elapsed_time(e[2]) for e in rev])
+    timing = {"timed_steps_mean_ms": ms_per_step, "single_pair_ms": pair_ms,
+              "reps": reps, "step_median_ms": float(np.median(rep_step)),
+              "step_mean_ms": float(rep_step.mean()),
+              "attn_median_ms": float(np.median(rep_attn)),
+              "accept_median_ms": float(np.median(rep_acc)),
+              "median_tok_s": units / (float(np.median(rep_step)) / 1e3)}
 
     # end to end through the public API: every step's inputs copied from
     # pinned host memory and its results read back, inside the timed region.
@@ -431,6 +564,9 @@ def run_gpu(args, inp, world, rank, local):
         "data": "synthetic (seeded N(0,1) q/K/V, N(0,2) logits; no datasets or weights)",
         "config": workload_config(inp, "inputs > L2: %d rotating copies of %.0f MB" %
                                   (n_sets, nbytes["total"] / 1e6)),
+        "accepted_tok_s": accepted_tok_s,
+        "accepted_tokens_per_step": gained,
+        "timing": timing,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (launches_per_step(inp) + (1 if rejection else 0)),
@@ -446,9 +582,7 @@ def run_gpu(args, inp, world, rank, local):
     if rejection:
         line["config"]["accept"] = "rejection sampling (T = 1, SplitMix64 draws, fresh seed per step)"
     if rank == 0 and not args.no_cpu_baseline and not rejection:
-        t_cpu, desc = oracle_step_estimate(inp, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": units / t_cpu, "unit": UNIT, "cores": 1,
-                                "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

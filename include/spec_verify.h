@@ -233,18 +233,23 @@ SPEC_API int spec_codec_decode(const void *pairs, const int32_t *num_pairs, int6
  * this is an interface convenience of this library.)
  *
  * Same operation, arguments and results as spec_accept_greedy, for callers
- * that cannot allocate device memory -- e.g. code recording the step into a
- * CUDA graph (an allocation cannot be captured, and growing the library
- * workspace synchronises the device) or a serving loop whose device memory is
- * reserved up front by its own allocator.  Its scratch (reduction partials
- * and completion tickets) is a fixed array of this library's device code,
- * present on every GPU that loads the library until exit:
+ * that cannot allocate device memory: a serving process whose GPU memory is
+ * reserved up front by its own caching allocator (a cudaMalloc outside that
+ * pool can fail once the pool holds the device, and growing this library's
+ * workspace synchronises the device in the middle of a step), or a host that
+ * loads the library as a plugin without the right to allocate.  Its scratch
+ * (reduction partials and completion tickets) is a fixed array of this
+ * library's device code, present on every GPU that loads the library until
+ * exit:
  *   - limits: batch <= SPEC_NOALLOC_MAX_BATCH and
  *     batch * (num_draft + 1) * ceil(vocab / 8192) <= SPEC_NOALLOC_MAX_PARTIALS
  *     (512 KiB of partials); larger calls return SPEC_ERR_UNSUPPORTED and
  *     enqueue nothing;
  *   - the first call on a device looks up the array's device address (and may
  *     load the library's device code): make it before any stream capture;
+ *   - that address is kept for the life of the process: calls after
+ *     cudaDeviceReset (or after the device's primary context was destroyed
+ *     and re-created) are not supported;
  *   - every call shares the array and it keeps the last call's contents; the
  *     call clears the tickets itself (an async memset on `stream`), but calls
  *     that overlap on the GPU race: order them on one stream.

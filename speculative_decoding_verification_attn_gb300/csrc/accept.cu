@@ -400,13 +400,12 @@ cudaError_t launch_accept(const AcceptArgs& a, void* workspace, int32_t* tickets
 
 // ---------------------------------------------------------------- no-allocation variant
 //
-// Greedy acceptance for callers that cannot allocate device memory: code that
-// records the verification step into a CUDA graph (an allocation cannot be
-// captured, and growing the library workspace synchronises the device), and
-// serving loops whose device memory is reserved up front by their own
-// allocator, where an extra cudaMalloc may fail or stall the step.  The
-// reduction partials and completion tickets live in one fixed array of this
-// file; every call on a device shares it.
+// Greedy acceptance for callers that cannot allocate device memory: serving
+// loops whose device memory is reserved up front by their own allocator,
+// where an extra cudaMalloc may fail or stall the step, and hosts that load
+// the library as a plugin without the right to allocate.  The reduction
+// partials and completion tickets live in one fixed array of this file;
+// every call on a device shares it.
 
 namespace specv {
 namespace {
@@ -431,7 +430,9 @@ namespace {
 
 // Device address of the fixed scratch on the current device.  The first call
 // on a device looks it up with cudaGetSymbolAddress (which may load this
-// library's device code); later calls reuse the cached address.
+// library's device code); later calls reuse the cached address, which stays
+// valid for the life of the device's primary context (a cudaDeviceReset would
+// leave it stale; the header rules such calls out).
 int noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -40,3 +40,36 @@ def rel_l2(a, b) -> float:
     b = np.asarray(b, np.float64)
     den = np.linalg.norm(b.ravel())
     return float(np.linalg.norm((a - b).ravel()) / (den if den > 0 else 1.0))
+
+
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def all_rows(inp: VerifyInputs) -> np.ndarray:
+    """Every (b, i, h) output row of a call, row-major like out[B, k, Hq]."""
+    s = inp.spec
+    grid = np.meshgrid(np.arange(s.batch), np.arange(s.num_draft), np.arange(s.num_q_heads),
+                       indexing="ij")
+    return np.stack(grid, -1).reshape(-1, 3).astype(np.int32)
+
+
+def oracle_rows_parallel(oracle, inp: VerifyInputs, rows, threads=None):
+    """oracle_rows over chunks of rows on every host core.  The oracle is a C
+    library called through ctypes, which releases the GIL for the call, so
+    threads run it in parallel on the same (shared, read-only) inputs."""
+    from concurrent.futures import ThreadPoolExecutor
+    rows = np.ascontiguousarray(np.asarray(rows, np.int32).reshape(-1, 3))
+    threads = threads or host_threads()
+    n = rows.shape[0]
+    if n == 0:
+        return np.zeros((0, inp.spec.head_dim)), np.zeros((0,))
+    chunks = [c for c in np.array_split(rows, min(n, 8 * threads)) if len(c)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda c: oracle_rows(oracle, inp, np.ascontiguousarray(c)), chunks))
+    return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))

@@ -7,7 +7,7 @@ import torch
 from speculative_decoding_verification_attn_gb300 import binding
 from speculative_decoding_verification_attn_gb300.workload import VerifyInputs
 
-from _util import oracle_accept, oracle_attn, oracle_rows, rel_l2
+from _util import all_rows, oracle_accept, oracle_attn, oracle_rows, oracle_rows_parallel, rel_l2
 
 # Tolerances for the attention output against the float64 oracle: fp32
 # inputs keep fp32 arithmetic end to end (max-abs 1e-5); bf16 / INT8 caches
@@ -65,28 +65,15 @@ def check_attn_full(oracle, inp: VerifyInputs, what=""):
     assert binding.spec_device_error() == 0
 
 
-def sample_rows(inp: VerifyInputs, n: int, seed: int = 0):
-    """n (b, i, h) rows: random ones plus the first/last draft of the
-    shortest and longest sequences and the last head."""
-    s = inp.spec
-    rng = np.random.default_rng(seed)
-    rows = [(int(rng.integers(s.batch)), int(rng.integers(s.num_draft)),
-             int(rng.integers(s.num_q_heads))) for _ in range(n)]
-    for b in (int(np.argmin(inp.ctx_lens)), int(np.argmax(inp.ctx_lens)), s.batch - 1):
-        for i in (0, s.num_draft - 1):
-            rows.append((b, i, s.num_q_heads - 1))
-            rows.append((b, i, 0))
-    return np.array(rows, np.int32)
-
-
-def check_attn_sampled(oracle, inp: VerifyInputs, n=48, t=None, what=""):
+def check_attn_every_row(oracle, inp: VerifyInputs, t=None, what=""):
+    """Every output row of a (full-size) call against the oracle, which runs
+    on every host core."""
     out, lse = gpu_attn(inp, t)
-    rows = sample_rows(inp, n)
-    ref_o, ref_l = oracle_rows(oracle, inp, rows)
-    got_o = np.stack([out[b, i, h] for b, i, h in rows])
-    got_l = np.array([lse[b, i, h] for b, i, h in rows])
-    assert_attn_close(got_o, got_l, ref_o, ref_l, tol_for(inp), what)
-    assert np.isfinite(out).all(), "non-finite output somewhere %s" % what
+    s = inp.spec
+    ref_o, ref_l = oracle_rows_parallel(oracle, inp, all_rows(inp))
+    ref_o = ref_o.reshape(s.batch, s.num_draft, s.num_q_heads, s.head_dim)
+    ref_l = ref_l.reshape(s.batch, s.num_draft, s.num_q_heads)
+    assert_attn_close(out, lse, ref_o, ref_l, tol_for(inp), what)
     assert binding.spec_device_error() == 0
     return out, lse
 

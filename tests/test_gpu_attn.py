@@ -3,8 +3,9 @@
 Small cases (the oracle computes every output) span several 64-key tiles,
 ragged tails, contexts of zero, every supported page size, GQA groups of 1 to
 8 and 1 to 128 query rows per kv-head, forced stream-K splits of every size,
-both kernels; the named full-size workloads are checked on sampled rows at
-the launch configuration the benchmark times.  NaN canaries fill every
+every kernel; the named full-size workloads are checked on every output row,
+for three seeds, at the launch configuration the benchmark times (the oracle
+runs on every host core).  NaN canaries fill every
 unused cache slot: a kernel that reads past a sequence shows non-finite
 output.
 """
@@ -18,7 +19,7 @@ from speculative_decoding_verification_attn_gb300 import binding
 from speculative_decoding_verification_attn_gb300.workload import (
     WORKLOADS, make_inputs, small_spec)
 
-from gpu_util import (assert_attn_close, check_attn_full, check_attn_sampled, full_inputs,
+from gpu_util import (assert_attn_close, check_attn_every_row, check_attn_full, full_inputs,
                       gpu_attn, tol_for)
 from _util import oracle_attn
 
@@ -183,11 +184,18 @@ def test_tensor_core_matches_simt():
     assert np.abs(a_lse - b_lse).max() < 2e-3
 
 
-@pytest.mark.parametrize("name", ["mha7b_bf16", "gqa8b_ragged_bf16", "long_step_k16_bf16",
-                                  "int8kv_70b_layer"])
-def test_named_workload_sampled(oracle_mod, name):
-    inp = full_inputs(name, 0)
-    check_attn_sampled(oracle_mod, inp, n=40, what=name)
+FULL_SIZE = [(name, seed) for name in ("mha7b_bf16", "gqa8b_ragged_bf16", "long_step_k16_bf16",
+                                        "int8kv_70b_layer") for seed in (0, 1, 2)]
+
+
+@pytest.mark.parametrize("name,seed", FULL_SIZE, ids=["%s-%d" % c for c in FULL_SIZE])
+def test_named_workload_every_row(oracle_mod, name, seed):
+    # the full-size workloads at the launch configuration the benchmark times
+    # (automatic kernel choice, one CTA per SM): every (b, i, h) output row
+    # against the oracle, so every stream-K range boundary and piece merge of
+    # the full-size split is checked
+    inp = full_inputs(name, seed)
+    check_attn_every_row(oracle_mod, inp, what="%s seed %d" % (name, seed))
 
 
 def test_lse_optional(oracle_mod):

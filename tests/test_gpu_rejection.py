@@ -4,7 +4,10 @@ Both sides draw from the same SplitMix64 stream, so the accepted length and
 the next token are compared exactly.  The kernel decides in fp32: a test
 whose uniform lies within 1e-4 of p/q, or a Gumbel-max whose two best keys
 lie within 1e-3, may legitimately go the other way; such sequences are
-checked for validity instead (and must be rare).  An independent
+checked for validity instead (and must be rare): the kept drafts passed and
+the rejected one failed their tests with the same draws, and the emitted
+token lies in the support of the residual (or of p after k acceptances)
+with a Gumbel key within the tolerance of the best.  An independent
 distribution check confirms that the GPU's first emitted token follows p.
 """
 from __future__ import annotations
@@ -15,6 +18,8 @@ import torch
 
 from speculative_decoding_verification_attn_gb300 import binding
 from speculative_decoding_verification_attn_gb300.workload import make_rejection_inputs
+
+from _util import stored_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +55,46 @@ def gpu_reject(r, seed=None, tl=None, dl=None, dr=None):
     return acc.cpu().numpy(), nxt.cpu().numpy()
 
 
+def _probs(logits, dtype, temperature):
+    """softmax(logits / T) per row in float64 (stored values widened)."""
+    x = stored_to_f64(logits, dtype) / temperature
+    x = x - x.max(axis=-1, keepdims=True)
+    e = np.exp(x)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def check_valid(oracle_mod, r, b, acc_b, nxt_b, p, q):
+    """A result the fp32 kernel may legitimately reach on a near-tie: every
+    kept draft passed its test u < p/q and the first rejected one failed it
+    (each up to U_AMBIG, with the same SplitMix64 uniforms), the emitted token
+    lies in the support of the residual max(p - q, 0) at the rejection (or of
+    p after k acceptances), and its Gumbel key ln w + g is within KEY_AMBIG of
+    the best key over that support."""
+    k = r.draft_tokens.shape[1]
+    x = r.draft_tokens[b]
+    for i in range(min(acc_b + 1, k)):
+        ratio = p[b, i, x[i]] / q[b, i, x[i]]
+        u = oracle_mod.accept_uniform(r.seed, b, i)
+        if i < acc_b:
+            assert u < ratio + U_AMBIG, "sequence %d kept draft %d with u %.6g >= p/q %.6g" % (
+                b, i, u, ratio)
+        else:
+            assert u >= ratio - U_AMBIG, "sequence %d rejected draft %d with u %.6g < p/q %.6g" % (
+                b, i, u, ratio)
+    if acc_b < k:
+        w = np.maximum(p[b, acc_b] - q[b, acc_b], 0.0)
+        # p and q are fp32 in the kernel: a token with p ~ q may sit on either side
+        assert p[b, acc_b, nxt_b] >= q[b, acc_b, nxt_b] * (1 - 1e-4), (
+            "sequence %d: token %d outside the residual's support" % (b, nxt_b))
+    else:
+        w = p[b, k]
+    support = np.nonzero(w > 0)[0]
+    keys = np.array([np.log(w[v]) + oracle_mod.gumbel(r.seed, b, int(v)) for v in support])
+    got = (np.log(w[nxt_b]) if w[nxt_b] > 0 else -np.inf) + oracle_mod.gumbel(r.seed, b, nxt_b)
+    assert got >= keys.max() - KEY_AMBIG, "sequence %d: token %d key %.6g, best %.6g" % (
+        b, nxt_b, got, keys.max())
+
+
 def check_against_oracle(oracle_mod, r, min_exact=0.9):
     acc, nxt = gpu_reject(r)
     o_acc, o_nxt, ratio, unif, gap = oracle_mod.accept_rejection(
@@ -57,13 +102,21 @@ def check_against_oracle(oracle_mod, r, min_exact=0.9):
     B, k = r.draft_tokens.shape
     V = r.target_logits.shape[-1]
     assert np.all((acc >= 0) & (acc <= k)) and np.all((nxt >= 0) & (nxt < V))
+    p = q = None
     exact = 0
     for b in range(B):
         n = o_acc[b]
         tested = min(n + 1, k)  # positions whose test the oracle ran
         ambiguous = bool(np.any(np.abs(unif[b, :tested] - ratio[b, :tested]) < U_AMBIG))
-        if ambiguous:
-            continue
+        if ambiguous or gap[b] < KEY_AMBIG:
+            # near a tie the fp32 kernel may go the other way: check that its
+            # result is one the rule allows
+            if p is None:
+                p = _probs(r.target_logits, r.dtype, r.temperature)
+                q = _probs(r.draft_logits, r.dtype, r.temperature)
+            check_valid(oracle_mod, r, b, int(acc[b]), int(nxt[b]), p, q)
+            if ambiguous:
+                continue
         assert acc[b] == n, "sequence %d: accepted %d, oracle %d" % (b, acc[b], n)
         if gap[b] < KEY_AMBIG:
             continue
