@@ -69,8 +69,9 @@ enum {
 
 /* Options for spec_set_option (process-wide; default 0 = automatic). */
 enum {
-    /* 0 auto, 1 SIMT (CUDA cores) kernel, 2 tcgen05 kernel, 3 warp-MMA
-     * (mma.sync) kernel for <= 16 query rows per kv-head */
+    /* 0 auto, 1 SIMT (CUDA cores) kernel with split-KV chunks, 2 tcgen05
+     * kernel, 3 warp-MMA (mma.sync) kernel for <= 16 query rows per kv-head,
+     * 4 single-pass SIMT kernel (whole sequences in shared memory) */
     SPEC_OPT_ATTN_PATH = 0,
     /* persistent CTAs of the tensor-core kernel; 0 = number of SMs */
     SPEC_OPT_NUM_CTAS = 1,
@@ -78,7 +79,11 @@ enum {
      * launching (synchronises the stream); 0: no host check */
     SPEC_OPT_VALIDATE = 2,
     /* key chunk of the SIMT kernel's split-KV; 0 = automatic */
-    SPEC_OPT_SIMT_CHUNK = 3
+    SPEC_OPT_SIMT_CHUNK = 3,
+    /* tensor-core kernels: tiles charged per (sequence, kv-head) segment when
+     * the tile list is split over the persistent CTAs (a segment piece's
+     * fixed work); 0 = each kernel's default, v in [1, 257] = v - 1 tiles */
+    SPEC_OPT_SPLIT_WEIGHT = 4
 };
 
 /* Library version, major*10000 + minor*100 + patch. */
@@ -122,8 +127,10 @@ SPEC_API int spec_set_option(int32_t option, int64_t value);
  * 16-byte aligned.  A bf16 query over a bf16 cache with head_dim 128, a
  * power-of-two page_size in [16, 256] and batch <= 1024 runs on a
  * tensor-core kernel: the warp-MMA kernel when num_draft * (num_q_heads /
- * num_kv_heads) <= 16, the tcgen05 kernel up to 128; every other accepted
- * shape runs on the SIMT kernel.
+ * num_kv_heads) <= 16, the tcgen05 kernel up to 128.  Every other accepted
+ * shape runs on the CUDA cores: in one launch when every sequence's keys
+ * (max_pages_per_seq * page_size of them) fit the single-pass kernel's
+ * shared memory, else on the chunked split-KV kernel and its combine.
  */
 SPEC_API int spec_verify_attn(const void *q, const void *k_cache, const void *v_cache,
                      const void *k_scale, const void *v_scale,

@@ -165,6 +165,8 @@ accept_cluster_kernel(AcceptArgs a, int parts, int64_t part_len) {
     __shared__ int s_am[65];
     __shared__ int s_first_miss;
 
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const int tid = threadIdx.x;
     const int S = (a.k + 1) * parts;  // cluster size
     const uint32_t rank = cluster_ctarank();
@@ -235,6 +237,8 @@ accept_greedy_kernel(AcceptArgs a, int n_slices, float* __restrict__ part_v,
     __shared__ int s_am[65];
     __shared__ int s_first_miss;
 
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const int row = blockIdx.x / n_slices;  // row of [B, k+1]
     const int slice = blockIdx.x % n_slices;
     const int b = row / (a.k + 1);
@@ -353,13 +357,15 @@ cudaError_t launch_cluster(const AcceptArgs& a, int parts, cudaStream_t stream) 
     cfg.gridDim = dim3((unsigned)((int64_t)a.B * S));
     cfg.blockDim = dim3(kCThreads);
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)S;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, accept_cluster_kernel<T>, a, parts, part_len);
 }
 
@@ -389,11 +395,10 @@ cudaError_t launch_accept(const AcceptArgs& a, void* workspace, int32_t* tickets
     float* pv = static_cast<float*>(workspace);
     int* pi = reinterpret_cast<int*>(pv + total);
     if (a.dtype == SPEC_DTYPE_F32)
-        accept_greedy_kernel<float><<<(unsigned)total, kThreads, 0, stream>>>(a, ns, pv, pi, tickets);
-    else
-        accept_greedy_kernel<__nv_bfloat16>
-            <<<(unsigned)total, kThreads, 0, stream>>>(a, ns, pv, pi, tickets);
-    return cudaGetLastError();
+        return launch_dependent(accept_greedy_kernel<float>, dim3((unsigned)total), dim3(kThreads), 0,
+                                stream, a, ns, pv, pi, tickets);
+    return launch_dependent(accept_greedy_kernel<__nv_bfloat16>, dim3((unsigned)total),
+                            dim3(kThreads), 0, stream, a, ns, pv, pi, tickets);
 }
 
 }  // namespace specv

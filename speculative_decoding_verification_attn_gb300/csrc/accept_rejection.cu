@@ -37,8 +37,6 @@ namespace {
 constexpr int kRThreads = 256;
 constexpr int kRSlice = 2048;  // vocabulary entries per CTA (many small CTAs balance the
                                // Gumbel-heavy rows against the plain ones)
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ uint64_t sm64_at(uint64_t seed, uint64_t n) {
     uint64_t z = seed + (n + 1) * 0x9E3779B97F4A7C15ull;

@@ -60,6 +60,10 @@ constexpr int MAX_BATCH = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
+// tiles charged per segment in the split over the CTAs: none -- measured on
+// the 7B and 8B shapes, any charge made the slowest CTA later (this
+// kernel's per-piece work is small next to its 128-key tiles)
+constexpr int kSplitAlpha = 0;
 
 using Cursor = CursorT<TN>;
 
@@ -70,8 +74,9 @@ struct Smem {
     static constexpr int PREF_LSE = PREF + QROWS * D * 4;       // [128] float: its lse slot
     static constexpr int BARS = PREF_LSE + 128 * 4;
     static constexpr int B_KVFULL = 0, B_QFULL = NS * NW, NUM_BARS = NS * NW + 2;
-    static constexpr int MISC = BARS + NUM_BARS * 8;            // abort flag, prefetch state/slot
-    static constexpr int STAT = MISC + 16;                      // [NW][16] (m, l)
+    // abort flag, prefetch state / slot, then (at +16) the CTA's tile range
+    static constexpr int MISC = BARS + NUM_BARS * 8;
+    static constexpr int STAT = MISC + 32;                      // [NW][16] (m, l)
     static constexpr int CTX = STAT + 2 * NW * QROWS * 4;
     static constexpr int PRE = CTX + MAX_BATCH * 4;
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
@@ -144,6 +149,9 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         for (int e = tid; e < 2 * Q_BUF / 16; e += THREADS) q4[e] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
+    // the grids before this one have finished with every buffer this call touches
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     if (warp == 0) {
         const int per = (B + 31) / 32, lo = lane * per, hi = min(B, lo + per);
         int sum = 0;
@@ -170,13 +178,23 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
         if (lane == 31) s_pre[B] = incl;
     }
-    __syncthreads();
 
-    const int64_t T = (int64_t)s_pre[B] * Hkv;
-    const int64_t C = gridDim.x;
-    const int64_t t_begin = (int64_t)blockIdx.x * T / C;
-    const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
-    const int n_tiles = (int)(t_end - t_begin);
+    // the CTA's tile range [t_begin, t_end), kept in shared memory; the split
+    // is rebuilt where the merge needs it rather than held in registers
+    int64_t* s_rng = reinterpret_cast<int64_t*>(sm + Smem::MISC + 16);
+    auto make_split = [&]() {
+        TileSplit sp;
+        sp.init(s_pre, B, Hkv, a.split_alpha < 0 ? kSplitAlpha : a.split_alpha, gridDim.x);
+        return sp;
+    };
+    if (warp == 0) {
+        __syncwarp();  // the prefix above, written by this warp's lanes
+        if (lane < 2) s_rng[lane] = make_split().begin(blockIdx.x + lane);
+    }
+    __syncthreads();
+    auto t_begin = [&]() { return ld_shared_s64(s_rng); };
+    auto t_end = [&]() { return ld_shared_s64(s_rng + 1); };
+    const int n_tiles = (int)(t_end() - t_begin());
 
     {
         // ===== warp w owns keys [16w, 16w+16) of every tile and keeps its own
@@ -229,13 +247,13 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                             kvh * G, b * k);
         };
         // does a piece follow the one of cursor c in this CTA's range
-        auto has_next_piece = [&](const Cursor& c) { return c.seg_start + c.nb < t_end; };
+        auto has_next_piece = [&](const Cursor& c) { return c.seg_start + c.nb < t_end(); };
 
         Cursor cur, ahead;  // ahead: the tile NS past cur, the next one to load
         uint32_t pending = 0, phase = 0;  // per stage: a load in flight / the parity it completes
         int q_issued = 0;                 // warp 0: pieces whose query rows were loaded
         if (n_tiles > 0) {
-            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+            cur.init(t_begin(), s_pre, s_ctx, B, Hkv, k);
             ahead = cur;
             if (warp == 0) {
                 q_issued = has_next_piece(cur) ? 2 : 1;
@@ -273,9 +291,19 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 
         // pieces of a segment split over CTA ranges: CTA of tile t, empty
         // ranges, partial slot of CTA c's piece of the segment starting at s0
-        auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
-        auto empty_cta = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
-        auto slot_of = [&](int c, int64_t s0) { return 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1); };
+        // (the pieces of the segment under cursor c span CTAs first_cta(c) .. last_cta(c))
+        auto first_cta = [&](const Cursor& c) {
+            const TileSplit sp = make_split();
+            return sp.cta_of_cost(sp.cost_of(c.b, c.kvh, 0, c.nb));
+        };
+        auto last_cta = [&](const Cursor& c) {
+            const TileSplit sp = make_split();
+            return sp.cta_of_cost(sp.cost_of(c.b, c.kvh, c.nb - 1, c.nb));
+        };
+        auto empty_cta = [&](int c) { return make_split().empty(c); };
+        auto slot_of = [&](int c, int64_t s0) {
+            return 2 * c + (s0 < make_split().begin(c) ? 0 : 1);
+        };
         // End-of-range prefetch (warp 0).  The piece that ends this CTA's range
         // in a segment that continues in the next CTA is normally the last of
         // the segment's two pieces to finish (the other one ran at the start of
@@ -342,10 +370,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
                 m_ref[0] = m_ref[1] = -INFINITY;
                 lsum[0] = lsum[1] = 0.f;
-                if (warp == 0 && ok && !has_next_piece(cur) && cur.seg_start + cur.nb > t_end) {
+                if (warp == 0 && ok && !has_next_piece(cur) && cur.seg_start + cur.nb > t_end()) {
                     const int64_t s0 = cur.seg_start;
                     int npieces = 0, other = -1;
-                    for (int c = cta_of(s0); c <= cta_of(s0 + cur.nb - 1); ++c)
+                    for (int c = first_cta(cur); c <= last_cta(cur); ++c)
                         if (!empty_cta(c)) {
                             ++npieces;
                             if (c != (int)blockIdx.x) other = c;
@@ -578,7 +606,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     acc[0] = lo4.x; acc[1] = lo4.y; acc[2] = lo4.z; acc[3] = lo4.w;
                     acc[4] = hi4.x; acc[5] = hi4.y; acc[6] = hi4.z; acc[7] = hi4.w;
                 }
-                const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
+                const bool complete = cur.seg_start >= t_begin() && cur.seg_start + cur.nb <= t_end();
                 const int seg = cur.b * Hkv + cur.kvh;
                 const int64_t orow_rr =
                     ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
@@ -647,7 +675,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 } else {
                     // publish this piece's partial; warp 0 then counts the
                     // arrival, and the last piece of the segment merges them all
-                    const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
+                    const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin() ? 0 : 1);
                     if (ok) {
                         if (rr < R) {
                             float4* dst = reinterpret_cast<float4*>(
@@ -670,31 +698,46 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 if (count_arrival && warp == 0) {
                     const int64_t s0 = cur.seg_start;
-                    const int c_first = cta_of(s0), c_last = cta_of(s0 + cur.nb - 1);
+                    const int c_first = first_cta(cur), c_last = last_cta(cur);
+                    const int ncta = c_last - c_first + 1;
+                    // lane j: the partial slot of CTA c_first + j's piece, -1 for an
+                    // empty range (computed once here when the segment spans at most
+                    // 32 CTAs; per use beyond that)
+                    int my_slot = -1;
+                    if (lane < ncta) {
+                        const TileSplit sp = make_split();
+                        const int c = c_first + lane;
+                        const int64_t b0 = sp.begin(c), b1 = sp.begin(c + 1);
+                        if (b0 != b1) my_slot = 2 * c + (s0 < b0 ? 0 : 1);
+                    }
+                    const unsigned pieces = __ballot_sync(0xffffffffu, my_slot >= 0);
+                    int npieces = __popc(pieces);
+                    for (int j0 = 32; j0 < ncta; j0 += 32) {
+                        const bool ne = j0 + lane < ncta && !empty_cta(c_first + j0 + lane);
+                        npieces += __popc(__ballot_sync(0xffffffffu, ne));
+                    }
                     int merger = 0;
                     if (lane == 0) {
-                        int npieces = 0;
-                        for (int c = c_first; c <= c_last; ++c) npieces += empty_cta(c) ? 0 : 1;
                         __threadfence();  // release the partials (ordered by the barrier)
                         merger = atomicAdd(&a.seg_counters[seg], 1) == npieces - 1;
                         if (merger) __threadfence();  // acquire the other pieces' partials
                     }
                     merger = __shfl_sync(0xffffffffu, merger, 0);
                     if (merger) {
-                        // warp 0 merges every piece's partial; the other warps go on
-                        for (int idx = lane; idx < R * (D / 8); idx += 32) {
-                            const int r2 = idx / (D / 8), c8 = idx % (D / 8);
+                        // warp 0 merges every piece's partial; the other warps go on.
+                        // Every lane runs every round (the shuffles need the whole warp)
+                        for (int base = 0; base < R * (D / 8); base += 32) {
+                            const int idx = base + lane;
+                            const bool act = idx < R * (D / 8);
+                            const int r2 = act ? idx / (D / 8) : 0, c8 = idx % (D / 8);
                             float mx = -INFINITY, tot = 0.f;
                             float m8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-                            for (int c = c_first; c <= c_last; ++c) {
-                                if (empty_cta(c)) continue;
-                                const int sl = slot_of(c, s0);
+                            auto fold = [&](int sl) {
                                 const float lw = __ldcg(prm.part_lse + (int64_t)sl * 128 + r2);
                                 const float4* src = reinterpret_cast<const float4*>(
                                     prm.part_o + ((int64_t)sl * 128 + r2) * D + c8 * 8);
                                 const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-                                if (lw == -INFINITY) continue;
+                                if (lw == -INFINITY) return;
                                 const float mn = fmaxf(mx, lw);
                                 const float sa = mx == -INFINITY ? 0.f : __expf(mx - mn);
                                 const float sb = __expf(lw - mn);
@@ -704,11 +747,22 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                                 m8[2] = m8[2] * sa + sb * x0.z; m8[3] = m8[3] * sa + sb * x0.w;
                                 m8[4] = m8[4] * sa + sb * x1.x; m8[5] = m8[5] * sa + sb * x1.y;
                                 m8[6] = m8[6] * sa + sb * x1.z; m8[7] = m8[7] * sa + sb * x1.w;
+                            };
+                            if (ncta <= 32) {
+                                for (unsigned m = pieces; m; m &= m - 1) {
+                                    const int sl = __shfl_sync(0xffffffffu, my_slot, __ffs(m) - 1);
+                                    if (act) fold(sl);
+                                }
+                            } else if (act) {
+                                for (int c = c_first; c <= c_last; ++c)
+                                    if (!empty_cta(c)) fold(slot_of(c, s0));
                             }
-                            const int64_t orow =
-                                ((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G;
-                            store_out(orow, c8, m8, tot > 0.f ? 1.f / tot : 0.f);
-                            if (c8 == 0 && a.lse) a.lse[orow] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+                            if (act) {
+                                const int64_t orow =
+                                    ((int64_t)cur.b * k + r2 / G) * a.Hq + cur.kvh * G + r2 % G;
+                                store_out(orow, c8, m8, tot > 0.f ? 1.f / tot : 0.f);
+                                if (c8 == 0 && a.lse) a.lse[orow] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+                            }
                         }
                         if (lane == 0) a.seg_counters[seg] = 0;  // ready for the next call
                     }
@@ -797,7 +851,9 @@ cudaError_t launch_attn_mma(const AttnArgs& a, int num_ctas, void* workspace, cu
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attn_mma_kernel<<<num_ctas, THREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, prm);
+    e = launch_dependent(attn_mma_kernel, dim3(num_ctas), dim3(THREADS), SMEM_BYTES, stream, qmap,
+                         kmap, vmap, prm);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

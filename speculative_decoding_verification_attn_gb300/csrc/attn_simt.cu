@@ -58,6 +58,8 @@ template <typename TQ, typename TKV>
 __global__ void __launch_bounds__(kThreads)
 attn_simt_kernel(AttnArgs a, SimtPlan p, float* __restrict__ part_o, float* __restrict__ part_lse) {
     extern __shared__ float sm[];
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const int D = a.D, G = a.Hq / a.Hkv, R = a.k * G, RG = p.rows_per_group;
     const int chunk_id = blockIdx.x;
     const int rg = blockIdx.y % p.row_groups;
@@ -178,6 +180,8 @@ template <typename TQ>
 __global__ void __launch_bounds__(256)
 combine_simt_kernel(AttnArgs a, SimtPlan p, const float* __restrict__ part_o,
                     const float* __restrict__ part_lse) {
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const int seg = blockIdx.x, kvh = seg % a.Hkv, b = seg / a.Hkv;
     const int G = a.Hq / a.Hkv, R = a.k * G, D = a.D;
     const int row = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -223,13 +227,12 @@ cudaError_t launch_typed(const AttnArgs& a, const SimtPlan& p, float* part_o, fl
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.max_chunks, a.B * a.Hkv * p.row_groups);
-    kern<<<grid, kThreads, smem, stream>>>(a, p, part_o, part_lse);
-    e = cudaGetLastError();
+    e = launch_dependent(kern, grid, dim3(kThreads), smem, stream, a, p, part_o, part_lse);
     if (e != cudaSuccess || p.max_chunks <= 1) return e;
     const int R = a.k * (a.Hq / a.Hkv);
     dim3 cgrid(a.B * a.Hkv, (R + 7) / 8);
-    combine_simt_kernel<TQ><<<cgrid, 256, 0, stream>>>(a, p, part_o, part_lse);
-    return cudaGetLastError();
+    return launch_dependent(combine_simt_kernel<TQ>, cgrid, dim3(256), 0, stream, a, p,
+                            static_cast<const float*>(part_o), static_cast<const float*>(part_lse));
 }
 
 }  // namespace

@@ -88,6 +88,14 @@ __host__ __device__ constexpr uint32_t idesc_pv() {  // B (V) MN-major
 }
 using Cursor = CursorT<TN>;
 
+// Tiles charged per segment in the split over the CTAs: a piece boundary
+// drains the tensor-core pipeline (the next piece's queries, the merge of the
+// softmax states) for about six 64-key tiles of the bf16 cache's work, five
+// of the INT8 cache's slower ones.
+__host__ __device__ inline int split_alpha(const AttnArgs& a) {
+    return a.split_alpha >= 0 ? a.split_alpha : a.kv_dtype == SPEC_DTYPE_I8 ? 5 : 6;
+}
+
 // Shared-memory plan (offsets from the 1024-aligned base).  INT8 cache:
 // boxes land in NSR raw stages, converted tiles go to NCV operand stages,
 // with one fp32 row of per-key k / v scales per operand stage.
@@ -122,10 +130,11 @@ struct SmemT {
                          B_SFULL = B_QFULL + 2, B_SFREE = B_SFULL + NSB, B_ODONE = B_SFREE + NSB,
                          B_DRAIN = B_ODONE + 2, B_QCP = B_DRAIN + 3,
                          NUM_BARS = B_QCP + 1;
-    static constexpr int MISC = BARS + NUM_BARS * 8;          // tmem base, abort flag
+    // tmem base, abort flag, then (at +16) the CTA's tile range
+    static constexpr int MISC = BARS + NUM_BARS * 8;
     // (m, l) of [set x copy][row]: bf16 two sets x up to 4 copies, INT8 one set
     static constexpr int NSTAT = KV8 ? 4 : 8;
-    static constexpr int STAT = MISC + 16;
+    static constexpr int STAT = MISC + 32;
     // TMA producer warps (5, 6, ...): tile it is issued by warp 5 + it % NPROD.
     // bf16: three, since one issuing thread caps the bytes a CTA keeps in
     // flight; INT8: one (its raw boxes are small and the widening warps set
@@ -183,7 +192,7 @@ struct Cta {
     const int* s_ctx;
     const int* s_pre;
     uint32_t tmem;
-    int64_t t_begin, t_end;
+    const int64_t* rng;  // shared memory: the CTA's tile range [rng[0], rng[1])
     int n_tiles, R, G, BH;
 };
 
@@ -263,7 +272,7 @@ __device__ void softmax_role(const Cta& x) {
     bool has = false;  // this set has taken a tile of the current piece
     uint64_t mrow = 0;  // draft bits of this thread's query row, per piece
     Cursor cur;
-    if (x.n_tiles > 0) cur.init(x.t_begin, x.s_pre, x.s_ctx, a.B, a.Hkv, k);
+    if (x.n_tiles > 0) cur.init(ld_shared_s64(x.rng), x.s_pre, x.s_ctx, a.B, a.Hkv, k);
     bool ok = true;
     for (int it = 0; it < x.n_tiles; ++it) {
         const bool first = (it == 0) || (cur.lt == 0);
@@ -492,8 +501,9 @@ __device__ void softmax_role(const Cta& x) {
                 }
                 tc_fence_after();
             }
-            const bool complete = cur.seg_start >= x.t_begin && cur.seg_start + cur.nb <= x.t_end;
-            const int slot = 2 * blockIdx.x + (cur.seg_start < x.t_begin ? 0 : 1);
+            const int64_t t_begin = ld_shared_s64(x.rng), t_end = ld_shared_s64(x.rng + 1);
+            const bool complete = cur.seg_start >= t_begin && cur.seg_start + cur.nb <= t_end;
+            const int slot = 2 * blockIdx.x + (cur.seg_start < t_begin ? 0 : 1);
             auto out_row = [&](int rr) {
                 return ((int64_t)cur.b * k + rr / G) * a.Hq + cur.kvh * G + rr % G;
             };
@@ -761,6 +771,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // the grids before this one have finished with every buffer this call touches
+    // (and with the tensor memory of this SM)
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     if (warp == 4) {
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
@@ -799,6 +813,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             run += (s_ctx[b] + k + TN - 1) / TN;
         }
         if (lane == 31) s_pre[B] = incl;
+        // the CTA's tile range [t_begin, t_end), kept in shared memory so that
+        // it occupies no register through the role loops
+        __syncwarp();  // the prefix above, written by this warp's lanes
+        if (lane < 2) {
+            TileSplit split;
+            split.init(s_pre, B, Hkv, split_alpha(a), gridDim.x);
+            reinterpret_cast<int64_t*>(sm + Smem::MISC + 16)[lane] = split.begin(blockIdx.x + lane);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -806,13 +828,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint32_t tmem = *tmem_slot;
 
     const int64_t T = (int64_t)s_pre[B] * Hkv;
-    const int64_t C = gridDim.x;
-    const int64_t t_begin = (int64_t)blockIdx.x * T / C;
-    const int64_t t_end = ((int64_t)blockIdx.x + 1) * T / C;
-    const int n_tiles = (int)(t_end - t_begin);
+    const int64_t* s_rng = reinterpret_cast<const int64_t*>(sm + Smem::MISC + 16);
+    const int64_t t_begin = ld_shared_s64(s_rng);
+    const int n_tiles = (int)(ld_shared_s64(s_rng + 1) - t_begin);
     if (tid == 0) {
         // the segment holding tile t_begin (b, kv-head, its tile index lt,
-        // its length) and T, for the combine; lt = -1: no tile there
+        // its length) and t_begin itself, for the combine; lt = -1: no tile
+        // there
         int4 r0 = make_int4(0, 0, -1, 0);
         if (t_begin < T) {
             Cursor c0;
@@ -820,7 +842,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             r0 = make_int4(c0.b, c0.kvh, c0.lt, c0.nb);
         }
         prm.seg_rec[2 * blockIdx.x] = r0;
-        prm.seg_rec[2 * blockIdx.x + 1] = make_int4((int)(T & 0xffffffff), (int)(T >> 32), 0, 0);
+        prm.seg_rec[2 * blockIdx.x + 1] =
+            make_int4((int)(t_begin & 0xffffffff), (int)(t_begin >> 32), 0, 0);
     }
     if (blockIdx.x == 0)
         for (int b = tid; b <= B; b += threads<KV8>()) prm.seg_pre[b] = s_pre[b];
@@ -1188,8 +1211,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         x.s_ctx = s_ctx;
         x.s_pre = s_pre;
         x.tmem = tmem;
-        x.t_begin = t_begin;
-        x.t_end = t_end;
+        x.rng = s_rng;
         x.n_tiles = n_tiles;
         x.R = R;
         x.G = G;
@@ -1227,7 +1249,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 // per warp.
 template <bool BY_SEG>
 __global__ void __launch_bounds__(256)
-combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
+combine_tc_kernel(AttnArgs a, int num_ctas, int alpha, const float* __restrict__ part_o,
                   const float* __restrict__ part_lse, const int4* __restrict__ seg_rec,
                   const int* __restrict__ seg_pre) {
     // BY_SEG: block x handles segment x (sequence x / Hkv, kv-head x % Hkv);
@@ -1235,17 +1257,21 @@ combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
     // x+1's first tile, when that is not the segment's first tile and this
     // is the first boundary inside it.  The launch takes the form with fewer
     // blocks.
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const int G = a.Hq / a.Hkv, R = a.k * G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t C = num_ctas;
+    // the attention kernel's split of the tile list over its CTAs
+    TileSplit split;
+    split.init(seg_pre, a.B, a.Hkv, alpha, C);
     int b, kvh, nb;
-    int64_t T, s0;
+    int64_t s0;
     if constexpr (BY_SEG) {
         b = blockIdx.x / a.Hkv;
         kvh = blockIdx.x % a.Hkv;
         const int p0 = __ldg(seg_pre + b);
         nb = __ldg(seg_pre + b + 1) - p0;
-        T = (int64_t)__ldg(seg_pre + a.B) * a.Hkv;
         s0 = (int64_t)p0 * a.Hkv + (int64_t)kvh * nb;
     } else {
         const int x = blockIdx.x + 1;
@@ -1254,21 +1280,25 @@ combine_tc_kernel(AttnArgs a, int num_ctas, const float* __restrict__ part_o,
         b = r0.x;
         kvh = r0.y;
         nb = r0.w;
-        T = (int64_t)(uint32_t)r1.x | ((int64_t)r1.y << 32);
-        s0 = (int64_t)x * T / C - r0.z;
+        s0 = ((int64_t)(uint32_t)r1.x | ((int64_t)r1.y << 32)) - r0.z;
     }
-    const int64_t s1 = s0 + nb;
-    auto cta_of = [&](int64_t t) { return (int)(((t + 1) * C - 1) / T); };
-    const int c_first = cta_of(s0), c_last = cta_of(s1 - 1);
+    const int c_first = split.cta_of_cost(split.cost_of(b, kvh, 0, nb));
+    const int c_last = split.cta_of_cost(split.cost_of(b, kvh, nb - 1, nb));
     if (BY_SEG ? c_first == c_last : c_first + 1 != (int)blockIdx.x + 1)
         return;  // written directly by its CTA / handled at an earlier boundary
     const int row = blockIdx.y * 8 + warp;
     if (row >= R) return;
 
-    // CTA c covers tiles [c*T/C, (c+1)*T/C); a CTA with an empty range wrote
-    // nothing and is skipped
-    auto empty = [&](int c) { return (int64_t)c * T / C == ((int64_t)c + 1) * T / C; };
-    auto slot_of = [&](int c) { return 2 * c + (s0 < (int64_t)c * T / C ? 0 : 1); };
+    // CTA c's first tile, from its record (CTA C: the end of the list); a
+    // CTA with an empty range wrote nothing and is skipped
+    const int64_t T = (int64_t)__ldg(seg_pre + a.B) * a.Hkv;
+    auto begin = [&](int c) -> int64_t {
+        if (c >= C) return T;
+        const int4 r = __ldg(seg_rec + 2 * c + 1);
+        return (int64_t)(uint32_t)r.x | ((int64_t)r.y << 32);
+    };
+    auto empty = [&](int c) { return begin(c) == begin(c + 1); };
+    auto slot_of = [&](int c) { return 2 * c + (s0 < begin(c) ? 0 : 1); };
     constexpr uint32_t kAll = 0xffffffffu;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse_tot;
@@ -1457,17 +1487,16 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
         e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_bytes<true>());
         if (e != cudaSuccess) return e;
-        attn_tc_kernel<true><<<num_ctas, threads<true>(), smem_bytes<true>(), stream>>>(
-            qmap, kmap, vmap, prm);
+        e = launch_dependent(attn_tc_kernel<true>, dim3(num_ctas), dim3(threads<true>()),
+                             smem_bytes<true>(), stream, qmap, kmap, vmap, prm);
     } else {
         e = cudaFuncSetAttribute(attn_tc_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_bytes<false>());
         if (e != cudaSuccess) return e;
-        attn_tc_kernel<false><<<num_ctas, threads<false>(), smem_bytes<false>(), stream>>>(
-            qmap, kmap, vmap, prm);
+        e = launch_dependent(attn_tc_kernel<false>, dim3(num_ctas), dim3(threads<false>()),
+                             smem_bytes<false>(), stream, qmap, kmap, vmap, prm);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, prm.seg_rec,
                                    prm.seg_pre, stream);
@@ -1478,15 +1507,16 @@ cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float
                                     const int* seg_pre, cudaStream_t stream) {
     if (num_ctas < 2) return cudaSuccess;  // one CTA splits nothing
     const int R = a.k * (a.Hq / a.Hkv);
+    const int alpha = split_alpha(a);
     const int64_t segs = (int64_t)a.B * a.Hkv;
     if (segs <= num_ctas - 1) {
         dim3 cgrid((unsigned)segs, (R + 7) / 8);
-        combine_tc_kernel<true>
-            <<<cgrid, 256, 0, stream>>>(a, num_ctas, part_o, part_lse, seg_rec, seg_pre);
+        return launch_dependent(combine_tc_kernel<true>, cgrid, dim3(256), 0, stream, a, num_ctas,
+                                alpha, part_o, part_lse, seg_rec, seg_pre);
     } else {
         dim3 cgrid(num_ctas - 1, (R + 7) / 8);
-        combine_tc_kernel<false>
-            <<<cgrid, 256, 0, stream>>>(a, num_ctas, part_o, part_lse, seg_rec, seg_pre);
+        return launch_dependent(combine_tc_kernel<false>, cgrid, dim3(256), 0, stream, a, num_ctas,
+                                alpha, part_o, part_lse, seg_rec, seg_pre);
     }
     return cudaGetLastError();
 }

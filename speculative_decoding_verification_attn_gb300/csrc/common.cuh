@@ -357,6 +357,82 @@ __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t start, uint32_t lb
 
 // ------------------------------------------------------------------ persistent tile walk
 
+// Split of the tile list over the C CTAs of a persistent grid.  Every piece
+// of a segment a CTA processes costs fixed work besides its tiles (loading
+// the piece's query rows, draining and merging its partial results), so an
+// equal number of tiles per CTA leaves the CTAs whose ranges hold more
+// segment starts finishing last.  The split therefore runs over a cost
+// coordinate in which each segment (sequence b, kv-head h; sequences in
+// order, kv-heads inside a sequence) is preceded by `alpha` units for that
+// fixed work and then holds its nb(b) = pre[b+1] - pre[b] tiles; CTA c takes
+// the tiles of costs [c W / C, (c+1) W / C).  alpha = 0 is the equal split.
+// `pre` is the per-sequence tile prefix (per kv-head), in shared or global
+// memory.
+struct TileSplit {
+    const int* pre;
+    int B, Hkv, alpha;
+    int64_t C, W;
+
+    __device__ void init(const int* pre_, int B_, int Hkv_, int alpha_, int64_t C_) {
+        pre = pre_;
+        B = B_;
+        Hkv = Hkv_;
+        alpha = alpha_;
+        C = C_;
+        W = cost_pre(B);
+    }
+    // cost at the start of sequence b
+    __device__ int64_t cost_pre(int b) const {
+        return ((int64_t)pre[b] + (int64_t)alpha * b) * Hkv;
+    }
+    // the first tile at or after cost x (32-bit arithmetic when the list is
+    // shorter than 2^31 cost units, as every realistic call is)
+    __device__ int64_t tile_at(int64_t x) const {
+        if (x >= W) return (int64_t)pre[B] * Hkv;
+        if (alpha == 0) return x;  // the cost of a tile is its index
+        int lo = 0, hi = B - 1;  // largest b with cost_pre(b) <= x
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cost_pre(mid) <= x) lo = mid; else hi = mid - 1;
+        }
+        const int nb = pre[lo + 1] - pre[lo];
+        const int64_t off = x - cost_pre(lo);
+        int64_t h, r;
+        if (W < (1LL << 31)) {
+            const uint32_t o32 = (uint32_t)off, seg = (uint32_t)(nb + alpha);
+            h = o32 / seg;
+            r = o32 - (uint32_t)h * seg;
+        } else {
+            h = off / (nb + alpha);
+            r = off % (nb + alpha);
+        }
+        return (int64_t)pre[lo] * Hkv + h * nb + (r > alpha ? r - alpha : 0);
+    }
+    // first tile of CTA c (c = C: the end of the list)
+    __device__ int64_t begin(int64_t c) const {
+        const int64_t x = W < (1LL << 31) && c < 65536
+                              ? (int64_t)((uint64_t)c * (uint64_t)W / (uint64_t)C)
+                              : c * W / C;
+        return tile_at(x);
+    }
+    __device__ bool empty(int64_t c) const { return begin(c) == begin(c + 1); }
+    // cost of tile lt of segment (b, kvh) with nb tiles
+    __device__ int64_t cost_of(int b, int kvh, int lt, int nb) const {
+        return cost_pre(b) + (int64_t)kvh * (nb + alpha) + alpha + lt;
+    }
+    // CTA whose range holds the tile of cost x
+    __device__ int cta_of_cost(int64_t x) const { return (int)(((x + 1) * C - 1) / W); }
+};
+
+// A 64-bit value in shared memory, read afresh at every use: the persistent
+// kernels keep their CTA range there so that it occupies no register through
+// their main loops.
+__device__ __forceinline__ int64_t ld_shared_s64(const int64_t* p) {
+    int64_t v;
+    asm volatile("ld.shared.s64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
 // Verification work is the list of TILE_KEYS-key tiles of every (sequence,
 // kv-head) segment, sequences in order, kv-heads inside a sequence.  pre[b]
 // = tiles of sequences 0..b-1 (per kv-head), ctx[b] = clamped context.
@@ -507,4 +583,37 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+
+
+// ------------------------------------------------------------------ dependent launch
+//
+// The step's kernels are launched with programmatic stream serialization: the
+// next kernel on the stream may be scheduled while this one is still running,
+// which hides the launch latency between the two calls of a step (and between
+// steps).  Stream order is kept by the waits: every kernel waits for the
+// grids before it to complete, and their writes to be visible, before its
+// first global-memory access (read or write); until then it only sets up
+// on-chip state.  A kernel launched without the attribute, or with nothing
+// before it, passes the wait at once.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` on `stream` with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 }  // namespace specv

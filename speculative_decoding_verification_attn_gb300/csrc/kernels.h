@@ -28,6 +28,9 @@ struct AttnArgs {
     // [B, k] draft-visibility bits (bit t of row i: query i sees draft t), or
     // null for the causal chain (bits 0..i)
     const uint64_t* tree_mask;
+    // tensor-core kernels: tiles charged per segment when the tile list is
+    // split over the persistent CTAs (TileSplit); < 0 = the kernel's default
+    int32_t split_alpha = -1;
 };
 
 // Draft bits visible to query i of sequence b: the tree row, or the causal chain.
@@ -52,15 +55,22 @@ size_t simt_workspace_bytes(const AttnArgs& a, const SimtPlan& p);
 cudaError_t launch_attn_simt(const AttnArgs& a, const SimtPlan& p, void* workspace,
                              cudaStream_t stream);
 
+// ---- single-pass SIMT kernel for short contexts (one launch, no split) ----
+// Longest context it holds (the whole block table of a sequence), or 0 when
+// the call does not fit its shared-memory plan.
+int small_attn_max_keys(const AttnArgs& a);
+cudaError_t launch_attn_small(const AttnArgs& a, cudaStream_t stream);
+
 // ---- tensor-core kernel (tcgen05 + TMA, persistent, split-KV stream-K) ----
 bool tc_supported(const AttnArgs& a);
 size_t tc_workspace_bytes(const AttnArgs& a, int num_ctas);
 cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream);
 
 // Merge of the split-KV partials written by the tensor-core kernel (64-key
-// tiles over `num_ctas` persistent CTAs; partial slots [2*C][128][D]; per CTA
-// boundary the segment record {b, kv-head, tile-in-segment, tiles} and T;
-// per sequence the tile prefix).
+// tiles over `num_ctas` persistent CTAs, split by TileSplit with the kernel's
+// per-segment charge; partial slots [2*C][128][D]; per CTA boundary the
+// segment record {b, kv-head, tile-in-segment, tiles} and the CTA's first
+// tile; per sequence the tile prefix).
 cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float* part_o,
                                     const float* part_lse, const int4* seg_rec,
                                     const int* seg_pre, cudaStream_t stream);

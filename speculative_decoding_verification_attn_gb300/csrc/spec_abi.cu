@@ -32,7 +32,8 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(SPEC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opt_path{0}, g_opt_ctas{0}, g_opt_validate{0}, g_opt_simt_chunk{0};
+std::atomic<int64_t> g_opt_path{0}, g_opt_ctas{0}, g_opt_validate{0}, g_opt_simt_chunk{0},
+    g_opt_split{0};
 
 // Per-device workspace: [error word | acceptance tickets | segment counters |
 // scratch].  The header is zeroed at allocation; tickets and counters are
@@ -139,7 +140,8 @@ const char* spec_last_error(void) { return g_err.c_str(); }
 int spec_set_option(int32_t option, int64_t value) {
     switch (option) {
     case SPEC_OPT_ATTN_PATH:
-        if (value < 0 || value > 3) return fail(SPEC_ERR_INVALID, "attn path must be 0, 1, 2 or 3");
+        if (value < 0 || value > 4)
+            return fail(SPEC_ERR_INVALID, "attn path must be 0, 1, 2, 3 or 4");
         g_opt_path = value;
         return SPEC_OK;
     case SPEC_OPT_NUM_CTAS:
@@ -152,6 +154,10 @@ int spec_set_option(int32_t option, int64_t value) {
     case SPEC_OPT_SIMT_CHUNK:
         if (value < 0 || value > (1 << 30)) return fail(SPEC_ERR_INVALID, "chunk out of range");
         g_opt_simt_chunk = value;
+        return SPEC_OK;
+    case SPEC_OPT_SPLIT_WEIGHT:
+        if (value < 0 || value > 257) return fail(SPEC_ERR_INVALID, "split weight out of range");
+        g_opt_split = value;
         return SPEC_OK;
     default:
         return fail(SPEC_ERR_INVALID, "unknown option %d", option);
@@ -207,24 +213,29 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
     a.out = out; a.lse = lse;
     a.dev_err = nullptr; a.seg_counters = nullptr;
     a.tree_mask = tree_mask;
+    const int64_t split_opt = g_opt_split.load();
+    a.split_alpha = split_opt > 0 ? (int32_t)(split_opt - 1) : -1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    // kernels: 1 SIMT, 2 tcgen05, 3 warp MMA; automatic = warp MMA for <= 16
-    // query rows per kv-head, tcgen05 above, SIMT for everything else
+    // kernels: 1 SIMT (chunked), 2 tcgen05, 3 warp MMA, 4 single-pass SIMT;
+    // automatic = warp MMA for <= 16 query rows per kv-head, tcgen05 above,
+    // and for every other shape the single-pass SIMT kernel when a whole
+    // sequence fits its shared memory, else the chunked one
     const int64_t path = g_opt_path.load();
     const bool tc_ok = specv::tc_supported(a), mma_ok = specv::mma_supported(a);
+    const bool small_ok = specv::small_attn_max_keys(a) > 0;
     int kernel;
     if (path == 1) kernel = 1;
-    else if (path == 2 || path == 3) {
-        if ((path == 2 && !tc_ok) || (path == 3 && !mma_ok))
+    else if (path >= 2) {
+        if ((path == 2 && !tc_ok) || (path == 3 && !mma_ok) || (path == 4 && !small_ok))
             return fail(SPEC_ERR_UNSUPPORTED, "forced attention kernel %d does not support this "
                         "shape/dtype", (int)path);
         kernel = (int)path;
-    } else kernel = mma_ok ? 3 : tc_ok ? 2 : 1;
+    } else kernel = mma_ok ? 3 : tc_ok ? 2 : small_ok ? 4 : 1;
     if (kernel == 3 && (int64_t)batch * num_kv_heads > kMaxCounters)
         return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads > %d for the warp-MMA kernel",
                     kMaxCounters);
-    const bool use_tc = kernel != 1;
+    const bool use_tc = kernel == 2 || kernel == 3;
 
     Workspace* ws = nullptr;
     int rc = get_workspace(0, &ws);
@@ -244,6 +255,10 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
         e = kernel == 3 ? specv::launch_attn_mma(a, ctas, static_cast<char*>(ws->base) + kHeader, st)
                         : specv::launch_attn_tc(a, ctas, static_cast<char*>(ws->base) + kHeader, st);
         if (e != cudaSuccess) return cuda_fail(e, "verify_attn (tensor-core) launch");
+    } else if (kernel == 4) {
+        a.dev_err = static_cast<int*>(ws->base);
+        e = specv::launch_attn_small(a, st);
+        if (e != cudaSuccess) return cuda_fail(e, "verify_attn (single-pass SIMT) launch");
     } else {
         const specv::SimtPlan p = specv::simt_plan(a, ws->sms, (int)g_opt_simt_chunk.load());
         const int64_t gy = (int64_t)batch * num_kv_heads * p.row_groups;

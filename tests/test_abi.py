@@ -165,11 +165,17 @@ def test_codec_decode_rejects_unaligned(lib):
 
 
 def test_options(lib):
-    assert lib.spec_set_option(0, 4) == -1
+    assert lib.spec_set_option(0, 5) == -1
+    assert lib.spec_set_option(0, 4) == 0
     assert lib.spec_set_option(0, 3) == 0
     assert lib.spec_set_option(99, 0) == -1
     assert lib.spec_set_option(0, 0) == 0
     assert lib.spec_set_option(1, 0) == 0
+    # split weight: 0 = each kernel's default, 1..257 = that many tiles + 1
+    assert lib.spec_set_option(4, 258) == -1
+    assert lib.spec_set_option(4, -1) == -1
+    assert lib.spec_set_option(4, 7) == 0
+    assert lib.spec_set_option(4, 0) == 0
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -27,7 +27,7 @@ def _lib():
     from speculative_decoding_verification_attn_gb300 import build
     build.build()
     binding.load()
-    for opt in range(4):
+    for opt in range(5):
         binding.spec_set_option(opt, 0)
 
 

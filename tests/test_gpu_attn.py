@@ -31,10 +31,10 @@ def _defaults():
     from speculative_decoding_verification_attn_gb300 import build
     build.build()
     binding.load()
-    for opt in range(4):
+    for opt in range(5):
         binding.spec_set_option(opt, 0)
     yield
-    for opt in range(4):
+    for opt in range(5):
         binding.spec_set_option(opt, 0)
 
 
@@ -75,6 +75,26 @@ def test_tensor_core_stream_k_splits(oracle_mod, ctas, heads):
     binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
     binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
     check_attn_full(oracle_mod, inp, "ctas=%d heads=%s" % (ctas, heads))
+
+
+# the split of the tile list over the persistent CTAs charges every segment a
+# number of tiles for its fixed work (option value = tiles + 1; 1: the equal
+# split): ranges then start and end at other places, with more or fewer
+# pieces per segment and empty ranges when the charge dominates
+@pytest.mark.parametrize("weight", [1, 2, 14, 65])
+@pytest.mark.parametrize("path,kw", [
+    (2, dict(num_q_heads=28, num_kv_heads=4, num_draft=12)),            # tcgen05, 84 rows
+    (2, dict(num_q_heads=16, num_kv_heads=2, num_draft=6)),             # tcgen05, copies
+    (2, dict(num_q_heads=32, num_kv_heads=4, num_draft=8, kv_dtype="i8")),
+    (3, dict(num_q_heads=16, num_kv_heads=4, num_draft=4)),             # warp-MMA
+], ids=["tc84", "tc48", "tc_i8", "mma16"])
+@pytest.mark.parametrize("ctas", [5, 37, 152])
+def test_split_weights(oracle_mod, weight, path, kw, ctas):
+    inp = make_inputs(small_spec(batch=6, ctx=(0, 1500), **kw), seed=34)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, path)
+    binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
+    binding.spec_set_option(binding.SPEC_OPT_SPLIT_WEIGHT, weight)
+    check_attn_full(oracle_mod, inp, "path %d weight %d ctas %d" % (path, weight, ctas))
 
 
 SMALL_I8 = [
@@ -159,6 +179,37 @@ def test_simt_small(oracle_mod, kw, chunk):
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_tiny_fp32_workload(oracle_mod, seed):
     check_attn_full(oracle_mod, make_inputs("tiny_fp32", seed=seed), "tiny_fp32")
+
+
+# single-pass SIMT kernel: whole sequences in shared memory, one launch
+SINGLE_PASS = [
+    dict(q_dtype="f32", kv_dtype="f32", head_dim=64),
+    dict(q_dtype="f32", kv_dtype="f32", head_dim=64, batch=1, num_q_heads=2, num_kv_heads=2,
+         ctx=[128], num_draft=4),
+    dict(ctx=(0, 150)),                                                       # bf16
+    dict(kv_dtype="i8", num_q_heads=16, num_kv_heads=2, num_draft=8, ctx=(0, 110)),  # 64 rows
+    dict(q_dtype="f32", kv_dtype="i8", head_dim=256, num_draft=2, ctx=(0, 60)),
+    dict(q_dtype="bf16", kv_dtype="f32", head_dim=32, page_size=5, ctx=(0, 77)),
+    dict(head_dim=96, page_size=3, ctx=[0, 10, 31]),
+    dict(num_q_heads=4, num_kv_heads=2, num_draft=64, ctx=(0, 60)),          # 128 rows: 2 groups
+    dict(batch=300, num_q_heads=4, num_kv_heads=4, num_draft=3, ctx=(0, 40)),
+]
+
+
+@pytest.mark.parametrize("kw", SINGLE_PASS, ids=[str(i) for i in range(len(SINGLE_PASS))])
+def test_single_pass_simt(oracle_mod, kw):
+    inp = make_inputs(small_spec(**kw), seed=35)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 4)
+    check_attn_full(oracle_mod, inp, "single pass %s" % kw)
+
+
+def test_single_pass_refuses_long_tables():
+    # a block table longer than the kernel's shared memory holds: forced
+    # single pass is refused, the automatic choice runs the chunked kernel
+    inp = make_inputs(small_spec(q_dtype="f32", kv_dtype="f32", batch=1, ctx=[5000]), seed=36)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 4)
+    with pytest.raises(binding.SpecError, match="does not support"):
+        gpu_attn(inp)
 
 
 def test_page_size_8_runs_on_simt(oracle_mod):

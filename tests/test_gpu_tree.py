@@ -27,10 +27,10 @@ def _defaults():
     from speculative_decoding_verification_attn_gb300 import build
     build.build()
     binding.load()
-    for opt in range(4):
+    for opt in range(5):
         binding.spec_set_option(opt, 0)
     yield
-    for opt in range(4):
+    for opt in range(5):
         binding.spec_set_option(opt, 0)
 
 
@@ -63,6 +63,8 @@ CASES = [  # (attention path, spec)
     (2, dict(num_q_heads=16, num_kv_heads=2, num_draft=8, kv_dtype="i8")),    # INT8 tcgen05
     (1, dict(num_q_heads=8, num_kv_heads=2, num_draft=6)),                     # SIMT
     (1, dict(q_dtype="f32", kv_dtype="f32", head_dim=64, num_draft=5)),        # SIMT fp32
+    (4, dict(q_dtype="f32", kv_dtype="f32", head_dim=64, num_draft=5)),        # single pass
+    (4, dict(num_q_heads=2, num_kv_heads=2, num_draft=64, ctx=(0, 40))),      # single pass, k = 64
 ]
 
 
@@ -79,9 +81,11 @@ def test_tree_attention_matches_oracle(oracle_mod, path, kw, width):
     assert binding.spec_device_error() == 0
 
 
-@pytest.mark.parametrize("path", [0, 1, 2, 3])
+@pytest.mark.parametrize("path", [0, 1, 2, 3, 4])
 def test_chain_mask_reproduces_causal(path):
-    inp = make_inputs(small_spec(num_q_heads=8, num_kv_heads=2, num_draft=4, ctx=(0, 300)), seed=73)
+    # (the single-pass kernel holds whole sequences: shorter contexts there)
+    ctx = (0, 100) if path == 4 else (0, 300)
+    inp = make_inputs(small_spec(num_q_heads=8, num_kv_heads=2, num_draft=4, ctx=ctx), seed=73)
     chain = np.tile(np.arange(-1, 3, dtype=np.int32), (inp.spec.batch, 1))
     binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, path)
     t = binding.inputs_to_torch(inp)
