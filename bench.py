@@ -88,7 +88,8 @@ def measured_peaks():
 # sources whose change makes the committed attention / acceptance counters stale:
 # the kernels of the step and the device helpers they include (the ABI's other
 # entry points and their kernels do not run in the step)
-STEP_SOURCES = ("attn_tc.cu", "attn_mma.cu", "attn_simt.cu", "accept.cu", "common.cuh")
+STEP_SOURCES = ("attn_tc.cu", "attn_mma.cu", "attn_simt.cu", "attn_small.cu", "accept.cu",
+                "common.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -565,6 +566,9 @@ def run_gpu(args, inp, world, rank, local):
     }
     if rejection:
         line["config"]["accept"] = "rejection sampling (T = 1, SplitMix64 draws, fresh seed per step)"
+    if args.num_ctas or args.split_weight:
+        line["config"]["num_ctas"] = args.num_ctas
+        line["config"]["split_weight"] = args.split_weight
     if rank == 0 and not args.no_cpu_baseline and not rejection:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
     if rank == 0:
@@ -644,6 +648,15 @@ def launches_per_step(inp) -> int:
     return (1 if warp_mma else 2) + 1
 
 
+def workload_spec(args):
+    """The named workload, with the sweep overrides applied."""
+    import dataclasses
+    spec = WORKLOADS[args.workload]
+    if args.ctx is not None:
+        spec = dataclasses.replace(spec, ctx=int(args.ctx), name="%s@ctx%d" % (spec.name, args.ctx))
+    return spec
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -660,19 +673,30 @@ def main(argv=None):
     ap.add_argument("--codec", action="store_true",
                     help="time the delta + run-length page codec on the workload's INT8 cache "
                          "instead of the step")
+    ap.add_argument("--ctx", type=int, default=None,
+                    help="sweeps: every sequence's cached context set to this length")
+    ap.add_argument("--num-ctas", type=int, default=0,
+                    help="sweeps: persistent CTAs of the tensor-core kernels (0 = one per SM)")
+    ap.add_argument("--split-weight", type=int, default=0,
+                    help="sweeps: SPEC_OPT_SPLIT_WEIGHT (0 = the kernels' default)")
     args = ap.parse_args(argv)
 
     world, rank, local = dist_env()
     if args.impl == "reference":
         if rank == 0:
-            run_reference(args, make_inputs(args.workload, args.seed, canary=False), world, rank)
+            run_reference(args, make_inputs(workload_spec(args), args.seed, canary=False), world,
+                          rank)
         return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
     import __graft_entry__
     __graft_entry__.build()
-    inp = make_inputs(args.workload, args.seed, canary=False)
+    inp = make_inputs(workload_spec(args), args.seed, canary=False)
+    if args.num_ctas or args.split_weight:
+        from speculative_decoding_verification_attn_gb300 import binding
+        binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, args.num_ctas)
+        binding.spec_set_option(binding.SPEC_OPT_SPLIT_WEIGHT, args.split_weight)
     if args.codec:
         if rank == 0:
             run_codec(args, inp)

@@ -56,8 +56,20 @@ enum {
     SPEC_DTYPE_F32 = 0,
     SPEC_DTYPE_BF16 = 1,
     SPEC_DTYPE_F16 = 2, /* scales only */
-    SPEC_DTYPE_I8 = 3
+    SPEC_DTYPE_I8 = 3,
+    SPEC_DTYPE_I32 = 4  /* tables, lengths and token ids (descriptor form) */
 };
+
+/* A tensor described by itself (the descriptor form of the two hot-path
+ * calls): device pointer, element type, rank (<= 4), shape and strides, both
+ * in elements, row-major order of dimensions.  The caller owns `data`. */
+typedef struct {
+    void *data;
+    int32_t dtype;
+    int32_t ndim;
+    int64_t shape[4];
+    int64_t stride[4];
+} spec_tensor_t;
 
 /* Status codes. */
 enum {
@@ -166,6 +178,35 @@ SPEC_API int spec_verify_attn(const void *q, const void *k_cache, const void *v_
 SPEC_API int spec_accept_greedy(const void *logits, int32_t logits_dtype, const int32_t *draft_tokens,
                        int32_t batch, int32_t num_draft, int64_t vocab,
                        int32_t *accepted_len, int32_t *next_token, void *stream);
+
+/*
+ * Descriptor form of spec_verify_attn and spec_accept_greedy.  Same
+ * operations, results, limits and stream behaviour; every tensor comes as a
+ * spec_tensor_t and the sizes are read from the descriptors:
+ *   q [B, num_draft, Hq, D] (F32 | BF16), k_cache / v_cache [NP, Hkv, P, D]
+ *   (F32 | BF16 | I8, same type), k_scale / v_scale [NP, Hkv, P] F16 (I8
+ *   cache only, else ignored), block_table [B, max_pages] I32, ctx_lens [B]
+ *   I32, out [B, num_draft, Hq, D] in q's type, lse [B, num_draft, Hq] F32
+ *   or NULL;
+ *   logits [B, num_draft + 1, V] (F32 | BF16), draft_tokens [B, num_draft]
+ *   I32, accepted_len / next_token [B] I32.
+ * Errors: SPEC_ERR_INVALID for a null descriptor, a wrong rank, element
+ * type or size, or a q / cache / out / logits pointer not 16-byte aligned;
+ * SPEC_ERR_UNSUPPORTED for strides other than dense row-major (the kernels
+ * read dense tensors); then whatever the flat call returns.  Nothing is
+ * enqueued on an error.
+ */
+SPEC_API int spec_verify_attn_tensors(const spec_tensor_t *q, const spec_tensor_t *k_cache,
+                                      const spec_tensor_t *v_cache, const spec_tensor_t *k_scale,
+                                      const spec_tensor_t *v_scale,
+                                      const spec_tensor_t *block_table,
+                                      const spec_tensor_t *ctx_lens, int32_t num_draft,
+                                      float scale, spec_tensor_t *out, spec_tensor_t *lse,
+                                      void *stream);
+SPEC_API int spec_accept_greedy_tensors(const spec_tensor_t *logits,
+                                        const spec_tensor_t *draft_tokens, int32_t num_draft,
+                                        spec_tensor_t *accepted_len, spec_tensor_t *next_token,
+                                        void *stream);
 
 /*
  * Verification attention over a tree of drafts (token trees verified in one

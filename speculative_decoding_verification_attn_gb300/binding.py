@@ -17,7 +17,7 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
 
-SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_F16, SPEC_DTYPE_I8 = 0, 1, 2, 3
+SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_F16, SPEC_DTYPE_I8, SPEC_DTYPE_I32 = 0, 1, 2, 3, 4
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_OPT_ATTN_PATH, SPEC_OPT_NUM_CTAS, SPEC_OPT_VALIDATE, SPEC_OPT_SIMT_CHUNK = 0, 1, 2, 3
 SPEC_OPT_SPLIT_WEIGHT = 4
@@ -27,13 +27,37 @@ SPEC_DEVERR_CODEC = 32
 
 # every symbol the public header declares
 EXPORTED = ["spec_version", "spec_last_error", "spec_set_option", "spec_verify_attn",
-            "spec_accept_greedy", "spec_accept_greedy_noalloc", "spec_accept_rejection",
+            "spec_accept_greedy", "spec_verify_attn_tensors", "spec_accept_greedy_tensors",
+            "spec_accept_greedy_noalloc", "spec_accept_rejection",
             "spec_kv_append", "spec_commit", "spec_verify_attn_tree", "spec_accept_tree",
             "spec_codec_encode", "spec_codec_decode", "spec_device_error", "spec_release"]
 SPEC_NOALLOC_MAX_PARTIALS, SPEC_NOALLOC_MAX_BATCH = 65536, 4096
 
 _TORCH_DT = {torch.float32: SPEC_DTYPE_F32, torch.bfloat16: SPEC_DTYPE_BF16,
-             torch.float16: SPEC_DTYPE_F16, torch.int8: SPEC_DTYPE_I8}
+             torch.float16: SPEC_DTYPE_F16, torch.int8: SPEC_DTYPE_I8,
+             torch.int32: SPEC_DTYPE_I32}
+
+
+class SpecTensor(ctypes.Structure):
+    """spec_tensor_t: data pointer, element type, rank, shape, strides (elements)."""
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+def tensor_desc(t: Optional[torch.Tensor]):
+    """The spec_tensor_t of a torch tensor (any strides; None stays None)."""
+    if t is None:
+        return None
+    if t.dim() > 4:
+        raise ValueError("descriptors hold at most 4 dimensions")
+    d = SpecTensor()
+    d.data = t.data_ptr()
+    d.dtype = _TORCH_DT[t.dtype]
+    d.ndim = t.dim()
+    for i, (n, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = n
+        d.stride[i] = st
+    return d
 
 _lib = None
 
@@ -85,6 +109,11 @@ def _open(path: str):
     lib.spec_verify_attn_tree.restype = ctypes.c_int
     lib.spec_accept_tree.argtypes = [P, i32, P, P, i32, i32, i64, P, P, P, P]
     lib.spec_accept_tree.restype = ctypes.c_int
+    T = ctypes.POINTER(SpecTensor)
+    lib.spec_verify_attn_tensors.argtypes = [T, T, T, T, T, T, T, i32, ctypes.c_float, T, T, P]
+    lib.spec_verify_attn_tensors.restype = ctypes.c_int
+    lib.spec_accept_greedy_tensors.argtypes = [T, T, i32, T, T, P]
+    lib.spec_accept_greedy_tensors.restype = ctypes.c_int
     lib.spec_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.spec_device_error.restype = ctypes.c_int
     lib.spec_release.restype = ctypes.c_int
@@ -142,6 +171,30 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, ctx_lens, num_draft: int,
         _TORCH_DT[k_cache.dtype], float(scale), _ptr(out), _ptr(lse), _stream(stream)))
 
 
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def spec_verify_attn_tensors(q, k_cache, v_cache, block_table, ctx_lens, num_draft: int,
+                             scale: float, out, lse=None, k_scale=None, v_scale=None,
+                             stream=None) -> None:
+    """spec_verify_attn through the descriptor form (sizes and strides are
+    read from the tensors; the library checks them)."""
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, k_scale, v_scale, block_table,
+                                      ctx_lens, out, lse)]
+    _check(load().spec_verify_attn_tensors(*[_ref(d) for d in descs[:7]], int(num_draft),
+                                           float(scale), _ref(descs[7]), _ref(descs[8]),
+                                           _stream(stream)))
+
+
+def spec_accept_greedy_tensors(logits, draft_tokens, num_draft: int, accepted_len, next_token,
+                               stream=None) -> None:
+    """spec_accept_greedy through the descriptor form."""
+    descs = [tensor_desc(t) for t in (logits, draft_tokens, accepted_len, next_token)]
+    _check(load().spec_accept_greedy_tensors(_ref(descs[0]), _ref(descs[1]), int(num_draft),
+                                             _ref(descs[2]), _ref(descs[3]), _stream(stream)))
+
+
 def spec_verify_attn_tree(q, k_cache, v_cache, block_table, ctx_lens, tree_mask, num_draft: int,
                           scale: float, out, lse=None, k_scale=None, v_scale=None,
                           stream=None) -> None:
@@ -187,9 +240,10 @@ def spec_accept_greedy_noalloc(logits, draft_tokens, num_draft: int, accepted_le
                                stream=None) -> None:
     """spec_accept_greedy without any device allocation (fixed library scratch).
 
-    For callers that cannot allocate device memory, e.g. while recording a
-    CUDA graph.  Sizes are limited (see include/spec_verify.h); calls that
-    overlap on the GPU share the scratch and race.
+    For callers that cannot allocate device memory, e.g. a serving loop whose
+    GPU memory is reserved up front by its own allocator.  Sizes are limited
+    (see include/spec_verify.h); calls that overlap on the GPU share the
+    scratch and race.
     """
     B, k1, V = logits.shape
     if k1 != num_draft + 1 or tuple(draft_tokens.shape) != (B, num_draft):

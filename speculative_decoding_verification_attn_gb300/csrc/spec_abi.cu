@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -512,6 +513,115 @@ int spec_release(void) {
         g_ws[dev].bytes = 0;
     }
     return SPEC_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- tensor-descriptor form
+//
+// The same two calls taking self-describing tensors (pointer, element type,
+// rank, shape, strides in elements): the descriptors are checked against
+// one another and forwarded to the flat entry points above.  The kernels
+// read dense row-major tensors, so any other stride is refused (-2).
+
+namespace {
+
+// Dense row-major strides of `t` (in elements) match the given ones?
+bool dense(const spec_tensor_t& t) {
+    int64_t s = 1;
+    for (int d = t.ndim - 1; d >= 0; --d) {
+        if (t.shape[d] != 1 && t.stride[d] != s) return false;
+        s *= t.shape[d];
+    }
+    return true;
+}
+
+// Checks rank, element type, shape (-1 = any), alignment and density of a
+// descriptor; returns 0 or sets the error.
+int check_tensor(const spec_tensor_t* t, const char* name, int ndim, std::initializer_list<int32_t> dtypes,
+                 std::initializer_list<int64_t> shape, bool need16 = false) {
+    if (!t) return fail(SPEC_ERR_INVALID, "%s: null descriptor", name);
+    if (t->ndim != ndim) return fail(SPEC_ERR_INVALID, "%s: rank %d, expected %d", name, t->ndim, ndim);
+    bool ok = false;
+    for (int32_t dt : dtypes) ok = ok || t->dtype == dt;
+    if (!ok) return fail(SPEC_ERR_INVALID, "%s: unsupported element type %d", name, t->dtype);
+    int d = 0;
+    for (int64_t want : shape) {
+        if (t->shape[d] < 0 || (want >= 0 && t->shape[d] != want))
+            return fail(SPEC_ERR_INVALID, "%s: dimension %d is %lld, expected %lld", name, d,
+                        (long long)t->shape[d], (long long)want);
+        ++d;
+    }
+    if (need16 && (reinterpret_cast<uintptr_t>(t->data) & 15))
+        return fail(SPEC_ERR_INVALID, "%s: data must be 16-byte aligned", name);
+    if (!dense(*t))
+        return fail(SPEC_ERR_UNSUPPORTED, "%s: only dense row-major strides are supported", name);
+    return SPEC_OK;
+}
+
+bool fits_i32(int64_t v) { return v >= 0 && v < (1LL << 31); }
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_attn_tensors(const spec_tensor_t* q, const spec_tensor_t* k_cache,
+                             const spec_tensor_t* v_cache, const spec_tensor_t* k_scale,
+                             const spec_tensor_t* v_scale, const spec_tensor_t* block_table,
+                             const spec_tensor_t* ctx_lens, int32_t num_draft, float scale,
+                             spec_tensor_t* out, spec_tensor_t* lse, void* stream) {
+    g_err.clear();
+    int rc = check_tensor(q, "q", 4, {SPEC_DTYPE_F32, SPEC_DTYPE_BF16}, {-1, num_draft, -1, -1}, true);
+    if (rc) return rc;
+    const int64_t B = q->shape[0], Hq = q->shape[2], D = q->shape[3];
+    rc = check_tensor(k_cache, "k_cache", 4, {SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_I8},
+                      {-1, -1, -1, D}, true);
+    if (rc) return rc;
+    const int64_t NP = k_cache->shape[0], Hkv = k_cache->shape[1], P = k_cache->shape[2];
+    rc = check_tensor(v_cache, "v_cache", 4, {k_cache->dtype}, {NP, Hkv, P, D}, true);
+    if (rc) return rc;
+    const bool i8 = k_cache->dtype == SPEC_DTYPE_I8;
+    if (i8) {
+        rc = check_tensor(k_scale, "k_scale", 3, {SPEC_DTYPE_F16}, {NP, Hkv, P});
+        if (!rc) rc = check_tensor(v_scale, "v_scale", 3, {SPEC_DTYPE_F16}, {NP, Hkv, P});
+        if (rc) return rc;
+    }
+    rc = check_tensor(block_table, "block_table", 2, {SPEC_DTYPE_I32}, {B, -1});
+    if (!rc) rc = check_tensor(ctx_lens, "ctx_lens", 1, {SPEC_DTYPE_I32}, {B});
+    if (!rc) rc = check_tensor(out, "out", 4, {q->dtype}, {B, num_draft, Hq, D}, true);
+    if (!rc && lse) rc = check_tensor(lse, "lse", 3, {SPEC_DTYPE_F32}, {B, num_draft, Hq});
+    if (rc) return rc;
+    const int64_t MP = block_table->shape[1];
+    if (!fits_i32(B) || !fits_i32(Hq) || !fits_i32(D) || !fits_i32(NP) || !fits_i32(Hkv) ||
+        !fits_i32(P) || !fits_i32(MP))
+        return fail(SPEC_ERR_INVALID, "a dimension does not fit int32");
+    return spec_verify_attn(q->data, k_cache->data, v_cache->data, i8 ? k_scale->data : nullptr,
+                            i8 ? v_scale->data : nullptr,
+                            static_cast<const int32_t*>(block_table->data),
+                            static_cast<const int32_t*>(ctx_lens->data), (int32_t)B, num_draft,
+                            (int32_t)Hq, (int32_t)Hkv, (int32_t)D, (int32_t)P, (int32_t)NP,
+                            (int32_t)MP, q->dtype, k_cache->dtype, scale, out->data,
+                            lse ? static_cast<float*>(lse->data) : nullptr, stream);
+}
+
+int spec_accept_greedy_tensors(const spec_tensor_t* logits, const spec_tensor_t* draft_tokens,
+                               int32_t num_draft, spec_tensor_t* accepted_len,
+                               spec_tensor_t* next_token, void* stream) {
+    g_err.clear();
+    int rc = check_tensor(logits, "logits", 3, {SPEC_DTYPE_F32, SPEC_DTYPE_BF16},
+                          {-1, (int64_t)num_draft + 1, -1}, true);
+    if (rc) return rc;
+    const int64_t B = logits->shape[0];
+    rc = check_tensor(draft_tokens, "draft_tokens", 2, {SPEC_DTYPE_I32}, {B, num_draft});
+    if (!rc) rc = check_tensor(accepted_len, "accepted_len", 1, {SPEC_DTYPE_I32}, {B});
+    if (!rc) rc = check_tensor(next_token, "next_token", 1, {SPEC_DTYPE_I32}, {B});
+    if (rc) return rc;
+    if (!fits_i32(B)) return fail(SPEC_ERR_INVALID, "batch does not fit int32");
+    return spec_accept_greedy(logits->data, logits->dtype,
+                              static_cast<const int32_t*>(draft_tokens->data), (int32_t)B,
+                              num_draft, logits->shape[2],
+                              static_cast<int32_t*>(accepted_len->data),
+                              static_cast<int32_t*>(next_token->data), stream);
 }
 
 }  // extern "C"

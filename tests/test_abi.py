@@ -182,3 +182,79 @@ def test_binding_fails_loudly_without_library(tmp_path):
     from speculative_decoding_verification_attn_gb300 import binding
     with pytest.raises(RuntimeError):
         binding._open(str(tmp_path / "missing.so"))
+
+
+# ---- descriptor form (spec_tensor_t): argument checks precede every CUDA call
+
+def _desc(shape, dtype, data=4096, strides=None):
+    from speculative_decoding_verification_attn_gb300 import binding
+    d = binding.SpecTensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    st = strides
+    if st is None:
+        st, acc = [], 1
+        for n in reversed(shape):
+            st.insert(0, acc)
+            acc *= n
+    for i, (n, s) in enumerate(zip(shape, st)):
+        d.shape[i] = n
+        d.stride[i] = s
+    return d
+
+
+def _attn_descs(**over):
+    B, k, Hq, Hkv, D, NP, P, MP = 2, 4, 8, 2, 128, 16, 16, 8
+    d = dict(q=_desc([B, k, Hq, D], 1), kc=_desc([NP, Hkv, P, D], 1), vc=_desc([NP, Hkv, P, D], 1),
+             ks=None, vs=None, bt=_desc([B, MP], 4), ctx=_desc([B], 4),
+             out=_desc([B, k, Hq, D], 1), lse=_desc([B, k, Hq], 0), k=k)
+    d.update(over)
+    return d
+
+
+def _call_attn(lib, d):
+    r = lambda x: None if x is None else ctypes.byref(x)
+    return lib.spec_verify_attn_tensors(r(d["q"]), r(d["kc"]), r(d["vc"]), r(d["ks"]), r(d["vs"]),
+                                        r(d["bt"]), r(d["ctx"]), d["k"], 0.088, r(d["out"]),
+                                        r(d["lse"]), None)
+
+
+@pytest.mark.parametrize("over,code,needle", [
+    (dict(q=_desc([2, 4, 8], 1)), -1, "q: rank"),
+    (dict(q=_desc([2, 4, 8, 128], 3)), -1, "q: unsupported element type"),
+    (dict(k=5), -1, "q: dimension 1"),
+    (dict(kc=_desc([16, 2, 16, 64], 1)), -1, "k_cache: dimension 3"),
+    (dict(vc=_desc([16, 2, 16, 128], 0)), -1, "v_cache: unsupported element type"),
+    (dict(kc=_desc([16, 2, 16, 128], 3), vc=_desc([16, 2, 16, 128], 3)), -1, "k_scale: null"),
+    (dict(bt=_desc([3, 8], 4)), -1, "block_table: dimension 0"),
+    (dict(ctx=_desc([2], 0)), -1, "ctx_lens: unsupported element type"),
+    (dict(out=_desc([2, 4, 8, 128], 0)), -1, "out: unsupported element type"),
+    (dict(lse=_desc([2, 4, 7], 0)), -1, "lse: dimension 2"),
+    (dict(q=_desc([2, 4, 8, 128], 1, data=4098)), -1, "q: data must be 16-byte aligned"),
+    (dict(q=_desc([2, 4, 8, 128], 1, strides=[4096, 1024, 256, 1])), -2, "dense row-major"),
+    (dict(kc=_desc([16, 2, 16, 128], 1, strides=[2, 1, 32, 256])), -2, "dense row-major"),
+])
+def test_attn_descriptors_rejected(lib, over, code, needle):
+    assert _call_attn(lib, _attn_descs(**over)) == code
+    assert needle in lib.spec_last_error().decode()
+
+
+@pytest.mark.parametrize("over,code,needle", [
+    (dict(logits=_desc([2, 4, 1000], 1)), -1, "logits: dimension 1"),
+    (dict(logits=_desc([2, 5, 1000], 3)), -1, "logits: unsupported element type"),
+    (dict(drafts=_desc([2, 3], 4)), -1, "draft_tokens: dimension 1"),
+    (dict(acc=_desc([2], 0)), -1, "accepted_len: unsupported element type"),
+    (dict(nxt=_desc([3], 4)), -1, "next_token: dimension 0"),
+    (dict(logits=_desc([2, 5, 1000], 1, strides=[5000, 1000, 2])), -2, "dense row-major"),
+])
+def test_accept_descriptors_rejected(lib, over, code, needle):
+    d = dict(logits=_desc([2, 5, 1000], 1), drafts=_desc([2, 4], 4), acc=_desc([2], 4),
+             nxt=_desc([2], 4))
+    d.update(over)
+    r = ctypes.byref
+    rc = lib.spec_accept_greedy_tensors(r(d["logits"]), r(d["drafts"]), 4, r(d["acc"]),
+                                        r(d["nxt"]), None)
+    assert rc == code
+    assert needle in lib.spec_last_error().decode()
+

@@ -340,3 +340,33 @@ def test_batch_beyond_tensor_core_limit(oracle_mod):
     out, lse = gpu_attn(inp, t)
     ref_out, ref_lse = oracle_attn(oracle_mod, inp)
     assert_attn_close(out, lse, ref_out, ref_lse, tol_for(inp), "batch 1025")
+
+
+def test_descriptor_form_matches_flat_calls():
+    # spec_verify_attn_tensors / spec_accept_greedy_tensors: same kernels, same
+    # results as the flat calls, bit for bit (bf16 and INT8 caches)
+    for kw in (dict(), dict(kv_dtype="i8", num_q_heads=16, num_kv_heads=2, num_draft=8)):
+        inp = make_inputs(small_spec(**kw), seed=37)
+        t = binding.inputs_to_torch(inp)
+        a = binding.alloc_outputs(inp)
+        b = binding.alloc_outputs(inp)
+        s = inp.spec
+        binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                 t["ctx_lens"], s.num_draft, inp.scale, a["out"], a["lse"],
+                                 t.get("k_scale"), t.get("v_scale"))
+        binding.spec_verify_attn_tensors(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                         t["ctx_lens"], s.num_draft, inp.scale, b["out"], b["lse"],
+                                         t.get("k_scale"), t.get("v_scale"))
+        binding.spec_accept_greedy(t["logits"], t["draft_tokens"], s.num_draft, a["accepted_len"],
+                                   a["next_token"])
+        binding.spec_accept_greedy_tensors(t["logits"], t["draft_tokens"], s.num_draft,
+                                           b["accepted_len"], b["next_token"])
+        torch.cuda.synchronize()
+        for n in ("out", "lse", "accepted_len", "next_token"):
+            assert torch.equal(a[n], b[n]), n
+    # a strided (non-dense) q is refused before anything runs
+    wide = torch.empty(inp.q.shape[:-1] + (2 * s.head_dim,), dtype=t["q"].dtype, device="cuda")
+    with pytest.raises(binding.SpecError, match="dense row-major"):
+        binding.spec_verify_attn_tensors(wide[..., :s.head_dim], t["k_cache"], t["v_cache"],
+                                         t["block_table"], t["ctx_lens"], s.num_draft, inp.scale,
+                                         b["out"], b["lse"], t.get("k_scale"), t.get("v_scale"))
