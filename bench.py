@@ -431,6 +431,26 @@ def run_gpu(args, inp, world, rank, local):
             accept(t, o, j)
             rev[j][2].record(stream)
         torch.cuda.synchronize()
+        # a third and fourth region: the attention calls alone, then the
+        # acceptance calls alone, K each back to back between one event pair
+        # (each kernel's average launch duration in a stream of its own
+        # launches, for the roofline; the per-call events above block the
+        # launch overlap of consecutive kernels and add their own cost)
+        a0, a1, c0, c1 = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        held(2 * args.steps)
+        a0.record(stream)
+        for j in range(args.steps):
+            t, o = sets[j % n_sets], outs[j % n_sets]
+            binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                     t["ctx_lens"], k, scale, o["out"], o["lse"],
+                                     t.get("k_scale"), t.get("v_scale"))
+        a1.record(stream)
+        c0.record(stream)
+        for j in range(args.steps):
+            t, o = sets[j % n_sets], outs[j % n_sets]
+            accept(t, o, j)
+        c1.record(stream)
+        torch.cuda.synchronize()
     clocks = clk.summary()
     value, slowest_step_s = aggregate(units, e0.elapsed_time(e1) / 1e3 / args.steps, world,
                                       device)
@@ -438,17 +458,23 @@ def run_gpu(args, inp, world, rank, local):
     rep_step = np.array([e[0].elapsed_time(e[2]) for e in rev])
     rep_attn = np.array([e[0].elapsed_time(e[1]) for e in rev])
     rep_acc = np.array([e[1].elapsed_time(e[2]) for e in rev])
-    attn_ms, acc_ms = float(rep_attn.mean()), float(rep_acc.mean())
+    attn_ms = a0.elapsed_time(a1) / args.steps
+    acc_ms = c0.elapsed_time(c1) / args.steps
     # goodput: tokens the step gains, sum over sequences of accepted_len + 1
     # (every input set holds the same values, so any set's results serve)
     gained = int((outs[0]["accepted_len"].long() + 1).sum().item())
     accepted_tok_s = gained * world / slowest_step_s
     timing = {"timed_region": "K steps between one event pair (value, ms_per_step)",
               "breakdown_region": "%d steps, an event pair around each call" % reps,
+              "kernel_regions": "K attention calls, then K acceptance calls, back to back "
+                                "between one event pair each (roofline attn_ms / accept_ms)",
               "reps": reps, "step_median_ms": float(np.median(rep_step)),
               "step_mean_ms": float(rep_step.mean()),
-              "attn_median_ms": float(np.median(rep_attn)), "attn_mean_ms": attn_ms,
-              "accept_median_ms": float(np.median(rep_acc)), "accept_mean_ms": acc_ms}
+              "attn_median_ms": float(np.median(rep_attn)),
+              "attn_mean_ms": float(rep_attn.mean()),
+              "accept_median_ms": float(np.median(rep_acc)),
+              "accept_mean_ms": float(rep_acc.mean()),
+              "attn_back_to_back_ms": attn_ms, "accept_back_to_back_ms": acc_ms}
 
     # end to end through the public API: every step's inputs copied from
     # pinned host memory and its results read back, inside the timed region.
@@ -557,7 +583,8 @@ def run_gpu(args, inp, world, rank, local):
         "gpu_launches": args.steps * (launches_per_step(inp) + (1 if rejection else 0)),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "spec_verify_attn (attention + split-KV combine)",
+                     "kernel": "spec_verify_attn (attention + split-KV combine), K calls back "
+                               "to back between one event pair",
                      "peak_source": peak_kind, "attn_ms": attn_ms, "accept_ms": acc_ms,
                      "attn_bytes": nbytes["attn"], "step_bytes": nbytes["total"],
                      "accept_GBps": nbytes["accept"] / (acc_ms / 1e3) / 1e9,
@@ -637,15 +664,28 @@ def run_codec(args, inp):
 
 
 def launches_per_step(inp) -> int:
-    """Kernels one step launches: the warp-MMA attention kernel (bf16, head_dim
-    128, <= 16 query rows per kv-head, page size 16..256) merges its split-KV
-    partials itself; the tcgen05 and SIMT kernels are followed by a combine
-    kernel; plus the acceptance kernel."""
+    """Kernels one step launches (mirrors the library's automatic choice): the
+    warp-MMA attention kernel (bf16, head_dim 128, <= 16 query rows per
+    kv-head, page size 16..256) merges its split-KV partials itself, the
+    tcgen05 kernel (up to 128 rows) is followed by a combine kernel; other
+    shapes run the single-pass SIMT kernel when a whole sequence fits its
+    shared memory (one launch), else the chunked SIMT kernel and its combine;
+    plus the acceptance kernel."""
     s = inp.spec
-    rows = s.num_draft * (s.num_q_heads // s.num_kv_heads)
-    warp_mma = (s.q_dtype == "bf16" and s.kv_dtype == "bf16" and s.head_dim == 128 and rows <= 16
+    G = s.num_q_heads // s.num_kv_heads
+    rows = s.num_draft * G
+    tc_shape = (s.q_dtype == "bf16" and s.kv_dtype in ("bf16", "i8") and s.head_dim == 128
                 and 16 <= s.page_size <= 256 and s.page_size & (s.page_size - 1) == 0)
-    return (1 if warp_mma else 2) + 1
+    if tc_shape and s.kv_dtype == "bf16" and rows <= 16:
+        return 1 + 1
+    if tc_shape and rows <= 128:
+        return 2 + 1
+    lcap = inp.block_table.shape[1] * s.page_size
+    rg = min(rows, 64)
+    floats = lcap * (s.head_dim + 4) + lcap * s.head_dim + (rg * lcap + 3) // 4 * 4 + \
+        rg * s.head_dim + 4 * 512 + rg
+    single = lcap <= 4096 and floats * 4 + (lcap // s.page_size + 2) * 4 <= 200 * 1024
+    return (1 if single else 2) + 1
 
 
 def workload_spec(args):
