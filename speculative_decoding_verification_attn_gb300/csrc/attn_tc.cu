@@ -916,16 +916,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 // K (bf16) / raw stage (INT8): free once Q K^T read it / the
                 // converter warps widened it
                 const int s = it % NL, use = it / NL;
-                if (lane == 0) {
-                    if (use >= 1)
-                        ok = mbar_wait(&bars[Smem::B_RAWFREE + s], (use - 1) & 1, abort_flag,
-                                       a.dev_err);
-                    if (ok)
-                        mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
-                                              KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
-                                                  : (nvalid + 7) / 8 * 2048u);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (use >= 1)
+                    ok = warp_wait(&bars[Smem::B_RAWFREE + s], (use - 1) & 1, abort_flag,
+                                   a.dev_err);
+                if (ok && lane == 0)
+                    mbar_arrive_expect_tx(&bars[Smem::B_KVFULL + s],
+                                          KV8 ? nbox * (2u * BH * D + 2u * BH * 2)
+                                              : (nvalid + 7) / 8 * 2048u);
+                __syncwarp();
                 if (!ok) break;
                 uint8_t* st = sm + Smem::RAW + s * Smem::RAW_STAGE;
                 if constexpr (KV8) {
@@ -961,13 +959,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 // V: 16-key boxes (4 KB) in the layout P V reads, into slot
                 // it % NV, free once P V of tile it - NV has read it
                 const int s = it % NV, use = it / NV;
-                if (lane == 0) {
-                    if (use >= 1)
-                        ok = mbar_wait(&bars[Smem::B_VEMPTY + s], (use - 1) & 1, abort_flag,
-                                       a.dev_err);
-                    if (ok) mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], nbox * 4096u);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (use >= 1)
+                    ok = warp_wait(&bars[Smem::B_VEMPTY + s], (use - 1) & 1, abort_flag,
+                                   a.dev_err);
+                if (ok && lane == 0) mbar_arrive_expect_tx(&bars[Smem::B_VFULL + s], nbox * 4096u);
+                __syncwarp();
                 if (!ok) break;
                 if (lane < nbox) {
                     const int row = (page_of(lane) * Hkv + cur.kvh) * P + (key0 + lane * BH) % P;
@@ -1109,12 +1105,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     if (first && q_issued == pc) {
                         // the previous piece had a single tile: its copy to
                         // TMEM was not yet seen done when its MMAs went out
-                        if (lane == 0) {
-                            ok = mbar_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag,
-                                           a.dev_err);
-                            if (ok) issue_q(cur);
-                        }
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        ok = warp_wait(&bars[Smem::B_QFREE], (pc - 1) & 1, abort_flag, a.dev_err);
+                        if (ok && lane == 0) issue_q(cur);
+                        __syncwarp();
                         q_issued = pc + 1;
                         if (!ok) break;
                     }
@@ -1498,16 +1491,15 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cud
                              smem_bytes<false>(), stream, qmap, kmap, vmap, prm);
     }
     if (e != cudaSuccess) return e;
-    return launch_combine_stream_k(a, num_ctas, prm.part_o, prm.part_lse, prm.seg_rec,
-                                   prm.seg_pre, stream);
+    return launch_combine_stream_k(a, num_ctas, split_alpha(a), prm.part_o, prm.part_lse,
+                                   prm.seg_rec, prm.seg_pre, stream);
 }
 
-cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float* part_o,
-                                    const float* part_lse, const int4* seg_rec,
-                                    const int* seg_pre, cudaStream_t stream) {
+cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, int alpha,
+                                    const float* part_o, const float* part_lse,
+                                    const int4* seg_rec, const int* seg_pre, cudaStream_t stream) {
     if (num_ctas < 2) return cudaSuccess;  // one CTA splits nothing
     const int R = a.k * (a.Hq / a.Hkv);
-    const int alpha = split_alpha(a);
     const int64_t segs = (int64_t)a.B * a.Hkv;
     if (segs <= num_ctas - 1) {
         dim3 cgrid((unsigned)segs, (R + 7) / 8);

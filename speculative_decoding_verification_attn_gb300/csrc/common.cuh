@@ -232,6 +232,15 @@ __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -554,12 +563,28 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the whole warp gets its verdict.
+// Warp-uniform bounded wait (the whole warp calls it): every lane polls in
+// step and every decision is a warp vote, so the warp leaves converged.  A
+// wait spun by one lane while the others park leaves the warp split, and the
+// tcgen05.mma issued right after it (elect.sync) then issues several times
+// slower for the rest of the batch.  Gives up like mbar_wait.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* dev_err) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, dev_err);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    constexpr uint32_t kAll = 0xffffffffu;
+    if (__all_sync(kAll, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (__all_sync(kAll, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(kAll, *abort_flag != 0)) return false;
+        if (__any_sync(kAll, globaltimer_ns() - t0 > kWaitLimitNs)) {
+            if ((threadIdx.x & 31) == 0) {
+                *abort_flag = 1;
+                raise_device_error(dev_err, SPEC_DEVERR_TIMEOUT);
+            }
+            __syncwarp();
+            return false;
+        }
+    }
 }
 
 // Bounded wait used only while draining after an abort (ignores the flag).

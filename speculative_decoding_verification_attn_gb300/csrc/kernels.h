@@ -66,14 +66,19 @@ bool tc_supported(const AttnArgs& a);
 size_t tc_workspace_bytes(const AttnArgs& a, int num_ctas);
 cudaError_t launch_attn_tc(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream);
 
-// Merge of the split-KV partials written by the tensor-core kernel (64-key
-// tiles over `num_ctas` persistent CTAs, split by TileSplit with the kernel's
-// per-segment charge; partial slots [2*C][128][D]; per CTA boundary the
+// Merge of the split-KV partials written by a tensor-core kernel (its tiles
+// over `num_ctas` persistent CTAs, split by TileSplit with `alpha` tiles
+// charged per segment; partial slots [2*C][128][D]; per CTA boundary the
 // segment record {b, kv-head, tile-in-segment, tiles} and the CTA's first
-// tile; per sequence the tile prefix).
-cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, const float* part_o,
-                                    const float* part_lse, const int4* seg_rec,
-                                    const int* seg_pre, cudaStream_t stream);
+// tile; per sequence the tile prefix, in the kernel's tile units).
+cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, int alpha,
+                                    const float* part_o, const float* part_lse,
+                                    const int4* seg_rec, const int* seg_pre, cudaStream_t stream);
+
+// ---- tensor-core kernel with 128-key tiles: bf16, head_dim 128, 65..128
+// query rows per kv-head (two softmax sets); workspace as tc_workspace_bytes ----
+bool tc2_supported(const AttnArgs& a);
+cudaError_t launch_attn_tc2(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream);
 
 // ---- warp-MMA kernel for k*G <= 16 query rows (mma.sync m16n8k16, TMA pages) ----
 bool mma_supported(const AttnArgs& a);

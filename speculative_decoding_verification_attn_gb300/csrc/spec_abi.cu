@@ -141,8 +141,8 @@ const char* spec_last_error(void) { return g_err.c_str(); }
 int spec_set_option(int32_t option, int64_t value) {
     switch (option) {
     case SPEC_OPT_ATTN_PATH:
-        if (value < 0 || value > 4)
-            return fail(SPEC_ERR_INVALID, "attn path must be 0, 1, 2, 3 or 4");
+        if (value < 0 || value > 5)
+            return fail(SPEC_ERR_INVALID, "attn path must be 0, 1, 2, 3, 4 or 5");
         g_opt_path = value;
         return SPEC_OK;
     case SPEC_OPT_NUM_CTAS:
@@ -218,17 +218,20 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
     a.split_alpha = split_opt > 0 ? (int32_t)(split_opt - 1) : -1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    // kernels: 1 SIMT (chunked), 2 tcgen05, 3 warp MMA, 4 single-pass SIMT;
-    // automatic = warp MMA for <= 16 query rows per kv-head, tcgen05 above,
-    // and for every other shape the single-pass SIMT kernel when a whole
-    // sequence fits its shared memory, else the chunked one
+    // kernels: 1 SIMT (chunked), 2 tcgen05 (64-key tiles), 3 warp MMA,
+    // 4 single-pass SIMT, 5 tcgen05 (128-key tiles); automatic = warp MMA for
+    // <= 16 query rows per kv-head, tcgen05 (64-key tiles) above, and for
+    // every other shape the single-pass SIMT kernel when a whole sequence
+    // fits its shared memory, else the chunked one
     const int64_t path = g_opt_path.load();
     const bool tc_ok = specv::tc_supported(a), mma_ok = specv::mma_supported(a);
+    const bool tc2_ok = specv::tc2_supported(a);
     const bool small_ok = specv::small_attn_max_keys(a) > 0;
     int kernel;
     if (path == 1) kernel = 1;
     else if (path >= 2) {
-        if ((path == 2 && !tc_ok) || (path == 3 && !mma_ok) || (path == 4 && !small_ok))
+        if ((path == 2 && !tc_ok) || (path == 3 && !mma_ok) || (path == 4 && !small_ok) ||
+            (path == 5 && !tc2_ok))
             return fail(SPEC_ERR_UNSUPPORTED, "forced attention kernel %d does not support this "
                         "shape/dtype", (int)path);
         kernel = (int)path;
@@ -236,7 +239,7 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
     if (kernel == 3 && (int64_t)batch * num_kv_heads > kMaxCounters)
         return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads > %d for the warp-MMA kernel",
                     kMaxCounters);
-    const bool use_tc = kernel == 2 || kernel == 3;
+    const bool use_tc = kernel == 2 || kernel == 3 || kernel == 5;
 
     Workspace* ws = nullptr;
     int rc = get_workspace(0, &ws);
@@ -253,8 +256,10 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
         if (rc) return rc;
         a.dev_err = static_cast<int*>(ws->base);
         a.seg_counters = reinterpret_cast<int*>(static_cast<char*>(ws->base) + kCountersOff);
-        e = kernel == 3 ? specv::launch_attn_mma(a, ctas, static_cast<char*>(ws->base) + kHeader, st)
-                        : specv::launch_attn_tc(a, ctas, static_cast<char*>(ws->base) + kHeader, st);
+        void* wsp = static_cast<char*>(ws->base) + kHeader;
+        e = kernel == 3   ? specv::launch_attn_mma(a, ctas, wsp, st)
+            : kernel == 5 ? specv::launch_attn_tc2(a, ctas, wsp, st)
+                          : specv::launch_attn_tc(a, ctas, wsp, st);
         if (e != cudaSuccess) return cuda_fail(e, "verify_attn (tensor-core) launch");
     } else if (kernel == 4) {
         a.dev_err = static_cast<int*>(ws->base);

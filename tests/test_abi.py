@@ -165,7 +165,8 @@ def test_codec_decode_rejects_unaligned(lib):
 
 
 def test_options(lib):
-    assert lib.spec_set_option(0, 5) == -1
+    assert lib.spec_set_option(0, 6) == -1
+    assert lib.spec_set_option(0, 5) == 0
     assert lib.spec_set_option(0, 4) == 0
     assert lib.spec_set_option(0, 3) == 0
     assert lib.spec_set_option(99, 0) == -1
