@@ -88,8 +88,8 @@ def measured_peaks():
 # sources whose change makes the committed attention / acceptance counters stale:
 # the kernels of the step and the device helpers they include (the ABI's other
 # entry points and their kernels do not run in the step)
-STEP_SOURCES = ("attn_tc.cu", "attn_mma.cu", "attn_simt.cu", "attn_small.cu", "accept.cu",
-                "common.cuh")
+STEP_SOURCES = ("attn_tc.cu", "attn_tc2.cu", "attn_mma.cu", "attn_simt.cu", "attn_small.cu",
+                "accept.cu", "common.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -667,7 +667,8 @@ def launches_per_step(inp) -> int:
     """Kernels one step launches (mirrors the library's automatic choice): the
     warp-MMA attention kernel (bf16, head_dim 128, <= 16 query rows per
     kv-head, page size 16..256) merges its split-KV partials itself, the
-    tcgen05 kernel (up to 128 rows) is followed by a combine kernel; other
+    tcgen05 kernels (128-key tiles for a bf16 cache and 65..128 rows, 64-key
+    tiles otherwise, up to 128 rows) are followed by a combine kernel; other
     shapes run the single-pass SIMT kernel when a whole sequence fits its
     shared memory (one launch), else the chunked SIMT kernel and its combine;
     plus the acceptance kernel."""

@@ -20,8 +20,8 @@
 //    the set's S buffer, which therefore stays busy until P V has read it.
 //  * Warps: 0-3 and 8-11 two softmax sets taking alternate tiles, each with
 //    its own S buffer, running max, row sum and O; 4 Q loads and Q K^T
-//    issue; 5-6 TMA producers (tile it by warp 5 + it % 2, which owns K and
-//    V slot it % 2); 7 P V issue.
+//    issue; 5 and 6 TMA producers of K and of V (tile it into slot it % 2
+//    of each ring); 7 P V issue.
 //  * The softmax of a tile reads S in two 64-column halves: the row maximum
 //    of both first, then p = 2^(s - m) of each half, packed to bf16 into
 //    TMEM.  The running maximum moves only when it grows by more than 2^8
@@ -44,14 +44,11 @@ namespace {
 constexpr int D = 128;
 constexpr int TN = 128;                 // keys per tile
 constexpr int ROWS = 128;               // MMA M
-constexpr int KBOX = 8;                 // keys per K box (2 KB: both head-dim halves)
-constexpr int VBOX = 16;                // keys per V box (4 KB)
-constexpr int NKB = TN / KBOX;          // 16 K boxes per tile
-constexpr int NVB = TN / VBOX;          // 8 V boxes per tile
+constexpr int NVB = TN / 16;            // P V MMAs per tile (16 keys each)
 constexpr int Q_HALF = ROWS * 128;      // 16 KB: 64 head-dim columns of Q
 constexpr int Q_BYTES = 2 * Q_HALF;     // 32 KB
 constexpr int SLOT_BYTES = TN * D * 2;  // 32 KB: one tile of K or of V
-constexpr int LOOKAHEAD = 4;            // own tiles of block-table entries prefetched
+constexpr int LOOKAHEAD = 6;            // tiles of block-table entries prefetched
 constexpr int MAX_BATCH = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_O = 256;
@@ -77,7 +74,7 @@ struct Smem {
                          B_EPI = 18, B_DRAIN = 19, NUM_BARS = 21;
     static constexpr int MISC = BARS + NUM_BARS * 8;    // tmem base, abort flag, range at +16
     static constexpr int STAT = MISC + 32;              // (m, l) of [set][row]
-    static constexpr int PIDS = STAT + 2 * 2 * ROWS * 4;  // [2 producers][LOOKAHEAD+1][NVB] int
+    static constexpr int PIDS = STAT + 2 * 2 * ROWS * 4;  // [2 producers][LOOKAHEAD+1][8] int
     static constexpr int CTX = PIDS + 2 * (LOOKAHEAD + 1) * NVB * 4;
     static constexpr int PRE = CTX + MAX_BATCH * 4;
     static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
@@ -176,6 +173,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, k = a.k, Hkv = a.Hkv, G = a.Hq / a.Hkv, R = k * G, P = a.P;
+    const int CH = P < TN ? P : TN, NCH = TN / CH;  // keys per page chunk, chunks per tile
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -272,96 +270,84 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     };
 
     if (warp == 5 || warp == 6) {
-        // ================= TMA producers: tile it by warp 5 + it % 2 =================
-        // Producer p owns K slot p and V slot p.  K boxes: 8 keys x both
-        // head-dim halves (2 KB), landing [group][half][8 rows][128 B], the
-        // layout an N = 128 Q K^T reads; V boxes: 16 keys (4 KB) in the layout
-        // P V reads.  Block-table entries (one per 16 keys) are prefetched
-        // LOOKAHEAD own tiles ahead with cp.async.
-        const int p = warp - 5;
-        int* pids = reinterpret_cast<int*>(sm + Smem::PIDS) + p * (LOOKAHEAD + 1) * NVB;
-        const int n_own = n_tiles > p ? (n_tiles - 1 - p) / 2 + 1 : 0;
+        // ================= TMA producers: warp 5 K, warp 6 V, every tile =================
+        // Tile it goes to slot it % 2 of each ring: its K slot is free once
+        // Q K^T of tile it - 2 read it, its V slot once P V of tile it - 2
+        // did, so a K copy never waits on a P V.  A tile is NCH chunks of CH
+        // = min(P, 128) keys, each inside one page (CH * 256 contiguous bytes
+        // of the cache), and each chunk is one copy: K as 8-key groups, each
+        // [half][8 rows][128 B] (2 KB), the layout an N = 128 Q K^T reads; V
+        // as 16-key groups, each [half][16 rows][128 B] (4 KB), the layout a
+        // P V of 16 keys reads.  Block-table entries (one per chunk) are
+        // prefetched LOOKAHEAD tiles ahead with cp.async.
+        const bool is_v = warp == 6;
+        int* pids = reinterpret_cast<int*>(sm + Smem::PIDS) + (is_v ? 1 : 0) * (LOOKAHEAD + 1) * NVB;
+        uint64_t* full = &bars[is_v ? Smem::B_VFULL : Smem::B_KFULL];
+        uint64_t* empty = &bars[is_v ? Smem::B_VEMPTY : Smem::B_KEMPTY];
+        uint8_t* ring = sm + (is_v ? Smem::VS : Smem::KS);
+        const CUtensorMap* map = is_v ? &vmap : &kmap;
+        const int gshift = is_v ? 4 : 3;  // log2 of the rows of a group
         Cursor cur, ahead;
-        if (n_own > 0) {
-            cur.init(t_begin + p, s_pre, s_ctx, B, Hkv, k);
+        if (n_tiles > 0) {
+            cur.init(t_begin, s_pre, s_ctx, B, Hkv, k);
             ahead = cur;
         }
-        auto advance = [&](Cursor& c, int from) {
-            for (int j = 1; j <= 2; ++j)
-                if (from + j < n_tiles) c.next(s_ctx, Hkv, k);
-        };
         const uint64_t pol = l2_policy_evict_first();
-        if (lane == 0 && p == 0) {
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
-        }
+        if (lane == 0) prefetch_tmap(map);
         auto fetch_pids = [&](int slot, const Cursor& c) {
             const int key0 = c.lt * TN;
             const int nvalid = min(TN, s_ctx[c.b] + k - key0);
-            if (lane < NVB && lane * VBOX < nvalid)
+            if (lane < NCH && lane * CH < nvalid)
                 cp_async_4(&pids[slot * NVB + lane],
-                           &a.block_table[(int64_t)c.b * a.max_pages + (key0 + lane * VBOX) / P]);
+                           &a.block_table[(int64_t)c.b * a.max_pages + (key0 + lane * CH) / P]);
         };
         for (int la = 0; la < LOOKAHEAD; ++la) {
-            if (la < n_own) {
+            if (la < n_tiles) {
                 fetch_pids(la % (LOOKAHEAD + 1), ahead);
-                advance(ahead, p + la * 2);
+                if (la + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
             }
             cp_async_commit();
         }
-        int nk_issued = 0, nv_issued = 0;
+        int n_issued = 0;
         bool ok = true;
-        for (int q = 0; q < n_own && ok; ++q) {
-            const int it = p + q * 2;
-            if (q + LOOKAHEAD < n_own) {
-                fetch_pids((q + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
-                advance(ahead, p + (q + LOOKAHEAD) * 2);
+        for (int it = 0; it < n_tiles && ok; ++it) {
+            if (it + LOOKAHEAD < n_tiles) {
+                fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
+                if (it + LOOKAHEAD + 1 < n_tiles) ahead.next(s_ctx, Hkv, k);
             }
             cp_async_commit();
             cp_async_wait<LOOKAHEAD>();  // entries of tile `it`
             __syncwarp();
-            const int* pid = pids + (q % (LOOKAHEAD + 1)) * NVB;
+            const int* pid = pids + (it % (LOOKAHEAD + 1)) * NVB;
             const int key0 = cur.lt * TN;
             const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
-            auto row_of = [&](int key) {  // cache row of key `key` of this tile
-                int page = pid[key / VBOX];
+            const int nck = (nvalid + CH - 1) / CH;  // chunks holding keys of the tile
+            const int s = it & 1;
+            if (it >= 2) ok = warp_wait(&empty[s], ((it >> 1) - 1) & 1, abort_flag, a.dev_err);
+            if (ok && lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nck * CH) * 256u);
+            __syncwarp();
+            if (!ok) break;
+            if (lane < nck) {
+                int page = pid[lane];
                 if (page < 0 || page >= a.num_pages) {
                     raise_device_error(a.dev_err, SPEC_DEVERR_PAGE);
                     page = 0;
                 }
-                return (page * Hkv + cur.kvh) * P + (key0 + key) % P;
-            };
-            // K of tile it: slot p, free once Q K^T of tile it - 2 read it
-            if (q >= 1)
-                ok = warp_wait(&bars[Smem::B_KEMPTY + p], (q - 1) & 1, abort_flag, a.dev_err);
-            if (ok && lane == 0)
-                mbar_arrive_expect_tx(&bars[Smem::B_KFULL + p],
-                                      (uint32_t)((nvalid + KBOX - 1) / KBOX) * 2048u);
+                const int row = (page * Hkv + cur.kvh) * P + (key0 + lane * CH) % P;
+                tma_load_4d_hint(ring + s * SLOT_BYTES + lane * CH * 256, map, &full[s], 0, 0, 0,
+                                 row >> gshift, pol);
+            }
+            n_issued = it + 1;
             __syncwarp();
-            if (!ok) break;
-            if (lane < NKB && lane * KBOX < nvalid)
-                tma_load_3d_hint(sm + Smem::KS + p * SLOT_BYTES + lane * 2048, &kmap,
-                                 &bars[Smem::B_KFULL + p], 0, row_of(lane * KBOX), 0, pol);
-            nk_issued = q + 1;
-            // V of tile it: slot p, free once P V of tile it - 2 read it
-            const int nvb = (nvalid + VBOX - 1) / VBOX;
-            if (q >= 1)
-                ok = warp_wait(&bars[Smem::B_VEMPTY + p], (q - 1) & 1, abort_flag, a.dev_err);
-            if (ok && lane == 0) mbar_arrive_expect_tx(&bars[Smem::B_VFULL + p], (uint32_t)nvb * 4096u);
-            __syncwarp();
-            if (!ok) break;
-            if (lane < nvb)
-                tma_load_3d_hint(sm + Smem::VS + p * SLOT_BYTES + lane * 4096, &vmap,
-                                 &bars[Smem::B_VFULL + p], 0, row_of(lane * VBOX), 0, pol);
-            nv_issued = q + 1;
-            __syncwarp();
-            advance(cur, it);
+            if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
         }
         cp_async_wait<0>();
         if (!ok && lane == 0) {
             // the latest copy into each slot lands before the CTA exits
-            if (nk_issued > 0) mbar_drain(&bars[Smem::B_KFULL + p], (nk_issued - 1) & 1);
-            if (nv_issued > 0) mbar_drain(&bars[Smem::B_VFULL + p], (nv_issued - 1) & 1);
+            for (int sl = 0; sl < 2; ++sl) {
+                const int last = (n_issued - 1) - (((n_issued - 1) - sl) & 1);
+                if (last >= 0) mbar_drain(&full[sl], (last >> 1) & 1);
+            }
         }
     } else if (warp == 4) {
         // ================= Q loads and Q K^T issue =================
@@ -419,7 +405,8 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 __syncwarp();
                 tc_fence_after();
                 {
-                    // S = Q K^T: k-slice kk at half kk/4, 32-byte step kk%4
+                    // S = Q K^T: k-slice kk at half kk/4 (Q: 16 KB on, K: 1 KB on
+                    // in every 8-key group), 32-byte step kk%4
                     const uint64_t qd = qdesc0 + ((uint32_t)((pc & 1) * Q_BYTES) >> 4);
                     const uint64_t kd = kdesc0 + ((uint32_t)(s * SLOT_BYTES) >> 4);
 #pragma unroll
@@ -453,8 +440,9 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             int pc = -1;
             bool ok = true;
             bool has0 = false, has1 = false;  // set 0 / 1 issued a P V in this piece
-            // V box j: MN-major, halves 2 KB apart (LBO), 8-key groups 1 KB (SBO)
-            const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::VS), VBOX * 128, 1024);
+            // V of 16 keys: MN-major, head-dim halves 2 KB apart (LBO), 8-key
+            // groups 1 KB (SBO)
+            const uint64_t vdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::VS), 2048, 1024);
             for (int it = 0; it < n_tiles && ok; ++it) {
                 const bool first = (it == 0) || (cur.lt == 0);
                 const int s = it & 1;
@@ -473,14 +461,15 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (ok)
                     ok = warp_wait(&bars[Smem::B_VFULL + s], (it >> 1) & 1, abort_flag, a.dev_err);
                 if (!ok) break;
-                const int nvb = (nvalid + VBOX - 1) / VBOX;
-                if (nvalid % VBOX != 0) {
-                    // keys past the sequence end inside its last box: zero their
-                    // V rows so that 0 * (stale or canary) never reaches O
-                    uint8_t* vst = sm + Smem::VS + s * SLOT_BYTES + (nvb - 1) * 4096;
-                    for (int e = (nvalid % VBOX) * 16 + lane; e < VBOX * 16; e += 32) {
-                        const int rr = e / 16, h = (e / 8) & 1, ch = e % 8;
-                        *reinterpret_cast<uint4*>(vst + h * VBOX * 128 + rr * 128 + ch * 16) =
+                const int nvb = (nvalid + 15) / 16;
+                if (nvalid % 16 != 0) {
+                    // keys past the sequence end that the last P V reads: zero
+                    // their V rows so that 0 * (stale or canary) never reaches O
+                    uint8_t* vst = sm + Smem::VS + s * SLOT_BYTES;
+                    for (int e = lane; e < (nvb * 16 - nvalid) * 16; e += 32) {
+                        const int t = nvalid + e / 16, h = (e / 8) & 1, c16 = e % 8;
+                        *reinterpret_cast<uint4*>(vst + (t / 16) * 4096 + h * 2048 +
+                                                  (t % 16) * 128 + c16 * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
@@ -488,8 +477,9 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 tc_fence_after();
                 {
-                    // O_s += P V: box j is keys [16j, 16j + 16), its P at the S
-                    // columns [8j, 8j + 8) (j < 4) or [64 + 8(j-4), ...)
+                    // O_s += P V: MMA j takes keys [16j, 16j + 16) (4 KB group j),
+                    // their P at the S columns [8j, 8j + 8) (j < 4) or
+                    // [64 + 8(j-4), ...)
                     const uint64_t vd = vdesc0 + ((uint32_t)(s * SLOT_BYTES) >> 4);
                     const bool hs = s ? has1 : has0;
                     const uint32_t sbuf = tmem + TM_S + s * TN;
@@ -735,15 +725,18 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, int num_ctas, void* workspace, cu
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    // K / V: [rows = num_pages*Hkv*P] x [2 halves] x [64 columns]; a box is
-    // KBOX (K) or VBOX (V) consecutive rows of one page, both halves
+    // K / V rows (num_pages*Hkv*P of 256 B) seen as [groups of g rows] x
+    // [2 halves] x [g rows] x [64 columns], g = 8 (K) or 16 (V); a box is CH =
+    // min(P, 128) consecutive rows of one page, landing group by group
     const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
+    const cuuint32_t ch = (cuuint32_t)(a.P < TN ? a.P : TN);
     for (int t = 0; t < 2; ++t) {
-        cuuint64_t dims[3] = {64, rows, 2};
-        cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-        cuuint32_t box[3] = {64, (cuuint32_t)(t == 0 ? KBOX : VBOX), 2};
-        cuuint32_t es[3] = {1, 1, 1};
-        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+        const cuuint32_t g = t == 0 ? 8 : 16;
+        cuuint64_t dims[4] = {64, g, 2, rows / g};
+        cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)g * D * 2};
+        cuuint32_t box[4] = {64, g, 2, ch / g};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                    const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

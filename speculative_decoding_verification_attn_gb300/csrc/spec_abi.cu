@@ -220,7 +220,8 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
 
     // kernels: 1 SIMT (chunked), 2 tcgen05 (64-key tiles), 3 warp MMA,
     // 4 single-pass SIMT, 5 tcgen05 (128-key tiles); automatic = warp MMA for
-    // <= 16 query rows per kv-head, tcgen05 (64-key tiles) above, and for
+    // <= 16 query rows per kv-head, tcgen05 above (128-key tiles where that
+    // kernel takes the shape: bf16, head_dim 128, 65..128 rows), and for
     // every other shape the single-pass SIMT kernel when a whole sequence
     // fits its shared memory, else the chunked one
     const int64_t path = g_opt_path.load();
@@ -235,7 +236,7 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
             return fail(SPEC_ERR_UNSUPPORTED, "forced attention kernel %d does not support this "
                         "shape/dtype", (int)path);
         kernel = (int)path;
-    } else kernel = mma_ok ? 3 : tc_ok ? 2 : small_ok ? 4 : 1;
+    } else kernel = mma_ok ? 3 : tc2_ok ? 5 : tc_ok ? 2 : small_ok ? 4 : 1;
     if (kernel == 3 && (int64_t)batch * num_kv_heads > kMaxCounters)
         return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads > %d for the warp-MMA kernel",
                     kMaxCounters);
