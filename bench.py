@@ -580,7 +580,9 @@ def run_gpu(args, inp, world, rank, local):
         "timing": timing,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (launches_per_step(inp) + (1 if rejection else 0)),
+        "gpu_launches": args.steps * (launches_per_step(
+            inp, torch.cuda.get_device_properties(device).multi_processor_count) +
+            (1 if rejection else 0)),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "spec_verify_attn (attention + split-KV combine), K calls back "
@@ -663,13 +665,14 @@ def run_codec(args, inp):
     print(json.dumps(line), flush=True)
 
 
-def launches_per_step(inp) -> int:
-    """Kernels one step launches (mirrors the library's automatic choice): the
-    warp-MMA attention kernel (bf16, head_dim 128, <= 16 query rows per
-    kv-head, page size 16..256) merges its split-KV partials itself, the
-    tcgen05 kernels (128-key tiles for a bf16 cache and 65..128 rows, 64-key
-    tiles otherwise, up to 128 rows) are followed by a combine kernel; other
-    shapes run the single-pass SIMT kernel when a whole sequence fits its
+def launches_per_step(inp, num_sms: int) -> int:
+    """Kernels one step launches (mirrors the library's automatic choice): for
+    a bf16 cache (head_dim 128, page size 16..256, up to 128 query rows per
+    kv-head) the 128-key tcgen05 kernel and its combine, except that with <=
+    16 rows, more (sequence, kv-head) segments than SMs and a block table
+    shorter than 3072 keys the warp-MMA kernel, which merges its split-KV
+    partials itself; an INT8 cache the 64-key tcgen05 kernel and its combine;
+    other shapes the single-pass SIMT kernel when a whole sequence fits its
     shared memory (one launch), else the chunked SIMT kernel and its combine;
     plus the acceptance kernel."""
     s = inp.spec
@@ -677,7 +680,9 @@ def launches_per_step(inp) -> int:
     rows = s.num_draft * G
     tc_shape = (s.q_dtype == "bf16" and s.kv_dtype in ("bf16", "i8") and s.head_dim == 128
                 and 16 <= s.page_size <= 256 and s.page_size & (s.page_size - 1) == 0)
-    if tc_shape and s.kv_dtype == "bf16" and rows <= 16:
+    many_short = (s.batch * s.num_kv_heads > num_sms
+                  and inp.block_table.shape[1] * s.page_size < 3072)
+    if tc_shape and s.kv_dtype == "bf16" and rows <= 16 and many_short:
         return 1 + 1
     if tc_shape and rows <= 128:
         return 2 + 1

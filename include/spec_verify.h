@@ -85,7 +85,7 @@ enum {
      * kernel (64-key tiles), 3 warp-MMA (mma.sync) kernel for <= 16 query
      * rows per kv-head, 4 single-pass SIMT kernel (whole sequences in shared
      * memory), 5 tcgen05 kernel with 128-key tiles (bf16 query and cache,
-     * head_dim 128, 65..128 query rows per kv-head, power-of-two pages of
+     * head_dim 128, up to 128 query rows per kv-head, power-of-two pages of
      * 16..256 keys) */
     SPEC_OPT_ATTN_PATH = 0,
     /* persistent CTAs of the tensor-core kernel; 0 = number of SMs */

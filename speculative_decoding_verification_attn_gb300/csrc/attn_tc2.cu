@@ -1,5 +1,5 @@
 // Verification attention on the tcgen05 tensor cores with 128-key tiles, for
-// 65..128 query rows per kv-head over a bf16 paged cache, head_dim 128.
+// up to 128 query rows per kv-head over a bf16 paged cache, head_dim 128.
 //
 // What it computes: multi-query causal attention of each sequence's k draft
 // queries over its paged cache ("Decoding Speculative Decoding from First
@@ -701,7 +701,7 @@ bool tc2_supported(const AttnArgs& a) {
     const int G = a.Hq / a.Hkv, R = a.k * G;
     const bool pow2 = (a.P & (a.P - 1)) == 0;
     return a.q_dtype == SPEC_DTYPE_BF16 && a.kv_dtype == SPEC_DTYPE_BF16 && a.D == D &&
-           R > 64 && R <= ROWS && G <= 256 && pow2 && a.P >= 16 && a.P <= 256 &&
+           R <= ROWS && G <= 256 && pow2 && a.P >= 16 && a.P <= 256 &&
            a.B <= MAX_BATCH && (int64_t)a.num_pages * a.Hkv * a.P < (1LL << 31) &&
            (int64_t)a.B * a.k < (1LL << 31);
 }

@@ -75,7 +75,7 @@ cudaError_t launch_combine_stream_k(const AttnArgs& a, int num_ctas, int alpha,
                                     const float* part_o, const float* part_lse,
                                     const int4* seg_rec, const int* seg_pre, cudaStream_t stream);
 
-// ---- tensor-core kernel with 128-key tiles: bf16, head_dim 128, 65..128
+// ---- tensor-core kernel with 128-key tiles: bf16, head_dim 128, up to 128
 // query rows per kv-head (two softmax sets); workspace as tc_workspace_bytes ----
 bool tc2_supported(const AttnArgs& a);
 cudaError_t launch_attn_tc2(const AttnArgs& a, int num_ctas, void* workspace, cudaStream_t stream);

@@ -218,12 +218,19 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
     a.split_alpha = split_opt > 0 ? (int32_t)(split_opt - 1) : -1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    Workspace* ws = nullptr;
+    int rc = get_workspace(0, &ws);
+    if (rc) return rc;
+
     // kernels: 1 SIMT (chunked), 2 tcgen05 (64-key tiles), 3 warp MMA,
-    // 4 single-pass SIMT, 5 tcgen05 (128-key tiles); automatic = warp MMA for
-    // <= 16 query rows per kv-head, tcgen05 above (128-key tiles where that
-    // kernel takes the shape: bf16, head_dim 128, 65..128 rows), and for
-    // every other shape the single-pass SIMT kernel when a whole sequence
-    // fits its shared memory, else the chunked one
+    // 4 single-pass SIMT, 5 tcgen05 (128-key tiles).  Automatic: a bf16
+    // cache with head_dim 128 takes the 128-key tcgen05 kernel, except that
+    // with <= 16 query rows per kv-head the warp-MMA kernel (whose pieces of
+    // a split segment cost less) keeps the calls with more segments than SMs
+    // and tables shorter than 3072 keys (about 24 tiles per segment, the
+    // point where the two cross over when measured); the INT8 cache takes
+    // the 64-key tcgen05 kernel; every other shape the single-pass SIMT
+    // kernel when a whole sequence fits its shared memory, else the chunked one
     const int64_t path = g_opt_path.load();
     const bool tc_ok = specv::tc_supported(a), mma_ok = specv::mma_supported(a);
     const bool tc2_ok = specv::tc2_supported(a);
@@ -236,15 +243,15 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
             return fail(SPEC_ERR_UNSUPPORTED, "forced attention kernel %d does not support this "
                         "shape/dtype", (int)path);
         kernel = (int)path;
-    } else kernel = mma_ok ? 3 : tc2_ok ? 5 : tc_ok ? 2 : small_ok ? 4 : 1;
+    } else {
+        const bool many_short = (int64_t)batch * num_kv_heads > ws->sms &&
+                                (int64_t)max_pages_per_seq * page_size < 3072;
+        kernel = mma_ok && (many_short || !tc2_ok) ? 3 : tc2_ok ? 5 : tc_ok ? 2 : small_ok ? 4 : 1;
+    }
     if (kernel == 3 && (int64_t)batch * num_kv_heads > kMaxCounters)
         return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads > %d for the warp-MMA kernel",
                     kMaxCounters);
     const bool use_tc = kernel == 2 || kernel == 3 || kernel == 5;
-
-    Workspace* ws = nullptr;
-    int rc = get_workspace(0, &ws);
-    if (rc) return rc;
     if (g_opt_validate.load()) {
         rc = validate_tables(a, st);
         if (rc) return rc;

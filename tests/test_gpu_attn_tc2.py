@@ -1,7 +1,7 @@
 """GPU parity of the 128-key-tile tcgen05 kernel (attention path 5) with the oracle.
 
-The kernel takes bf16 queries and cache, head_dim 128 and 65..128 query rows
-per kv-head.  Cases span 128-key tile edges, ragged tails, contexts of zero,
+The kernel takes bf16 queries and cache, head_dim 128 and up to 128 query
+rows per kv-head.  Cases span 128-key tile edges, ragged tails, contexts of zero,
 every page size it takes, one long segment, forced stream-K splits of every
 size (the combine in both its forms), charged splits, tree masks, and the
 shapes it must refuse.  NaN canaries fill every unused cache slot.
@@ -47,6 +47,11 @@ CASES = [
     dict(batch=1, num_q_heads=28, num_kv_heads=4, num_draft=16, ctx=[5000]),  # one long segment
     dict(num_q_heads=96, num_kv_heads=1, num_draft=1, ctx=(0, 300)),        # k = 1, G = 96
     dict(batch=200, num_q_heads=28, num_kv_heads=4, num_draft=16, ctx=(0, 100)),  # many pieces
+    dict(num_q_heads=16, num_kv_heads=2, num_draft=8),                      # 64 rows
+    dict(num_q_heads=12, num_kv_heads=2, num_draft=4, ctx=(0, 700)),        # 24 rows
+    dict(num_q_heads=8, num_kv_heads=2, num_draft=4),                       # 16 rows
+    dict(num_q_heads=4, num_kv_heads=4, num_draft=1, ctx=[0, 1, 127, 128, 129], batch=5),  # 1 row
+    dict(num_q_heads=32, num_kv_heads=32, num_draft=8, batch=2, ctx=(200, 900)),  # MHA, 8 rows
 ]
 
 
@@ -59,8 +64,8 @@ def test_tc128_small(oracle_mod, kw):
 
 # every size of split: one CTA (no combine), fewer CTAs than segments (the
 # combine by boundary), more (by segment), and CTAs left without tiles
-@pytest.mark.parametrize("heads", [(28, 4, 12), (16, 2, 16), (8, 4, 40)],
-                         ids=["84rows", "128rows", "80rows_G2"])
+@pytest.mark.parametrize("heads", [(28, 4, 12), (16, 2, 16), (8, 4, 40), (8, 2, 4)],
+                         ids=["84rows", "128rows", "80rows_G2", "16rows"])
 @pytest.mark.parametrize("ctas", [1, 2, 5, 37, 152, 400])
 def test_tc128_stream_k_splits(oracle_mod, ctas, heads):
     hq, hkv, k = heads
@@ -95,7 +100,8 @@ def test_tc128_long_step_shape_sampled(oracle_mod):
 @pytest.mark.parametrize("kw", [
     dict(num_q_heads=28, num_kv_heads=4, num_draft=16, page_size=32),
     dict(num_q_heads=2, num_kv_heads=1, num_draft=64, ctx=(0, 300)),       # 64-bit masks
-], ids=["112rows", "k64"])
+    dict(num_q_heads=8, num_kv_heads=2, num_draft=4),                       # 16 rows
+], ids=["112rows", "k64", "16rows"])
 def test_tc128_tree_masks(oracle_mod, kw, width):
     spec = small_spec(**kw)
     inp = make_inputs(spec, seed=85)
@@ -133,11 +139,11 @@ def test_tc128_close_to_tc64():
 
 
 @pytest.mark.parametrize("kw", [
-    dict(num_q_heads=16, num_kv_heads=2, num_draft=8),                     # 64 rows
+    dict(num_q_heads=32, num_kv_heads=2, num_draft=9),                     # 144 rows
     dict(num_q_heads=28, num_kv_heads=4, num_draft=16, kv_dtype="i8"),     # INT8 cache
     dict(num_q_heads=28, num_kv_heads=4, num_draft=16, head_dim=64),       # head_dim 64
     dict(num_q_heads=28, num_kv_heads=4, num_draft=16, q_dtype="f32", kv_dtype="f32"),
-], ids=["64rows", "i8", "d64", "f32"])
+], ids=["144rows", "i8", "d64", "f32"])
 def test_tc128_refuses_other_shapes(kw):
     inp = make_inputs(small_spec(**kw), seed=88)
     t = binding.inputs_to_torch(inp)

@@ -65,6 +65,8 @@ CASES = [  # (attention path, spec)
     (1, dict(q_dtype="f32", kv_dtype="f32", head_dim=64, num_draft=5)),        # SIMT fp32
     (4, dict(q_dtype="f32", kv_dtype="f32", head_dim=64, num_draft=5)),        # single pass
     (4, dict(num_q_heads=2, num_kv_heads=2, num_draft=64, ctx=(0, 40))),      # single pass, k = 64
+    (5, dict(num_q_heads=28, num_kv_heads=4, num_draft=16, page_size=32)),     # 128-key tiles
+    (5, dict(num_q_heads=8, num_kv_heads=2, num_draft=4)),                     # 128-key, 16 rows
 ]
 
 
@@ -81,7 +83,7 @@ def test_tree_attention_matches_oracle(oracle_mod, path, kw, width):
     assert binding.spec_device_error() == 0
 
 
-@pytest.mark.parametrize("path", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("path", [0, 1, 2, 3, 4, 5])
 def test_chain_mask_reproduces_causal(path):
     # (the single-pass kernel holds whole sequences: shorter contexts there)
     ctx = (0, 100) if path == 4 else (0, 300)
