@@ -1,5 +1,6 @@
 // Verification attention on the tcgen05 tensor cores with 128-key tiles, for
-// up to 128 query rows per kv-head over a bf16 paged cache, head_dim 128.
+// up to 128 query rows per kv-head over a bf16 or INT8 paged cache, head_dim
+// 128.
 //
 // What it computes: multi-query causal attention of each sequence's k draft
 // queries over its paged cache ("Decoding Speculative Decoding from First
@@ -29,6 +30,13 @@
 //  * Work split: stream-K over the 128-key tiles with the per-segment charge
 //    of TileSplit; partials of segments cut by a CTA range are merged by the
 //    combine kernel of the 64-key kernel (same records, this kernel's tiles).
+//  * INT8 cache (per-key fp16 scales): the producers land the raw int8 tile
+//    in the upper half of its operand slot and its scales in a small stage;
+//    four more warps (12-13 K, 14-15 V) dequantize it in place to fp16
+//    (int8 * scale, one rounding) in the layout the MMAs read.  q is turned to fp16 in
+//    place once per piece and P is packed as fp16, so A and B share a type.
+//    The 16 warps share the 64K registers of the block unevenly
+//    (setmaxnreg): softmax 160 each, issue / copy 80, dequantization 112.
 //  * Every mbarrier wait is bounded (1 s); a timeout sets the device error
 //    word and an abort flag, after which every role skips its remaining work
 //    (the softmax sets still pass their pairwise barriers), drains its copies
@@ -59,10 +67,24 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // drains the pipeline: the next piece's Q, the merge of the two sets)
 constexpr int kSplitAlpha = 3;
 
-constexpr uint32_t kIdescQK = umma_idesc_bf16(ROWS, TN, 0, 0);
-constexpr uint32_t kIdescPV = umma_idesc_bf16(ROWS, D, 0, 1);  // B (V) MN-major
+// A / B operand formats of tcgen05.mma kind::f16: bf16 cache: bf16; INT8
+// cache widened to fp16, so q and P are fp16 there too
+template <bool KV8>
+constexpr uint32_t idesc_qk() {
+    return KV8 ? umma_idesc_f16(ROWS, TN, 0, 0) : umma_idesc_bf16(ROWS, TN, 0, 0);
+}
+template <bool KV8>
+constexpr uint32_t idesc_pv() {  // B (V) MN-major
+    return KV8 ? umma_idesc_f16(ROWS, D, 0, 1) : umma_idesc_bf16(ROWS, D, 0, 1);
+}
+template <bool KV8>
+constexpr int threads() { return KV8 ? 16 * 32 : 12 * 32; }
 
 using Cursor = CursorT<TN>;
+
+// INT8: the raw int8 tile (128 keys x 128 B = 16 KB) lands in the upper half
+// of its 32 KB operand slot and is dequantized in place
+constexpr int RAW_OFF = SLOT_BYTES / 2;
 
 struct Smem {
     static constexpr int Q = 0;                         // 2 buffers (piece parity)
@@ -71,13 +93,15 @@ struct Smem {
     static constexpr int BARS = VS + 2 * SLOT_BYTES;
     static constexpr int B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8,
                          B_QFREE = 10, B_SFULL = 12, B_PREADY = 14, B_SFREE = 16,
-                         B_EPI = 18, B_DRAIN = 19, NUM_BARS = 21;
+                         B_EPI = 18, B_DRAIN = 19, B_KREADY = 21, B_VREADY = 23, NUM_BARS = 25;
     static constexpr int MISC = BARS + NUM_BARS * 8;    // tmem base, abort flag, range at +16
     static constexpr int STAT = MISC + 32;              // (m, l) of [set][row]
     static constexpr int PIDS = STAT + 2 * 2 * ROWS * 4;  // [2 producers][LOOKAHEAD+1][8] int
     static constexpr int CTX = PIDS + 2 * (LOOKAHEAD + 1) * NVB * 4;
     static constexpr int PRE = CTX + MAX_BATCH * 4;
-    static constexpr int END = PRE + (MAX_BATCH + 1) * 4;
+    // INT8: fp16 scales of tile it at stage it % 2, k then v
+    static constexpr int SCRAW = (PRE + (MAX_BATCH + 1) * 4 + 127) / 128 * 128;
+    static constexpr int END = SCRAW + 2 * 2 * TN * 2;
 };
 constexpr size_t SMEM_BYTES = Smem::END + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -124,7 +148,9 @@ __device__ __forceinline__ float scale_mask64(uint32_t (&r)[64], float sl2, uint
     return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
-// p = 2^(v - m) of 64 columns (fp32 bits), packed to bf16 pairs; returns their sum.
+// p = 2^(v - m) of 64 columns (fp32 bits), packed to bf16 (F16: fp16) pairs;
+// returns their sum.
+template <bool F16>
 __device__ __forceinline__ float exp_pack64(const uint32_t (&v)[64], float m, uint32_t (&pk)[32]) {
     const uint64_t neg_m = f2(-m, -m);
     uint64_t ps[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
@@ -135,7 +161,7 @@ __device__ __forceinline__ float exp_pack64(const uint32_t (&v)[64], float m, ui
         e0 = fast_exp2(e0);
         e1 = fast_exp2(e1);
         ps[(c >> 1) & 1] = f2_add(ps[(c >> 1) & 1], f2(e0, e1));
-        pk[c >> 1] = pack_bf16x2(e0, e1);
+        pk[c >> 1] = F16 ? pack_f16x2(e0, e1) : pack_bf16x2(e0, e1);
     }
     float a0, a1, b0, b1;
     f2_split(ps[0], a0, a1);
@@ -157,9 +183,11 @@ __device__ __forceinline__ uint64_t visible64(int key0, int c0, int nvalid, int 
     return (cbits | dbits) & valid;
 }
 
-__global__ void __launch_bounds__(12 * 32, 1)
+template <bool KV8>
+__global__ void __launch_bounds__(threads<KV8>(), 1)
 attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const Tc2Params prm) {
+    constexpr int NT = threads<KV8>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -186,6 +214,8 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             mbar_init(&bars[Smem::B_SFULL + s], 1);
             mbar_init(&bars[Smem::B_PREADY + s], 4);  // the 4 warps of the set
             mbar_init(&bars[Smem::B_SFREE + s], 1);
+            mbar_init(&bars[Smem::B_KREADY + s], 2);  // INT8: the 2 warps converting K / V
+            mbar_init(&bars[Smem::B_VREADY + s], 2);
         }
         mbar_init(&bars[Smem::B_EPI], 8);  // every softmax warp, once per piece
         mbar_init(&bars[Smem::B_DRAIN], 1);
@@ -204,7 +234,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     {
         // Q rows R..127 stay zero in both buffers (the TMA writes rows < R)
         uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
-        for (int e = tid; e < 2 * Q_BYTES / 16; e += 12 * 32) {
+        for (int e = tid; e < 2 * Q_BYTES / 16; e += NT) {
             const int row = (e % (Q_HALF / 16)) / 8;
             if (row >= R) q4[e] = make_uint4(0, 0, 0, 0);
         }
@@ -262,13 +292,18 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             make_int4((int)(t_begin & 0xffffffff), (int)(t_begin >> 32), 0, 0);
     }
     if (blockIdx.x == 0)
-        for (int b = tid; b <= B; b += 12 * 32) prm.seg_pre[b] = s_pre[b];
+        for (int b = tid; b <= B; b += NT) prm.seg_pre[b] = s_pre[b];
 
     // does a piece follow the one of cursor c in this CTA's range
     auto has_next_piece = [&](const Cursor& c) {
         return c.seg_start + c.nb < ld_shared_s64(s_rng + 1);
     };
-
+    // INT8 (16 warps on 64K registers): the softmax warpgroups take 160 each,
+    // the issue / copy warpgroup gives its registers down to 80 and the
+    // dequantizing one to 112 (2 x 160 + 80 + 112 = 4 x 128, the launch
+    // allocation), each warpgroup as the first step of its branch
+    if (warp >= 4 && warp < 8) {
+    if constexpr (KV8) regs_dec<80>();
     if (warp == 5 || warp == 6) {
         // ================= TMA producers: warp 5 K, warp 6 V, every tile =================
         // Tile it goes to slot it % 2 of each ring: its K slot is free once
@@ -280,6 +315,8 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         // as 16-key groups, each [half][16 rows][128 B] (4 KB), the layout a
         // P V of 16 keys reads.  Block-table entries (one per chunk) are
         // prefetched LOOKAHEAD tiles ahead with cp.async.
+        // INT8: each chunk is CH * 128 raw bytes into the upper half of the
+        // slot, and its CH fp16 scales into scale stage it % 2.
         const bool is_v = warp == 6;
         int* pids = reinterpret_cast<int*>(sm + Smem::PIDS) + (is_v ? 1 : 0) * (LOOKAHEAD + 1) * NVB;
         uint64_t* full = &bars[is_v ? Smem::B_VFULL : Smem::B_KFULL];
@@ -324,7 +361,8 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int nck = (nvalid + CH - 1) / CH;  // chunks holding keys of the tile
             const int s = it & 1;
             if (it >= 2) ok = warp_wait(&empty[s], ((it >> 1) - 1) & 1, abort_flag, a.dev_err);
-            if (ok && lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nck * CH) * 256u);
+            const uint32_t bytes = (uint32_t)(nck * CH) * (KV8 ? 128u + 2u : 256u);
+            if (ok && lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
             __syncwarp();
             if (!ok) break;
             if (lane < nck) {
@@ -334,8 +372,15 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     page = 0;
                 }
                 const int row = (page * Hkv + cur.kvh) * P + (key0 + lane * CH) % P;
-                tma_load_4d_hint(ring + s * SLOT_BYTES + lane * CH * 256, map, &full[s], 0, 0, 0,
-                                 row >> gshift, pol);
+                if constexpr (KV8) {
+                    tma_load_2d(ring + s * SLOT_BYTES + RAW_OFF + lane * CH * 128, map, &full[s], 0,
+                                row, pol);
+                    bulk_load(sm + Smem::SCRAW + (s * 2 + (is_v ? 1 : 0)) * TN * 2 + lane * CH * 2,
+                              (is_v ? a.v_scale : a.k_scale) + row, CH * 2, &full[s]);
+                } else {
+                    tma_load_4d_hint(ring + s * SLOT_BYTES + lane * CH * 256, map, &full[s], 0, 0,
+                                     0, row >> gshift, pol);
+                }
             }
             n_issued = it + 1;
             __syncwarp();
@@ -395,9 +440,19 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     ok = warp_wait(&bars[Smem::B_QFULL + (pc & 1)], (pc >> 1) & 1, abort_flag,
                                    a.dev_err);
                     if (!ok) break;
+                    if constexpr (KV8) {
+                        // the piece's q to fp16, in place (rows < R; the rest are zero)
+                        uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q + (pc & 1) * Q_BYTES);
+                        for (int e = lane; e < Q_BYTES / 16; e += 32)
+                            if ((e % (Q_HALF / 16)) / 8 < R) q4[e] = bf16x8_to_f16(q4[e]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
                 }
-                // K of tile it landed; S buffer s free (P V of tile it - 2 done)
-                ok = warp_wait(&bars[Smem::B_KFULL + s], (it >> 1) & 1, abort_flag, a.dev_err);
+                // K of tile it landed (INT8: widened); S buffer s free (P V of
+                // tile it - 2 done)
+                ok = warp_wait(&bars[(KV8 ? Smem::B_KREADY : Smem::B_KFULL) + s], (it >> 1) & 1,
+                               abort_flag, a.dev_err);
                 if (ok && it >= 2)
                     ok = warp_wait(&bars[Smem::B_SFREE + s], ((it >> 1) - 1) & 1, abort_flag,
                                    a.dev_err);
@@ -413,7 +468,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     for (int kk = 0; kk < 8; ++kk)
                         umma_ss_w(tmem + TM_S + s * TN,
                                   qd + (kk >> 2) * (Q_HALF >> 4) + (kk & 3) * 2,
-                                  kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, kIdescQK,
+                                  kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk<KV8>(),
                                   kk ? 1u : 0u);
                     umma_commit_w(&bars[Smem::B_SFULL + s]);
                     umma_commit_w(&bars[Smem::B_KEMPTY + s]);
@@ -456,13 +511,16 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         ok = warp_wait(&bars[Smem::B_EPI], (pc - 1) & 1, abort_flag, a.dev_err);
                     if (!ok) break;
                 }
-                // this set's P of tile it stored; V of tile it landed
+                // this set's P of tile it stored; V of tile it landed (INT8:
+                // widened)
                 ok = warp_wait(&bars[Smem::B_PREADY + s], (it >> 1) & 1, abort_flag, a.dev_err);
                 if (ok)
-                    ok = warp_wait(&bars[Smem::B_VFULL + s], (it >> 1) & 1, abort_flag, a.dev_err);
+                    ok = warp_wait(&bars[(KV8 ? Smem::B_VREADY : Smem::B_VFULL) + s],
+                                   (it >> 1) & 1, abort_flag, a.dev_err);
                 if (!ok) break;
                 const int nvb = (nvalid + 15) / 16;
-                if (nvalid % 16 != 0) {
+                // (INT8: the widened rows past the sequence end are finite)
+                if (!KV8 && nvalid % 16 != 0) {
                     // keys past the sequence end that the last P V reads: zero
                     // their V rows so that 0 * (stale or canary) never reaches O
                     uint8_t* vst = sm + Smem::VS + s * SLOT_BYTES;
@@ -488,7 +546,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     for (int j = 0; j < NVB; ++j)
                         if (j < nvb)
                             umma_ts_w(od, sbuf + (j < 4 ? 8 * j : 64 + 8 * (j - 4)),
-                                      vd + ((uint32_t)(j * 4096) >> 4), kIdescPV,
+                                      vd + ((uint32_t)(j * 4096) >> 4), idesc_pv<KV8>(),
                                       (hs || j > 0) ? 1u : 0u);
                     umma_commit_w(&bars[Smem::B_VEMPTY + s]);
                     umma_commit_w(&bars[Smem::B_SFREE + s]);
@@ -502,7 +560,84 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (lane == 0) mbar_drain(&bars[Smem::B_DRAIN + 1], 0);
             __syncwarp();
         }
-    } else if (warp < 4 || warp >= 8) {
+    }
+    } else if (KV8 && warp >= 12) {
+        if constexpr (KV8) regs_dec<112>();
+        // ================= INT8 dequantization (warps 12-13 K, 14-15 V) =================
+        // Every tile in order: each int8 widened exactly to fp16 and
+        // multiplied by its key's fp16 scale (one rounding to fp16), written
+        // in place over the slot in the layout the MMAs read.  The raw tile
+        // sits in the upper half: rows 0..63 are written to the lower half
+        // straight away; rows 64..127 land over the raw bytes, so the pair of
+        // warps first reads all of them and meets at a barrier.  Whole page
+        // chunks are converted; keys past the sequence end become zero rows
+        // (their stored scale may be anything, NaN included).  Every warp
+        // runs every tile and every barrier, also after an abort (then
+        // without waiting or work).
+        const bool is_v = warp >= 14;
+        const int ct = tid - (is_v ? 14 : 12) * 32;  // 0..63
+        Cursor c;
+        if (n_tiles > 0) c.init(t_begin, s_pre, s_ctx, B, Hkv, k);
+        bool ok = true;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int s = it & 1;
+            const int nvalid = min(TN, s_ctx[c.b] + k - c.lt * TN);
+            const int nch = (nvalid + CH - 1) / CH * CH * 8;  // raw 16-byte chunks loaded
+            if (ok)
+                ok = warp_wait(&bars[(is_v ? Smem::B_VFULL : Smem::B_KFULL) + s], (it >> 1) & 1,
+                               abort_flag, a.dev_err);
+            uint8_t* slot = sm + (is_v ? Smem::VS : Smem::KS) + s * SLOT_BYTES;
+            const __half* scl =
+                reinterpret_cast<const __half*>(sm + Smem::SCRAW + (s * 2 + (is_v ? 1 : 0)) * TN * 2);
+            // chunk id (key id / 8, 16 head dims id % 8): widen, scale, store
+            auto put = [&](int id, uint4 raw) {
+                const int j = id >> 3, c16 = id & 7, h = c16 >> 2, sw = j & 7;
+                const __half2 sc2 = __half2half2(j < nvalid ? scl[j] : __float2half(0.f));
+                uint4 lo, hi;
+                i8x16_to_f16(raw, lo, hi);
+                __half2* l2 = reinterpret_cast<__half2*>(&lo);
+                __half2* h2 = reinterpret_cast<__half2*>(&hi);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    l2[e] = __hmul2(l2[e], sc2);
+                    h2[e] = __hmul2(h2[e], sc2);
+                }
+                // fp16 chunks cc, cc+1 of half h (swizzled by the row); lanes
+                // of half 1 store their odd chunk first so that 8 consecutive
+                // lanes hit 8 bank groups
+                const int cc = (c16 & 3) * 2;
+                const int o0 = ((cc + h) ^ sw) << 4, o1 = ((cc + 1 - h) ^ sw) << 4;
+                uint8_t* row = is_v ? slot + (j >> 4) * 4096 + h * 2048 + (j & 15) * 128
+                                    : slot + (j >> 3) * 2048 + h * 1024 + (j & 7) * 128;
+                *reinterpret_cast<uint4*>(row + o0) = h ? hi : lo;
+                *reinterpret_cast<uint4*>(row + o1) = h ? lo : hi;
+            };
+            // rows 0..63: raw in [16, 24) KB, output in [0, 16) KB
+#pragma unroll 4
+            for (int u = 0; u < 8; ++u) {
+                const int id = ct + 64 * u;
+                if (ok && id < nch) put(id, *reinterpret_cast<const uint4*>(slot + RAW_OFF + id * 16));
+            }
+            // rows 64..127: read all raw first, their output overlaps it
+            uint4 raw[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int id = 512 + ct + 64 * u;
+                if (ok && id < nch) raw[u] = *reinterpret_cast<const uint4*>(slot + RAW_OFF + id * 16);
+            }
+            named_bar_sync(is_v ? 7 : 6, 64);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int id = 512 + ct + 64 * u;
+                if (ok && id < nch) put(id, raw[u]);
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[(is_v ? Smem::B_VREADY : Smem::B_KREADY) + s]);
+            if (it + 1 < n_tiles) c.next(s_ctx, Hkv, k);
+        }
+    } else {
+        if constexpr (KV8) regs_inc<160>();
         // ================= softmax sets (0: warps 0-3, even tiles; 1: 8-11, odd) =================
         const int set = warp >= 8 ? 1 : 0;
         const int quad = warp & 3;                 // TMEM lane quadrant
@@ -543,9 +678,10 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 if (ok && quad_active) {
                     tc_fence_after();
                     uint32_t v[64];
+                    const uint64_t vis0 = visible64(key0, 0, nvalid, ctx, mrow);
                     // row maximum over both halves; the second half stays in v
                     load64(s_mine, v);
-                    const float mx0 = scale_mask64(v, sl2, visible64(key0, 0, nvalid, ctx, mrow));
+                    const float mx0 = scale_mask64(v, sl2, vis0);
                     load64(s_mine + 64, v);
                     const float mx1 = scale_mask64(v, sl2, visible64(key0, 64, nvalid, ctx, mrow));
                     const float m_new = fmaxf(m_ref, fmaxf(mx0, mx1));
@@ -560,11 +696,11 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     uint32_t pk[32];
                     // P of keys 64..127 over S columns [64, 96), then keys 0..63
                     // (reloaded) over [0, 32)
-                    l += exp_pack64(v, m_use, pk);
+                    l += exp_pack64<KV8>(v, m_use, pk);
                     tmem_st32(s_mine + 64, pk);
                     load64(s_mine, v);
-                    scale_mask64(v, sl2, visible64(key0, 0, nvalid, ctx, mrow));
-                    l += exp_pack64(v, m_use, pk);
+                    scale_mask64(v, sl2, vis0);
+                    l += exp_pack64<KV8>(v, m_use, pk);
                     tmem_st32(s_mine, pk);
                     tmem_wait_st();
                     if (has && __any_sync(0xffffffffu, move)) {
@@ -700,7 +836,14 @@ EncodeTiledFn get_encode_fn() {
 bool tc2_supported(const AttnArgs& a) {
     const int G = a.Hq / a.Hkv, R = a.k * G;
     const bool pow2 = (a.P & (a.P - 1)) == 0;
-    return a.q_dtype == SPEC_DTYPE_BF16 && a.kv_dtype == SPEC_DTYPE_BF16 && a.D == D &&
+    // INT8 cache: the scales are fetched a page chunk (>= 32 bytes) at a time
+    // with bulk copies, which need 16-byte aligned sources
+    const bool kv_ok =
+        a.kv_dtype == SPEC_DTYPE_BF16 ||
+        (a.kv_dtype == SPEC_DTYPE_I8 && a.k_scale && a.v_scale &&
+         (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(a.v_scale) & 15) == 0);
+    return a.q_dtype == SPEC_DTYPE_BF16 && kv_ok && a.D == D &&
            R <= ROWS && G <= 256 && pow2 && a.P >= 16 && a.P <= 256 &&
            a.B <= MAX_BATCH && (int64_t)a.num_pages * a.Hkv * a.P < (1LL << 31) &&
            (int64_t)a.B * a.k < (1LL << 31);
@@ -727,10 +870,25 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, int num_ctas, void* workspace, cu
     }
     // K / V rows (num_pages*Hkv*P of 256 B) seen as [groups of g rows] x
     // [2 halves] x [g rows] x [64 columns], g = 8 (K) or 16 (V); a box is CH =
-    // min(P, 128) consecutive rows of one page, landing group by group
+    // min(P, 128) consecutive rows of one page, landing group by group.
+    // INT8: rows of 128 bytes, a box CH rows as they are (the widening warps
+    // swizzle)
     const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv * a.P;
     const cuuint32_t ch = (cuuint32_t)(a.P < TN ? a.P : TN);
-    for (int t = 0; t < 2; ++t) {
+    const bool kv8 = a.kv_dtype == SPEC_DTYPE_I8;
+    for (int t = 0; t < 2 && kv8; ++t) {
+        cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+        cuuint64_t strides[1] = {(cuuint64_t)D};
+        cuuint32_t box[2] = {(cuuint32_t)D, ch};
+        cuuint32_t es[2] = {1, 1};
+        if (encode(t == 0 ? &kmap : &vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<void*>(t == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int t = 0; t < 2 && !kv8; ++t) {
         const cuuint32_t g = t == 0 ? 8 : 16;
         cuuint64_t dims[4] = {64, g, 2, rows / g};
         cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)g * D * 2};
@@ -749,12 +907,20 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, int num_ctas, void* workspace, cu
     prm.part_lse = prm.part_o + (size_t)2 * num_ctas * ROWS * D;
     prm.seg_rec = reinterpret_cast<int4*>(prm.part_lse + (size_t)2 * num_ctas * ROWS);
     prm.seg_pre = reinterpret_cast<int*>(prm.seg_rec + 2 * (size_t)num_ctas);
-    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(attn_tc2_kernel, dim3(num_ctas), dim3(12 * 32), SMEM_BYTES, stream, qmap,
-                         kmap, vmap, prm);
+    cudaError_t e;
+    if (kv8) {
+        e = cudaFuncSetAttribute(attn_tc2_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(attn_tc2_kernel<true>, dim3(num_ctas), dim3(threads<true>()),
+                             SMEM_BYTES, stream, qmap, kmap, vmap, prm);
+    } else {
+        e = cudaFuncSetAttribute(attn_tc2_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(attn_tc2_kernel<false>, dim3(num_ctas), dim3(threads<false>()),
+                             SMEM_BYTES, stream, qmap, kmap, vmap, prm);
+    }
     if (e != cudaSuccess) return e;
     return launch_combine_stream_k(a, num_ctas, tc2_split_alpha(a), prm.part_o, prm.part_lse,
                                    prm.seg_rec, prm.seg_pre, stream);

@@ -374,6 +374,15 @@ __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t start, uint32_t lb
     return d;
 }
 
+// Register budget of the calling warpgroup (all four warps execute it): the
+// count moves between warpgroups inside the block's launch allocation.
+template <uint32_t N> __device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N> __device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ persistent tile walk
 
 // Split of the tile list over the C CTAs of a persistent grid.  Every piece
@@ -521,6 +530,34 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Widens 16 int8 (one 16-byte chunk) to 16 fp16 (two chunks), exactly: the
+// byte u = c + 128 placed under the fp16 exponent of 1024 reads as 1024 + u,
+// and subtracting 1152 leaves c (every step exact in fp16).
+__device__ __forceinline__ void i8x16_to_f16(const uint4 r, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {r.x ^ 0x80808080u, r.y ^ 0x80808080u, r.z ^ 0x80808080u,
+                           r.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t e01 = __byte_perm(w[i], 0x64646464u, 0x4140);
+        const uint32_t e23 = __byte_perm(w[i], 0x64646464u, 0x4342);
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i]) : "r"(e01), "r"(0x64806480u));
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i + 1]) : "r"(e23), "r"(0x64806480u));
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// bf16 -> fp16 in place (8 values per 16-byte chunk), round to nearest even.
+__device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 r) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {

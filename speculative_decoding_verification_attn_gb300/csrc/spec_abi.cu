@@ -246,7 +246,8 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
     } else {
         const bool many_short = (int64_t)batch * num_kv_heads > ws->sms &&
                                 (int64_t)max_pages_per_seq * page_size < 3072;
-        kernel = mma_ok && (many_short || !tc2_ok) ? 3 : tc2_ok ? 5 : tc_ok ? 2 : small_ok ? 4 : 1;
+        const bool tc2_auto = tc2_ok && kv_dtype == SPEC_DTYPE_BF16;
+        kernel = mma_ok && (many_short || !tc2_auto) ? 3 : tc2_auto ? 5 : tc_ok ? 2 : small_ok ? 4 : 1;
     }
     if (kernel == 3 && (int64_t)batch * num_kv_heads > kMaxCounters)
         return fail(SPEC_ERR_UNSUPPORTED, "batch * num_kv_heads > %d for the warp-MMA kernel",

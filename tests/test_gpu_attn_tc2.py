@@ -1,7 +1,7 @@
 """GPU parity of the 128-key-tile tcgen05 kernel (attention path 5) with the oracle.
 
-The kernel takes bf16 queries and cache, head_dim 128 and up to 128 query
-rows per kv-head.  Cases span 128-key tile edges, ragged tails, contexts of zero,
+The kernel takes bf16 queries over a bf16 or INT8 cache (fp16 scales per
+key), head_dim 128 and up to 128 query rows per kv-head.  Cases span 128-key tile edges, ragged tails, contexts of zero,
 every page size it takes, one long segment, forced stream-K splits of every
 size (the combine in both its forms), charged splits, tree masks, and the
 shapes it must refuse.  NaN canaries fill every unused cache slot.
@@ -140,10 +140,10 @@ def test_tc128_close_to_tc64():
 
 @pytest.mark.parametrize("kw", [
     dict(num_q_heads=32, num_kv_heads=2, num_draft=9),                     # 144 rows
-    dict(num_q_heads=28, num_kv_heads=4, num_draft=16, kv_dtype="i8"),     # INT8 cache
     dict(num_q_heads=28, num_kv_heads=4, num_draft=16, head_dim=64),       # head_dim 64
     dict(num_q_heads=28, num_kv_heads=4, num_draft=16, q_dtype="f32", kv_dtype="f32"),
-], ids=["144rows", "i8", "d64", "f32"])
+    dict(num_q_heads=28, num_kv_heads=4, num_draft=16, page_size=8),       # pages of 8
+], ids=["144rows", "d64", "f32", "page8"])
 def test_tc128_refuses_other_shapes(kw):
     inp = make_inputs(small_spec(**kw), seed=88)
     t = binding.inputs_to_torch(inp)
@@ -153,3 +153,70 @@ def test_tc128_refuses_other_shapes(kw):
         binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
                                  t["ctx_lens"], inp.spec.num_draft, inp.scale, o["out"], o["lse"],
                                  t.get("k_scale"), t.get("v_scale"))
+
+
+I8_CASES = [
+    dict(num_q_heads=64, num_kv_heads=8, num_draft=8),                      # 64 rows
+    dict(num_q_heads=28, num_kv_heads=4, num_draft=16, page_size=32),       # 112 rows
+    dict(num_q_heads=8, num_kv_heads=2, num_draft=4),                       # 16 rows
+    dict(num_q_heads=4, num_kv_heads=2, num_draft=64),                      # 128 rows
+    dict(num_q_heads=16, num_kv_heads=2, num_draft=8, ctx=[0, 1, 127, 128, 129], batch=5),
+    dict(num_q_heads=16, num_kv_heads=2, num_draft=8, page_size=64, ctx=(1, 700)),
+    dict(num_q_heads=16, num_kv_heads=2, num_draft=8, page_size=256, ctx=(250, 1200), batch=2),
+    dict(batch=1, num_q_heads=64, num_kv_heads=8, num_draft=8, ctx=[5000]),  # one long segment
+    dict(batch=200, num_q_heads=28, num_kv_heads=4, num_draft=16, ctx=(0, 100)),  # many pieces
+]
+
+
+@pytest.mark.parametrize("kw", I8_CASES, ids=[str(i) for i in range(len(I8_CASES))])
+def test_tc128_int8(oracle_mod, kw):
+    inp = make_inputs(small_spec(kv_dtype="i8", **kw), seed=89)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, PATH)
+    check_attn_full(oracle_mod, inp, "i8 %s" % kw)
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 5, 37, 152, 400])
+def test_tc128_int8_stream_k_splits(oracle_mod, ctas):
+    inp = make_inputs(small_spec(batch=4, num_q_heads=64, num_kv_heads=8, num_draft=8,
+                                 kv_dtype="i8", ctx=(0, 1800)), seed=90)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, PATH)
+    binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
+    check_attn_full(oracle_mod, inp, "i8 ctas=%d" % ctas)
+
+
+def test_tc128_int8_close_to_tc64():
+    # dequantization to fp16 before the MMAs (128-key kernel) against the
+    # scales kept in fp32 (64-key kernel)
+    inp = make_inputs(small_spec(batch=6, num_q_heads=64, num_kv_heads=8, num_draft=8,
+                                 kv_dtype="i8", ctx=(0, 2500)), seed=91)
+    t = binding.inputs_to_torch(inp)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, PATH)
+    a_out, a_lse = gpu_attn(inp, t)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 2)
+    b_out, b_lse = gpu_attn(inp, t)
+    assert np.isfinite(a_out).all() and np.isfinite(a_lse).all()
+    assert np.abs(a_out - b_out).max() < 2e-2
+    assert np.abs(a_lse - b_lse).max() < 1e-3
+
+
+@pytest.mark.parametrize("width", [0.0, 0.5, 1.0])
+def test_tc128_int8_tree_masks(oracle_mod, width):
+    spec = small_spec(num_q_heads=28, num_kv_heads=4, num_draft=16, kv_dtype="i8")
+    inp = make_inputs(spec, seed=92)
+    masks = tree_masks(random_trees(spec.batch, spec.num_draft, seed=93, width=width))
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, PATH)
+    t = binding.inputs_to_torch(inp)
+    o = binding.alloc_outputs(inp)
+    o["out"].fill_(float("nan"))
+    o["lse"].fill_(float("nan"))
+    tm = torch.from_numpy(masks.view(np.int64)).cuda()
+    binding.spec_verify_attn_tree(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                  t["ctx_lens"], tm, spec.num_draft, inp.scale, o["out"],
+                                  o["lse"], t["k_scale"], t["v_scale"])
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_mod.verify_attn_tree(
+        inp.q, spec.q_dtype, inp.k_cache, inp.v_cache, spec.kv_dtype, inp.k_scale, inp.v_scale,
+        inp.block_table, inp.ctx_lens, inp.scale, masks)
+    assert_attn_close(o["out"].double().cpu().numpy(), o["lse"].double().cpu().numpy(), ref_out,
+                      ref_lse, tol_for(inp), "i8 tree width %s" % width)
+    assert binding.spec_device_error() == 0
