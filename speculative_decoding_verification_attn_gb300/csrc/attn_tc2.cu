@@ -86,19 +86,14 @@ using Cursor = CursorT<TN>;
 // of its 32 KB operand slot and is dequantized in place
 constexpr int RAW_OFF = SLOT_BYTES / 2;
 
-// NKS K slots; with 3 (long segments, few pieces per CTA) the Q of a piece
-// has one buffer and loads once the previous piece's last Q K^T is done,
-// with 2 two buffers let the next piece's Q load early
-template <int NKS>
-struct SmemT {
-    static constexpr int NQ = NKS == 3 ? 1 : 2;
-    static constexpr int Q = 0;                         // NQ buffers (piece % NQ)
-    static constexpr int KS = Q + NQ * Q_BYTES;         // NKS K slots
-    static constexpr int VS = KS + NKS * SLOT_BYTES;    // 2 V slots
+struct Smem {
+    static constexpr int Q = 0;                         // 2 buffers (piece parity)
+    static constexpr int KS = Q + 2 * Q_BYTES;          // 2 K slots
+    static constexpr int VS = KS + 2 * SLOT_BYTES;      // 2 V slots
     static constexpr int BARS = VS + 2 * SLOT_BYTES;
-    static constexpr int B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 8, B_QFULL = 10,
-                         B_QFREE = 12, B_SFULL = 14, B_PREADY = 16, B_SFREE = 18,
-                         B_EPI = 20, B_DRAIN = 21, B_KREADY = 23, B_VREADY = 25, NUM_BARS = 27;
+    static constexpr int B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8,
+                         B_QFREE = 10, B_SFULL = 12, B_PREADY = 14, B_SFREE = 16,
+                         B_EPI = 18, B_DRAIN = 19, B_KREADY = 21, B_VREADY = 23, NUM_BARS = 25;
     static constexpr int MISC = BARS + NUM_BARS * 8;    // tmem base, abort flag, range at +16
     static constexpr int STAT = MISC + 32;              // (m, l) of [set][row]
     static constexpr int PIDS = STAT + 2 * 2 * ROWS * 4;  // [2 producers][LOOKAHEAD+1][8] int
@@ -108,10 +103,8 @@ struct SmemT {
     static constexpr int SCRAW = (PRE + (MAX_BATCH + 1) * 4 + 127) / 128 * 128;
     static constexpr int END = SCRAW + 2 * 2 * TN * 2;
 };
-template <int NKS>
-constexpr size_t smem_bytes() { return SmemT<NKS>::END + 1024; }  // + alignment slack
-static_assert(smem_bytes<2>() <= 227 * 1024 && smem_bytes<3>() <= 227 * 1024,
-              "shared memory budget");
+constexpr size_t SMEM_BYTES = Smem::END + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Tc2Params {
     AttnArgs a;
@@ -190,13 +183,11 @@ __device__ __forceinline__ uint64_t visible64(int key0, int c0, int nvalid, int 
     return (cbits | dbits) & valid;
 }
 
-template <bool KV8, int NKS>
+template <bool KV8>
 __global__ void __launch_bounds__(threads<KV8>(), 1)
 attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const Tc2Params prm) {
-    static_assert(!KV8 || NKS == 2, "INT8: two K slots");
-    using Smem = SmemT<NKS>;
-    constexpr int NT = threads<KV8>(), NQ = Smem::NQ;
+    constexpr int NT = threads<KV8>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,11 +204,9 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const int CH = P < TN ? P : TN, NCH = TN / CH;  // keys per page chunk, chunks per tile
 
     if (tid == 0) {
-        for (int s = 0; s < NKS; ++s) {
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[Smem::B_KFULL + s], 1);
             mbar_init(&bars[Smem::B_KEMPTY + s], 1);
-        }
-        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[Smem::B_VFULL + s], 1);
             mbar_init(&bars[Smem::B_VEMPTY + s], 1);
             mbar_init(&bars[Smem::B_QFULL + s], 1);
@@ -243,9 +232,9 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         tmem_relinquish();
     }
     {
-        // Q rows R..127 stay zero in every buffer (the TMA writes rows < R)
+        // Q rows R..127 stay zero in both buffers (the TMA writes rows < R)
         uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q);
-        for (int e = tid; e < NQ * Q_BYTES / 16; e += NT) {
+        for (int e = tid; e < 2 * Q_BYTES / 16; e += NT) {
             const int row = (e % (Q_HALF / 16)) / 8;
             if (row >= R) q4[e] = make_uint4(0, 0, 0, 0);
         }
@@ -317,9 +306,9 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     if constexpr (KV8) regs_dec<80>();
     if (warp == 5 || warp == 6) {
         // ================= TMA producers: warp 5 K, warp 6 V, every tile =================
-        // Tile it goes to K slot it % NKS and V slot it % 2: its K slot is
-        // free once Q K^T of tile it - NKS read it, its V slot once P V of
-        // tile it - 2 did, so a K copy never waits on a P V.  A tile is NCH chunks of CH
+        // Tile it goes to slot it % 2 of each ring: its K slot is free once
+        // Q K^T of tile it - 2 read it, its V slot once P V of tile it - 2
+        // did, so a K copy never waits on a P V.  A tile is NCH chunks of CH
         // = min(P, 128) keys, each inside one page (CH * 256 contiguous bytes
         // of the cache), and each chunk is one copy: K as 8-key groups, each
         // [half][8 rows][128 B] (2 KB), the layout an N = 128 Q K^T reads; V
@@ -358,7 +347,6 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
         int n_issued = 0;
         bool ok = true;
-        const int nsl = is_v ? 2 : NKS;  // slots of this ring
         for (int it = 0; it < n_tiles && ok; ++it) {
             if (it + LOOKAHEAD < n_tiles) {
                 fetch_pids((it + LOOKAHEAD) % (LOOKAHEAD + 1), ahead);
@@ -371,8 +359,8 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const int key0 = cur.lt * TN;
             const int nvalid = min(TN, s_ctx[cur.b] + k - key0);
             const int nck = (nvalid + CH - 1) / CH;  // chunks holding keys of the tile
-            const int s = it % nsl, use = it / nsl;
-            if (use >= 1) ok = warp_wait(&empty[s], (use - 1) & 1, abort_flag, a.dev_err);
+            const int s = it & 1;
+            if (it >= 2) ok = warp_wait(&empty[s], ((it >> 1) - 1) & 1, abort_flag, a.dev_err);
             const uint32_t bytes = (uint32_t)(nck * CH) * (KV8 ? 128u + 2u : 256u);
             if (ok && lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
             __syncwarp();
@@ -401,8 +389,10 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         cp_async_wait<0>();
         if (!ok && lane == 0) {
             // the latest copy into each slot lands before the CTA exits
-            for (int j = max(0, n_issued - nsl); j < n_issued; ++j)
-                mbar_drain(&full[j % nsl], (j / nsl) & 1);
+            for (int sl = 0; sl < 2; ++sl) {
+                const int last = (n_issued - 1) - (((n_issued - 1) - sl) & 1);
+                if (last >= 0) mbar_drain(&full[sl], (last >> 1) & 1);
+            }
         }
     } else if (warp == 4) {
         // ================= Q loads and Q K^T issue =================
@@ -412,22 +402,21 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             int pc = -1;                  // piece of the current tile
             int q_issued = 0;             // pieces whose Q load went out
             bool ok = true;
-            auto issue_q = [&](int j, int b, int kvh) {  // lane 0: piece j into buffer j % NQ
-                uint64_t* bar = &bars[Smem::B_QFULL + j % NQ];
+            auto issue_q = [&](int j, int b, int kvh) {  // lane 0: piece j into buffer j & 1
+                uint64_t* bar = &bars[Smem::B_QFULL + (j & 1)];
                 mbar_arrive_expect_tx(bar, 2 * R * 128);
                 for (int h = 0; h < 2; ++h)
-                    tma_load_3d(sm + Smem::Q + (j % NQ) * Q_BYTES + h * Q_HALF, &qmap, bar, h * 64,
+                    tma_load_3d(sm + Smem::Q + (j & 1) * Q_BYTES + h * Q_HALF, &qmap, bar, h * 64,
                                 kvh * G, b * k);
             };
-            const bool two_ahead = NQ == 2 && has_next_piece(cur);
             if (lane == 0) {
                 prefetch_tmap(&qmap);
                 issue_q(0, cur.b, cur.kvh);
-                if (two_ahead)
+                if (has_next_piece(cur))
                     issue_q(1, cur.kvh + 1 < Hkv ? cur.b : cur.b + 1,
                             cur.kvh + 1 < Hkv ? cur.kvh + 1 : 0);
             }
-            q_issued = two_ahead ? 2 : 1;
+            q_issued = has_next_piece(cur) ? 2 : 1;
             const uint64_t qdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::Q), 16, 1024);
             const uint64_t kdesc0 = umma_sdesc_sw128(smem_u32(sm + Smem::KS), 16, 2048);
             for (int it = 0; it < n_tiles && ok; ++it) {
@@ -436,39 +425,33 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 const int s = it & 1;
                 if (first) {
                     ++pc;
-                    // piece j = pc + NQ - 1 takes the buffer of piece pc - 1,
-                    // whose last Q K^T was committed to QFREE (NQ = 2: the
-                    // next piece, if any; NQ = 1: this one)
-                    const int j = pc + NQ - 1;
-                    if (pc >= 1 && q_issued == j && (NQ == 1 || has_next_piece(cur))) {
-                        ok = warp_wait(&bars[Smem::B_QFREE + (pc - 1) % NQ], ((pc - 1) / NQ) & 1,
+                    // the piece after the next reuses the buffer of piece
+                    // pc - 1, whose last Q K^T was committed to QFREE
+                    if (pc >= 1 && q_issued == pc + 1 && has_next_piece(cur)) {
+                        ok = warp_wait(&bars[Smem::B_QFREE + ((pc - 1) & 1)], ((pc - 1) >> 1) & 1,
                                        abort_flag, a.dev_err);
-                        if (ok && lane == 0) {
-                            if (NQ == 1) issue_q(j, cur.b, cur.kvh);
-                            else
-                                issue_q(j, cur.kvh + 1 < Hkv ? cur.b : cur.b + 1,
-                                        cur.kvh + 1 < Hkv ? cur.kvh + 1 : 0);
-                        }
+                        if (ok && lane == 0)
+                            issue_q(pc + 1, cur.kvh + 1 < Hkv ? cur.b : cur.b + 1,
+                                    cur.kvh + 1 < Hkv ? cur.kvh + 1 : 0);
                         __syncwarp();
-                        q_issued = j + 1;
+                        q_issued = pc + 2;
                         if (!ok) break;
                     }
-                    ok = warp_wait(&bars[Smem::B_QFULL + pc % NQ], (pc / NQ) & 1, abort_flag,
+                    ok = warp_wait(&bars[Smem::B_QFULL + (pc & 1)], (pc >> 1) & 1, abort_flag,
                                    a.dev_err);
                     if (!ok) break;
                     if constexpr (KV8) {
                         // the piece's q to fp16, in place (rows < R; the rest are zero)
-                        uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q + (pc % NQ) * Q_BYTES);
+                        uint4* q4 = reinterpret_cast<uint4*>(sm + Smem::Q + (pc & 1) * Q_BYTES);
                         for (int e = lane; e < Q_BYTES / 16; e += 32)
                             if ((e % (Q_HALF / 16)) / 8 < R) q4[e] = bf16x8_to_f16(q4[e]);
                         fence_proxy_async_smem();
                         __syncwarp();
                     }
                 }
-                // K of tile it landed in slot it % NKS (INT8: widened); S
-                // buffer s free (P V of tile it - 2 done)
-                const int ks = it % NKS;
-                ok = warp_wait(&bars[(KV8 ? Smem::B_KREADY : Smem::B_KFULL) + ks], (it / NKS) & 1,
+                // K of tile it landed (INT8: widened); S buffer s free (P V of
+                // tile it - 2 done)
+                ok = warp_wait(&bars[(KV8 ? Smem::B_KREADY : Smem::B_KFULL) + s], (it >> 1) & 1,
                                abort_flag, a.dev_err);
                 if (ok && it >= 2)
                     ok = warp_wait(&bars[Smem::B_SFREE + s], ((it >> 1) - 1) & 1, abort_flag,
@@ -479,8 +462,8 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 {
                     // S = Q K^T: k-slice kk at half kk/4 (Q: 16 KB on, K: 1 KB on
                     // in every 8-key group), 32-byte step kk%4
-                    const uint64_t qd = qdesc0 + ((uint32_t)((pc % NQ) * Q_BYTES) >> 4);
-                    const uint64_t kd = kdesc0 + ((uint32_t)(ks * SLOT_BYTES) >> 4);
+                    const uint64_t qd = qdesc0 + ((uint32_t)((pc & 1) * Q_BYTES) >> 4);
+                    const uint64_t kd = kdesc0 + ((uint32_t)(s * SLOT_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         umma_ss_w(tmem + TM_S + s * TN,
@@ -488,16 +471,16 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                                   kd + (kk >> 2) * (1024 >> 4) + (kk & 3) * 2, idesc_qk<KV8>(),
                                   kk ? 1u : 0u);
                     umma_commit_w(&bars[Smem::B_SFULL + s]);
-                    umma_commit_w(&bars[Smem::B_KEMPTY + ks]);
-                    if (last) umma_commit_w(&bars[Smem::B_QFREE + pc % NQ]);
+                    umma_commit_w(&bars[Smem::B_KEMPTY + s]);
+                    if (last) umma_commit_w(&bars[Smem::B_QFREE + (pc & 1)]);
                 }
                 if (it + 1 < n_tiles) cur.next(s_ctx, Hkv, k);
             }
             // Q loads in flight land before the CTA exits (loads of one buffer
             // complete in order)
             if (!ok && lane == 0)
-                for (int j = max(0, q_issued - NQ); j < q_issued; ++j)
-                    mbar_drain(&bars[Smem::B_QFULL + j % NQ], (j / NQ) & 1);
+                for (int j = max(0, q_issued - 2); j < q_issued; ++j)
+                    mbar_drain(&bars[Smem::B_QFULL + (j & 1)], (j >> 1) & 1);
             // every tensor-core op of this warp finishes before TMEM is released
             __syncwarp();
             umma_commit_w(&bars[Smem::B_DRAIN]);
@@ -848,18 +831,6 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-template <bool KV8, int NKS>
-cudaError_t launch_variant(const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, const Tc2Params& prm, int num_ctas,
-                           cudaStream_t stream) {
-    constexpr size_t smem = smem_bytes<NKS>();
-    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel<KV8, NKS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(attn_tc2_kernel<KV8, NKS>, dim3(num_ctas), dim3(threads<KV8>()), smem,
-                            stream, qmap, kmap, vmap, prm);
-}
-
 }  // namespace
 
 bool tc2_supported(const AttnArgs& a) {
@@ -936,12 +907,20 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, int num_ctas, void* workspace, cu
     prm.part_lse = prm.part_o + (size_t)2 * num_ctas * ROWS * D;
     prm.seg_rec = reinterpret_cast<int4*>(prm.part_lse + (size_t)2 * num_ctas * ROWS);
     prm.seg_pre = reinterpret_cast<int*>(prm.seg_rec + 2 * (size_t)num_ctas);
-    // bf16 with at most one segment per CTA (so at most two pieces each): a
-    // third K slot is worth more than loading the next piece's Q early
-    const bool three_k = !kv8 && (int64_t)a.B * a.Hkv <= num_ctas;
-    cudaError_t e = kv8       ? launch_variant<true, 2>(qmap, kmap, vmap, prm, num_ctas, stream)
-                    : three_k ? launch_variant<false, 3>(qmap, kmap, vmap, prm, num_ctas, stream)
-                              : launch_variant<false, 2>(qmap, kmap, vmap, prm, num_ctas, stream);
+    cudaError_t e;
+    if (kv8) {
+        e = cudaFuncSetAttribute(attn_tc2_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(attn_tc2_kernel<true>, dim3(num_ctas), dim3(threads<true>()),
+                             SMEM_BYTES, stream, qmap, kmap, vmap, prm);
+    } else {
+        e = cudaFuncSetAttribute(attn_tc2_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(attn_tc2_kernel<false>, dim3(num_ctas), dim3(threads<false>()),
+                             SMEM_BYTES, stream, qmap, kmap, vmap, prm);
+    }
     if (e != cudaSuccess) return e;
     return launch_combine_stream_k(a, num_ctas, tc2_split_alpha(a), prm.part_o, prm.part_lse,
                                    prm.seg_rec, prm.seg_pre, stream);
