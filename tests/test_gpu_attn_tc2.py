@@ -1,7 +1,8 @@
 """GPU parity of the 128-key-tile tcgen05 kernel (attention path 5) with the oracle.
 
 The kernel takes bf16 queries over a bf16 or INT8 cache (fp16 scales per
-key), head_dim 128 and up to 128 query rows per kv-head.  Cases span 128-key tile edges, ragged tails, contexts of zero,
+key), head_dim 128 and up to 128 query rows per kv-head.  Cases span 128-key
+tile edges, ragged tails, contexts of zero,
 every page size it takes, one long segment, forced stream-K splits of every
 size (the combine in both its forms), charged splits, tree masks, and the
 shapes it must refuse.  NaN canaries fill every unused cache slot.
@@ -220,3 +221,20 @@ def test_tc128_int8_tree_masks(oracle_mod, width):
     assert_attn_close(o["out"].double().cpu().numpy(), o["lse"].double().cpu().numpy(), ref_out,
                       ref_lse, tol_for(inp), "i8 tree width %s" % width)
     assert binding.spec_device_error() == 0
+
+
+# more (sequence, kv-head) segments than CTAs, ragged lengths and one long
+# sequence among short ones (a segment over many CTAs): the combine in its
+# by-boundary form; two calls in a row give the same bits
+@pytest.mark.parametrize("ctx", [(0, 4000), [9000] + [50] * 47], ids=["ragged", "one_long"])
+@pytest.mark.parametrize("ctas", [37, 100, 152])
+def test_tc128_many_segments(oracle_mod, ctx, ctas):
+    inp = make_inputs(small_spec(batch=48, num_q_heads=28, num_kv_heads=4, num_draft=12,
+                                 ctx=ctx), seed=94)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, PATH)
+    binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, ctas)
+    t = binding.inputs_to_torch(inp)
+    first, _ = gpu_attn(inp, t)
+    check_attn_full(oracle_mod, inp, "many segments ctas=%d" % ctas)
+    again, _ = gpu_attn(inp, t)
+    assert np.array_equal(first, again)
