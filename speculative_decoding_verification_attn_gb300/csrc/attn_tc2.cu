@@ -10,11 +10,11 @@
 // q-heads g*G .. g*G+G-1.  All R = k*G query rows of a (sequence, kv-head)
 // are the M side of one 128-row MMA, so every K/V byte is read once.
 //
-// Design.  With this many rows the 64-key-tile kernel is paced by its
-// hand-offs (each tile: 8 Q K^T and 4 P V MMAs, two commits, a softmax
-// set barrier and a P V issue from a softmax warp).  Here a tile is 128 keys:
-// Q K^T is 8 MMAs of N = 128 (A = Q from shared memory, B = K boxes), and the
-// hand-offs per key halve.
+// Design.  The 64-key-tile kernel is paced by its hand-offs (each tile: 8
+// Q K^T and 4 P V MMAs, two commits, a softmax set barrier and a P V issue
+// from a softmax warp).  Here a tile is 128 keys: Q K^T is 8 MMAs of N = 128
+// (A = Q from shared memory, B = K in 8-key groups, one TMA copy per page
+// chunk), and the hand-offs per key halve.
 //  * TMEM (512 columns): S of set 0 [0,128), S of set 1 [128,256), O of set 0
 //    [256,384), O of set 1 [384,512).  P (bf16) is written over the S columns
 //    it came from: keys 0..63 to columns [0,32), keys 64..127 to [64,96) of
@@ -33,8 +33,9 @@
 //  * INT8 cache (per-key fp16 scales): the producers land the raw int8 tile
 //    in the upper half of its operand slot and its scales in a small stage;
 //    four more warps (12-13 K, 14-15 V) dequantize it in place to fp16
-//    (int8 * scale, one rounding) in the layout the MMAs read.  q is turned to fp16 in
-//    place once per piece and P is packed as fp16, so A and B share a type.
+//    (int8 * scale, one rounding) in the layout the MMAs read.  q is turned
+//    to fp16 in place once per piece and P is packed as fp16, so A and B
+//    share a type.
 //    The 16 warps share the 64K registers of the block unevenly
 //    (setmaxnreg): softmax 160 each, issue / copy 80, dequantization 112.
 //  * Every mbarrier wait is bounded (1 s); a timeout sets the device error
