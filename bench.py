@@ -3,7 +3,9 @@
 One step = spec_verify_attn + spec_accept_greedy over one batch of a named
 synthetic workload (default: the largest one, the ragged GQA 8B-target bf16
 shape -- batch 32, 32 q / 8 kv heads, head_dim 128, contexts uniform in
-[1024, 8192], k = 4, page size 16, vocab 128256).
+[1024, 8192], k = 4, page size 16, vocab 128256).  The two calls are
+independent, so the acceptance runs on a second stream beside the attention
+(forked and joined every step; --no-overlap: one stream, in order).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the float64 CPU oracle, same metric
@@ -374,12 +376,32 @@ def run_gpu(args, inp, world, rank, local):
             binding.spec_accept_greedy(t["logits"], t["draft_tokens"], k, o["accepted_len"],
                                        o["next_token"])
 
-    def step(j):
-        t, o = sets[j % n_sets], outs[j % n_sets]
+    # The two calls of a step are independent (acceptance reads only the
+    # logits and the drafts), so by default the acceptance runs on a second
+    # stream forked before the attention call and joined after it, and takes
+    # the SMs the attention's tail leaves free; --no-overlap runs the two in
+    # order on one stream.
+    side = torch.cuda.Stream(device)
+    fork_ev = [torch.cuda.Event() for _ in range(2)]
+    join_ev = [torch.cuda.Event() for _ in range(2)]
+
+    def compute(t, o, j):
+        if args.overlap:
+            fork_ev[j & 1].record(stream)
+            side.wait_event(fork_ev[j & 1])
         binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
                                  t["ctx_lens"], k, scale, o["out"], o["lse"],
                                  t.get("k_scale"), t.get("v_scale"))
-        accept(t, o, j)
+        if args.overlap:
+            with torch.cuda.stream(side):
+                accept(t, o, j)
+            join_ev[j & 1].record(side)
+            stream.wait_event(join_ev[j & 1])
+        else:
+            accept(t, o, j)
+
+    def step(j):
+        compute(sets[j % n_sets], outs[j % n_sets], j)
 
     for j in range(max(args.warmup, 3)):
         step(j)
@@ -464,7 +486,10 @@ def run_gpu(args, inp, world, rank, local):
     # (every input set holds the same values, so any set's results serve)
     gained = int((outs[0]["accepted_len"].long() + 1).sum().item())
     accepted_tok_s = gained * world / slowest_step_s
-    timing = {"timed_region": "K steps between one event pair (value, ms_per_step)",
+    timing = {"step": ("acceptance on a second stream forked before the attention call and "
+                       "joined after it" if args.overlap else
+                       "attention then acceptance on one stream"),
+              "timed_region": "K steps between one event pair (value, ms_per_step)",
               "breakdown_region": "%d steps, an event pair around each call" % reps,
               "kernel_regions": "K attention calls, then K acceptance calls, back to back "
                                 "between one event pair each (roofline attn_ms / accept_ms)",
@@ -533,11 +558,7 @@ def run_gpu(args, inp, world, rank, local):
             stream.wait_event(ev_in)
             if read[i] is not None:
                 stream.wait_event(read[i])
-            t, o = e_sets[i], e_outs[i]
-            binding.spec_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
-                                     t["ctx_lens"], k, scale, o["out"], o["lse"],
-                                     t.get("k_scale"), t.get("v_scale"))
-            accept(t, o, j)
+            compute(e_sets[i], e_outs[i], j)
             done[i] = torch.cuda.Event()
             done[i].record(stream)
             read[i] = torch.cuda.Event()
@@ -725,6 +746,9 @@ def main(argv=None):
                     help="sweeps: persistent CTAs of the tensor-core kernels (0 = one per SM)")
     ap.add_argument("--split-weight", type=int, default=0,
                     help="sweeps: SPEC_OPT_SPLIT_WEIGHT (0 = the kernels' default)")
+    ap.add_argument("--no-overlap", dest="overlap", action="store_false",
+                    help="run a step's acceptance after its attention on one stream (default: "
+                         "on a second stream beside it)")
     args = ap.parse_args(argv)
 
     world, rank, local = dist_env()
