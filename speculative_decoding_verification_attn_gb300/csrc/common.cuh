@@ -80,25 +80,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete.  Gives up when the
-// CTA-wide abort flag is raised by another role, or after kWaitLimitNs, in
-// which case it raises the abort flag and the device timeout error.
-// Returns true when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* dev_err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            raise_device_error(dev_err, SPEC_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -159,12 +140,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -191,48 +166,14 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Copy a 128-row x 256-bit matrix (described by a smem descriptor) into TMEM
-// lanes 0..127, 8 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-// Warp-collective forms of the three issue instructions: the whole warp
-// runs them, converged and with warp-uniform operands, and elect.sync picks
-// the one lane (the lowest) that issues.  Issued from a converged warp the
-// operands stay in the uniform datapath; from a one-lane branch with
-// operands computed at run time each instruction costs several times more
-// issue cycles.  The commit must come from the same warp as the ops it
-// tracks (the same elected lane).
+// The tcgen05 issue instructions, run by a whole converged warp with
+// warp-uniform operands; elect.sync picks the one lane (the lowest) that
+// issues.  Issued that way the operands stay in the uniform datapath; from a
+// one-lane branch with operands computed at run time each instruction costs
+// several times more issue cycles.  ts: A from TMEM; ss: A from shared
+// memory; commit: arrive on `bar` once every tcgen05 op this thread issued
+// is done (it must come from the warp that issued them); cp: a 128-row x
+// 256-bit matrix (a shared-memory descriptor) into TMEM lanes 0..127.
 __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -614,7 +555,9 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 // step and every decision is a warp vote, so the warp leaves converged.  A
 // wait spun by one lane while the others park leaves the warp split, and the
 // tcgen05.mma issued right after it (elect.sync) then issues several times
-// slower for the rest of the batch.  Gives up like mbar_wait.
+// slower for the rest of the batch.  Gives up when the CTA-wide abort flag
+// is raised by another role, or after kWaitLimitNs, when it raises the abort
+// flag and the device timeout error.  Returns true when the phase completed.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* dev_err) {
     constexpr uint32_t kAll = 0xffffffffu;
