@@ -619,6 +619,8 @@ def run_gpu(args, inp, world, rank, local):
     if args.num_ctas or args.split_weight:
         line["config"]["num_ctas"] = args.num_ctas
         line["config"]["split_weight"] = args.split_weight
+    if args.small_cluster:
+        line["config"]["small_cluster"] = args.small_cluster
     if rank == 0 and not args.no_cpu_baseline and not rejection:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
     if rank == 0:
@@ -746,6 +748,9 @@ def main(argv=None):
                     help="sweeps: persistent CTAs of the tensor-core kernels (0 = one per SM)")
     ap.add_argument("--split-weight", type=int, default=0,
                     help="sweeps: SPEC_OPT_SPLIT_WEIGHT (0 = the kernels' default)")
+    ap.add_argument("--small-cluster", type=int, default=0,
+                    help="sweeps: SPEC_OPT_SMALL_CLUSTER, CTAs per unit of the single-pass "
+                         "kernel (0 = automatic, 1 = no cluster)")
     ap.add_argument("--no-overlap", dest="overlap", action="store_false",
                     help="run a step's acceptance after its attention on one stream (default: "
                          "on a second stream beside it)")
@@ -763,10 +768,11 @@ def main(argv=None):
     import __graft_entry__
     __graft_entry__.build()
     inp = make_inputs(workload_spec(args), args.seed, canary=False)
-    if args.num_ctas or args.split_weight:
+    if args.num_ctas or args.split_weight or args.small_cluster:
         from speculative_decoding_verification_attn_gb300 import binding
         binding.spec_set_option(binding.SPEC_OPT_NUM_CTAS, args.num_ctas)
         binding.spec_set_option(binding.SPEC_OPT_SPLIT_WEIGHT, args.split_weight)
+        binding.spec_set_option(binding.SPEC_OPT_SMALL_CLUSTER, args.small_cluster)
     if args.codec:
         if rank == 0:
             run_codec(args, inp)

@@ -98,7 +98,14 @@ enum {
     /* tensor-core kernels: tiles charged per (sequence, kv-head) segment when
      * the tile list is split over the persistent CTAs (a segment piece's
      * fixed work); 0 = each kernel's default, v in [1, 257] = v - 1 tiles */
-    SPEC_OPT_SPLIT_WEIGHT = 4
+    SPEC_OPT_SPLIT_WEIGHT = 4,
+    /* single-pass SIMT kernel: CTAs (one thread-block cluster) that share each
+     * (sequence, kv-head, query-row group), merging their softmax states
+     * through distributed shared memory; 0 = automatic (a cluster of up to 8
+     * while the clusters fit the SMs and every CTA keeps >= 16 keys of the
+     * block table; one CTA when the device cannot place it), 1..8 = forced
+     * (a cluster the device cannot place fails the call with SPEC_ERR_CUDA) */
+    SPEC_OPT_SMALL_CLUSTER = 5
 };
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -21,6 +21,8 @@ SPEC_DTYPE_F32, SPEC_DTYPE_BF16, SPEC_DTYPE_F16, SPEC_DTYPE_I8, SPEC_DTYPE_I32 =
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, -1, -2, -3
 SPEC_OPT_ATTN_PATH, SPEC_OPT_NUM_CTAS, SPEC_OPT_VALIDATE, SPEC_OPT_SIMT_CHUNK = 0, 1, 2, 3
 SPEC_OPT_SPLIT_WEIGHT = 4
+SPEC_OPT_SMALL_CLUSTER = 5
+NUM_OPTIONS = 6
 SPEC_DEVERR_PAGE, SPEC_DEVERR_CTX, SPEC_DEVERR_TIMEOUT, SPEC_DEVERR_TOKEN = 1, 2, 4, 8
 SPEC_DEVERR_TREE = 16
 SPEC_DEVERR_CODEC = 32

@@ -59,7 +59,12 @@ cudaError_t launch_attn_simt(const AttnArgs& a, const SimtPlan& p, void* workspa
 // Longest context it holds (the whole block table of a sequence), or 0 when
 // the call does not fit its shared-memory plan.
 int small_attn_max_keys(const AttnArgs& a);
-cudaError_t launch_attn_small(const AttnArgs& a, cudaStream_t stream);
+// CTAs (one cluster) per (sequence, kv-head, row group) the automatic choice takes.
+int small_attn_cluster_size(const AttnArgs& a, int num_sms);
+// `cluster` = CTAs per unit, 1..8, or 0 for the automatic choice (which falls
+// back to one CTA when the device cannot place the cluster; a forced size
+// returns the launch error instead).
+cudaError_t launch_attn_small(const AttnArgs& a, int num_sms, int cluster, cudaStream_t stream);
 
 // ---- tensor-core kernel (tcgen05 + TMA, persistent, split-KV stream-K) ----
 bool tc_supported(const AttnArgs& a);

@@ -34,7 +34,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 std::atomic<int64_t> g_opt_path{0}, g_opt_ctas{0}, g_opt_validate{0}, g_opt_simt_chunk{0},
-    g_opt_split{0};
+    g_opt_split{0}, g_opt_small_cluster{0};
 
 // Per-device workspace: [error word | acceptance tickets | segment counters |
 // scratch].  The header is zeroed at allocation; tickets and counters are
@@ -160,6 +160,10 @@ int spec_set_option(int32_t option, int64_t value) {
         if (value < 0 || value > 257) return fail(SPEC_ERR_INVALID, "split weight out of range");
         g_opt_split = value;
         return SPEC_OK;
+    case SPEC_OPT_SMALL_CLUSTER:
+        if (value < 0 || value > 8) return fail(SPEC_ERR_INVALID, "small cluster must be 0..8");
+        g_opt_small_cluster = value;
+        return SPEC_OK;
     default:
         return fail(SPEC_ERR_INVALID, "unknown option %d", option);
     }
@@ -272,7 +276,7 @@ int verify_attn_impl(const void* q, const void* k_cache, const void* v_cache, co
         if (e != cudaSuccess) return cuda_fail(e, "verify_attn (tensor-core) launch");
     } else if (kernel == 4) {
         a.dev_err = static_cast<int*>(ws->base);
-        e = specv::launch_attn_small(a, st);
+        e = specv::launch_attn_small(a, ws->sms, (int)g_opt_small_cluster.load(), st);
         if (e != cudaSuccess) return cuda_fail(e, "verify_attn (single-pass SIMT) launch");
     } else {
         const specv::SimtPlan p = specv::simt_plan(a, ws->sms, (int)g_opt_simt_chunk.load());

@@ -177,6 +177,12 @@ def test_options(lib):
     assert lib.spec_set_option(4, -1) == -1
     assert lib.spec_set_option(4, 7) == 0
     assert lib.spec_set_option(4, 0) == 0
+    # single-pass cluster size: 0 = automatic, 1..8 forced
+    assert lib.spec_set_option(5, 9) == -1
+    assert lib.spec_set_option(5, -1) == -1
+    assert lib.spec_set_option(5, 8) == 0
+    assert lib.spec_set_option(5, 0) == 0
+    assert lib.spec_set_option(6, 0) == -1
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

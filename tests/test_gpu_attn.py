@@ -31,10 +31,10 @@ def _defaults():
     from speculative_decoding_verification_attn_gb300 import build
     build.build()
     binding.load()
-    for opt in range(5):
+    for opt in range(binding.NUM_OPTIONS):
         binding.spec_set_option(opt, 0)
     yield
-    for opt in range(5):
+    for opt in range(binding.NUM_OPTIONS):
         binding.spec_set_option(opt, 0)
 
 
@@ -201,6 +201,42 @@ def test_single_pass_simt(oracle_mod, kw):
     inp = make_inputs(small_spec(**kw), seed=35)
     binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 4)
     check_attn_full(oracle_mod, inp, "single pass %s" % kw)
+
+
+# the same kernel with each unit's keys split over a thread-block cluster
+# (forced sizes, 5 not a power of two; ctx 0 leaves CTAs without keys)
+CLUSTER_CASES = [
+    dict(q_dtype="f32", kv_dtype="f32", head_dim=64, batch=1, num_q_heads=2, num_kv_heads=2,
+         ctx=[128], num_draft=4),
+    dict(q_dtype="f32", kv_dtype="f32", head_dim=64, batch=4, ctx=[0, 1, 7, 200]),
+    dict(ctx=(0, 150)),                                                       # bf16
+    dict(kv_dtype="i8", num_q_heads=16, num_kv_heads=2, num_draft=8, ctx=(0, 100)),  # 64 rows
+    dict(q_dtype="f32", kv_dtype="i8", head_dim=256, num_draft=2, ctx=(0, 60)),
+    dict(q_dtype="bf16", kv_dtype="f32", head_dim=32, page_size=5, ctx=(0, 77)),
+    dict(num_q_heads=4, num_kv_heads=2, num_draft=64, ctx=(0, 40)),          # 128 rows: 2 groups
+    dict(q_dtype="f32", kv_dtype="f32", head_dim=64, batch=2, ctx=[200, 250], num_draft=6),
+]
+
+
+@pytest.mark.parametrize("cluster", [2, 5, 8])
+@pytest.mark.parametrize("kw", CLUSTER_CASES, ids=[str(i) for i in range(len(CLUSTER_CASES))])
+def test_single_pass_cluster(oracle_mod, kw, cluster):
+    inp = make_inputs(small_spec(**kw), seed=37)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 4)
+    binding.spec_set_option(binding.SPEC_OPT_SMALL_CLUSTER, cluster)
+    check_attn_full(oracle_mod, inp, "single pass, cluster %d, %s" % (cluster, kw))
+
+
+def test_single_pass_cluster_matches_one_cta():
+    # automatic (a cluster of 8 on this few units) against one CTA per unit
+    inp = make_inputs("tiny_fp32", seed=3)
+    t = binding.inputs_to_torch(inp)
+    binding.spec_set_option(binding.SPEC_OPT_ATTN_PATH, 4)
+    a_out, a_lse = gpu_attn(inp, t)
+    binding.spec_set_option(binding.SPEC_OPT_SMALL_CLUSTER, 1)
+    b_out, b_lse = gpu_attn(inp, t)
+    assert np.abs(a_out - b_out).max() < 1e-5
+    assert np.abs(a_lse - b_lse).max() < 1e-5
 
 
 def test_single_pass_refuses_long_tables():

@@ -29,10 +29,10 @@ def _defaults():
     from speculative_decoding_verification_attn_gb300 import build
     build.build()
     binding.load()
-    for opt in range(5):
+    for opt in range(binding.NUM_OPTIONS):
         binding.spec_set_option(opt, 0)
     yield
-    for opt in range(5):
+    for opt in range(binding.NUM_OPTIONS):
         binding.spec_set_option(opt, 0)
 
 
