@@ -541,32 +541,35 @@ def run_gpu(args, inp, world, rank, local):
     e_sets = [dict(sets[i], **views(d_in[i], in_offs, h_in)) for i in range(n_sets)]
     e_outs = [views(d_out[i], out_offs, outs[0]) for i in range(n_sets)]
     h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    # per input set: its upload, the compute of its last step (inputs
+    # consumed) and the read-back of that step (outputs free).  Created once:
+    # a wait takes the event's most recent record, so re-recording is safe.
+    ev_in = [torch.cuda.Event() for _ in range(n_sets)]
+    ev_done = [torch.cuda.Event() for _ in range(n_sets)]
+    ev_read = [torch.cuda.Event() for _ in range(n_sets)]
 
     def e2e_run(n_steps, start_event=None):
-        done = [None] * n_sets  # compute of the set's last step (its inputs consumed)
-        read = [None] * n_sets  # read-back of the set's last step (its outputs free)
+        used = [False] * n_sets
         if start_event is not None:
             h2d_s.wait_event(start_event)
         for j in range(n_steps):
             i = j % n_sets
-            ev_in = torch.cuda.Event()
             with torch.cuda.stream(h2d_s):
-                if done[i] is not None:
-                    h2d_s.wait_event(done[i])
+                if used[i]:
+                    h2d_s.wait_event(ev_done[i])
                 d_in[i].copy_(h_in_pack, non_blocking=True)
-                ev_in.record(h2d_s)
-            stream.wait_event(ev_in)
-            if read[i] is not None:
-                stream.wait_event(read[i])
+                ev_in[i].record(h2d_s)
+            stream.wait_event(ev_in[i])
+            if used[i]:
+                stream.wait_event(ev_read[i])
             compute(e_sets[i], e_outs[i], j)
-            done[i] = torch.cuda.Event()
-            done[i].record(stream)
-            read[i] = torch.cuda.Event()
+            ev_done[i].record(stream)
             with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(done[i])
+                d2h_s.wait_event(ev_done[i])
                 h_out_pack.copy_(d_out[i], non_blocking=True)
-                read[i].record(d2h_s)
-        return read[(n_steps - 1) % n_sets]
+                ev_read[i].record(d2h_s)
+            used[i] = True
+        return ev_read[(n_steps - 1) % n_sets]
 
     e2e_run(max(args.warmup, 3))
     torch.cuda.synchronize()
