@@ -100,7 +100,7 @@ attn_small_kernel(AttnArgs a, int Lcap, int RG, int row_groups, int csize) {
     int* pages = reinterpret_cast<int*>(rm + RG);
 
     // ---- round trip 1, all loads independent: the context length, every
-    // block-table entry of the sequence (the used ones are checked below), the
+    // block-table entry of the sequence (those of this CTA's keys are checked below), the
     // query rows.  Lcap = max_pages * P keys: a context past Lcap - k is
     // clamped and flagged.
     int ctx = __ldg(a.ctx_lens + b);
